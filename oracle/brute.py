@@ -1,0 +1,107 @@
+"""Pure-Python fp64 brute force for tiny inputs -- TEST INFRASTRUCTURE ONLY.
+
+A second, independent statement of the computation, written in the order of
+"paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2 implementation":
+per sequence, gather the keys and values block by block through the block table
+(key blocks [kv_heads, d/x, block, x] permuted to [block, kv_heads, d], value
+blocks [kv_heads, d, block] permuted to [block, kv_heads, d]), expand the kv
+heads to query heads (repeat_interleave), then for each 512-token partition form
+the scores, the partition max, the exponential sum and the weighted value sum,
+and finally merge the partitions with the log-sum-exp reduce of Phase 2.
+Plain Python loops over Python floats; numpy only decodes storage types.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def _decode(a: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _gather(w, s):
+    """keys[t][kvh][d], values[t][kvh][d] for sequence s (Python lists)."""
+    kc = _decode(w.key_cache, w.dtype)
+    vc = _decode(w.value_cache, w.dtype)
+    bs, d, hkv = w.block_size, w.head_size, w.num_kv_heads
+    L = int(w.seq_lens[s])
+    nblk = (L + bs - 1) // bs
+    keys, values = [], []
+    for b in range(nblk):
+        phys = int(w.block_tables[s][b])
+        n_tok = min(bs, L - b * bs)
+        for o in range(n_tok):
+            krow, vrow = [], []
+            for h in range(hkv):
+                if w.layout == "split":
+                    x = kc.shape[-1]
+                    krow.append([float(kc[phys, h, dd // x, o, dd % x]) for dd in range(d)])
+                    vrow.append([float(vc[phys, h, dd, o]) for dd in range(d)])
+                else:
+                    krow.append([float(kc[phys, h, o, dd]) for dd in range(d)])
+                    vrow.append([float(vc[phys, h, o, dd]) for dd in range(d)])
+            keys.append(krow)
+            values.append(vrow)
+    return keys, values
+
+
+def brute_decode(w, partition_size: int = 512):
+    """Returns dict(out, max_logits, exp_sums, tmp_out) as nested Python lists.
+
+    out[s][h][d] is the Phase 2 reduce of the partitions; max_logits/exp_sums
+    are [s][h][p] for the sequence's own partitions (unused ones are -inf / 0),
+    tmp_out[s][h][p][d] the normalised partition outputs.
+    """
+    S, H, d = w.num_seqs, w.num_heads, w.head_size
+    group = H // w.num_kv_heads
+    q_all = _decode(w.query, w.dtype)
+    P_max = max(1, -(-int(w.max_seq_len) // partition_size))
+    out = [[[0.0] * d for _ in range(H)] for _ in range(S)]
+    ml = [[[-math.inf] * P_max for _ in range(H)] for _ in range(S)]
+    es = [[[0.0] * P_max for _ in range(H)] for _ in range(S)]
+    tmp = [[[[0.0] * d for _ in range(P_max)] for _ in range(H)] for _ in range(S)]
+    for s in range(S):
+        L = int(w.seq_lens[s])
+        if L == 0:
+            continue
+        keys, values = _gather(w, s)
+        n_parts = (L + partition_size - 1) // partition_size
+        for h in range(H):
+            kvh = h // group            # repeat_interleave of kv heads
+            q = [float(v) for v in q_all[s, h]]
+            slope = None if w.alibi_slopes is None else float(w.alibi_slopes[h])
+            part_max, part_sum, part_out = [], [], []
+            for p in range(n_parts):
+                start, end = p * partition_size, min((p + 1) * partition_size, L)
+                scores = []
+                for t in range(start, end):
+                    z = w.scale * sum(q[i] * keys[t][kvh][i] for i in range(d))
+                    if w.softcap > 0:
+                        z = w.softcap * math.tanh(z / w.softcap)
+                    if slope is not None:
+                        z += slope * t
+                    scores.append(z)
+                m = max(scores)
+                ex = [math.exp(z - m) for z in scores]
+                ssum = sum(ex)
+                acc = [0.0] * d
+                for j, t in enumerate(range(start, end)):
+                    for i in range(d):
+                        acc[i] += ex[j] * values[t][kvh][i]
+                acc = [a / ssum for a in acc]
+                part_max.append(m)
+                part_sum.append(ssum)
+                part_out.append(acc)
+                ml[s][h][p] = m
+                es[s][h][p] = ssum
+                tmp[s][h][p] = acc
+            gmax = max(part_max)
+            resc = [math.exp(m - gmax) * e for m, e in zip(part_max, part_sum)]
+            total = sum(resc)
+            out[s][h] = [sum(resc[p] * part_out[p][i] for p in range(n_parts)) / total
+                         for i in range(d)]
+    return {"out": out, "max_logits": ml, "exp_sums": es, "tmp_out": tmp}

@@ -1,0 +1,305 @@
+/*
+ * pa_oracle.c -- plain fp64 CPU oracle for single-token decode attention over a
+ * paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may build, load or call this code.
+ * It shares no code, header, table or helper with the CUDA library; the two
+ * meet only through the seeded input generator, which holds no arithmetic of
+ * the method.
+ *
+ * What it computes (sources are the page titles and sections they come from):
+ *
+ *  - "paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2
+ *    implementation", block gather loop: logical token t of sequence s lives in
+ *    physical block block_tables[s][t / block_size] at slot t % block_size;
+ *    only ceil(seq_len / block_size) table entries are read.
+ *  - same page, key/value cache shape comments: split key layout
+ *    [num_blocks][num_kv_heads][head_size/x][block_size][x] with
+ *    x = 16 / element_size, value layout [num_blocks][num_kv_heads][head_size]
+ *    [block_size].
+ *  - "ex_engine/factors/attn_dispatch.py", dispatch_decode signature: NHD
+ *    layout [num_blocks][num_kv_heads][block_size][head_dim] for both caches.
+ *  - GQA expansion (repeat_interleave): query head h reads kv head
+ *    h / (num_heads / num_kv_heads).
+ *  - Phase 1: logits z = scale * q.k (then softcap, then ALiBi
+ *    slope[h] * absolute position), per 512-token partition: m_p = max z,
+ *    e_p = sum exp(z - m_p), tmp_p = sum exp(z - m_p) v / e_p.
+ *  - Phase 2 (log-sum-exp reduce): M = max m_p, r_p = exp(m_p - M) e_p,
+ *    out = sum r_p tmp_p / sum r_p, stated on the page to equal the full
+ *    softmax -- so the dense result out = sum exp(z - Z) v / sum exp(z - Z)
+ *    is computed independently and both are returned.
+ *  - Unused partitions (p >= ceil(seq_len/512)): m = -inf, e = 0, tmp = 0.
+ *
+ * Readings where the pages are silent or inconsistent (each is listed in
+ * the design doc as well):
+ *  - tmp_p is stored normalised by e_p (the reduce on the page is only equal
+ *    to a full softmax with that reading).
+ *  - softcap (the `softcap` field of AttnDispatchConfig, formula not printed):
+ *    z = cap * tanh(z / cap), applied to the scaled logit, before ALiBi;
+ *    cap <= 0 means off.
+ *  - seq_len == 0: output row is zero, all partitions unused.
+ *
+ * All arithmetic is in double; inputs are decoded exactly from their storage
+ * type (fp32, IEEE binary16, bfloat16).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "pa_oracle.h"
+
+/* ---- exact decoding of the storage types into double ------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);     /* (1.f) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void* base, int64_t idx, int dtype) {
+    switch (dtype) {
+    case ORACLE_F32: return (double)((const float*)base)[idx];
+    case ORACLE_F16: return half_bits_to_double(((const uint16_t*)base)[idx]);
+    case ORACLE_BF16: return bf16_bits_to_double(((const uint16_t*)base)[idx]);
+    default: return NAN;
+    }
+}
+
+static int elem_bytes(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+
+/* ---- page addressing ----------------------------------------------------- */
+
+/* Element index of K[token slot o][dim d] inside physical block `blk`,
+ * kv head `kvh`. */
+static int64_t key_index(const oracle_args* a, int64_t blk, int kvh, int o, int d) {
+    int64_t base = (blk * a->num_kv_heads + kvh) * (int64_t)a->head_size * a->block_size;
+    if (a->layout == ORACLE_LAYOUT_SPLIT) {
+        int x = 16 / elem_bytes(a->dtype);
+        /* [head_size/x][block_size][x] */
+        return base + ((int64_t)(d / x) * a->block_size + o) * x + (d % x);
+    }
+    /* NHD: [block_size][head_size] */
+    return base + (int64_t)o * a->head_size + d;
+}
+
+static int64_t value_index(const oracle_args* a, int64_t blk, int kvh, int o, int d) {
+    int64_t base = (blk * a->num_kv_heads + kvh) * (int64_t)a->head_size * a->block_size;
+    if (a->layout == ORACLE_LAYOUT_SPLIT) {
+        /* [head_size][block_size] */
+        return base + (int64_t)d * a->block_size + o;
+    }
+    return base + (int64_t)o * a->head_size + d;
+}
+
+/* ---- one (sequence, head) --------------------------------------------- */
+
+typedef struct {
+    double* z;       /* logits, length seq_len */
+    double* vrow;    /* one value row, length head_size */
+} scratch_t;
+
+static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
+    const int d_sz = a->head_size;
+    const int group = a->num_heads / a->num_kv_heads;
+    const int kvh = h / group;
+    const int len = a->seq_lens[s];
+    const int P_max = a->max_num_partitions;
+    const int PS = a->partition_size;
+    const int32_t* table = a->block_tables + (int64_t)s * a->max_blocks_per_seq;
+    const int64_t qoff = ((int64_t)s * a->num_heads + h) * d_sz;
+    double* out = a->out + qoff;
+    double* out_v2 = a->out_v2 ? a->out_v2 + qoff : NULL;
+    const int64_t stat_off = ((int64_t)s * a->num_heads + h) * P_max;
+    const int num_parts = (len + PS - 1) / PS;
+
+    /* unused partitions */
+    for (int p = num_parts; p < P_max; ++p) {
+        if (a->max_logits) a->max_logits[stat_off + p] = -INFINITY;
+        if (a->exp_sums) a->exp_sums[stat_off + p] = 0.0;
+        if (a->tmp_out)
+            for (int d = 0; d < d_sz; ++d) a->tmp_out[(stat_off + p) * d_sz + d] = 0.0;
+    }
+    if (len <= 0) {
+        for (int d = 0; d < d_sz; ++d) out[d] = 0.0;
+        if (out_v2) for (int d = 0; d < d_sz; ++d) out_v2[d] = 0.0;
+        return;
+    }
+
+    /* logits */
+    double Z = -INFINITY;
+    for (int t = 0; t < len; ++t) {
+        int64_t blk = table[t / a->block_size];
+        int o = t % a->block_size;
+        double dot = 0.0;
+        for (int d = 0; d < d_sz; ++d)
+            dot += load_elem(a->query, qoff + d, a->dtype) *
+                   load_elem(a->key_cache, key_index(a, blk, kvh, o, d), a->dtype);
+        double z = a->scale * dot;
+        if (a->softcap > 0.0) z = a->softcap * tanh(z / a->softcap);
+        if (a->alibi_slopes) z += (double)a->alibi_slopes[h] * (double)t;
+        sc->z[t] = z;
+        if (z > Z) Z = z;
+    }
+
+    /* dense softmax-weighted sum of V */
+    double denom = 0.0;
+    for (int d = 0; d < d_sz; ++d) out[d] = 0.0;
+    for (int t = 0; t < len; ++t) {
+        int64_t blk = table[t / a->block_size];
+        int o = t % a->block_size;
+        double w = exp(sc->z[t] - Z);
+        denom += w;
+        for (int d = 0; d < d_sz; ++d)
+            out[d] += w * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), a->dtype);
+    }
+    for (int d = 0; d < d_sz; ++d) out[d] /= denom;
+
+    if (!(a->max_logits || a->exp_sums || a->tmp_out || out_v2)) return;
+
+    /* per-partition statistics (Phase 1) and the oracle's own reduce (Phase 2) */
+    double M = -INFINITY;
+    for (int p = 0; p < num_parts; ++p) {
+        int t0 = p * PS, t1 = t0 + PS < len ? t0 + PS : len;
+        double m = -INFINITY;
+        for (int t = t0; t < t1; ++t) if (sc->z[t] > m) m = sc->z[t];
+        if (m > M) M = m;
+    }
+    double r_total = 0.0;
+    if (out_v2) for (int d = 0; d < d_sz; ++d) out_v2[d] = 0.0;
+    for (int p = 0; p < num_parts; ++p) {
+        int t0 = p * PS, t1 = t0 + PS < len ? t0 + PS : len;
+        double m = -INFINITY;
+        for (int t = t0; t < t1; ++t) if (sc->z[t] > m) m = sc->z[t];
+        double e = 0.0;
+        for (int d = 0; d < d_sz; ++d) sc->vrow[d] = 0.0;
+        for (int t = t0; t < t1; ++t) {
+            int64_t blk = table[t / a->block_size];
+            int o = t % a->block_size;
+            double w = exp(sc->z[t] - m);
+            e += w;
+            for (int d = 0; d < d_sz; ++d)
+                sc->vrow[d] += w * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), a->dtype);
+        }
+        for (int d = 0; d < d_sz; ++d) sc->vrow[d] /= e;      /* tmp_p, normalised */
+        if (a->max_logits) a->max_logits[stat_off + p] = m;
+        if (a->exp_sums) a->exp_sums[stat_off + p] = e;
+        if (a->tmp_out)
+            for (int d = 0; d < d_sz; ++d) a->tmp_out[(stat_off + p) * d_sz + d] = sc->vrow[d];
+        double r = exp(m - M) * e;
+        r_total += r;
+        if (out_v2) for (int d = 0; d < d_sz; ++d) out_v2[d] += r * sc->vrow[d];
+    }
+    if (out_v2) for (int d = 0; d < d_sz; ++d) out_v2[d] /= r_total;
+}
+
+/* ---- threading over the selected (sequence, head) pairs ----------------- */
+
+typedef struct {
+    const oracle_args* a;
+    int64_t n_items;
+    int64_t next;
+    pthread_mutex_t lock;
+    int max_len;
+    int failed;
+} pool_t;
+
+static void* worker(void* arg) {
+    pool_t* pool = (pool_t*)arg;
+    const oracle_args* a = pool->a;
+    scratch_t sc;
+    sc.z = (double*)malloc(sizeof(double) * (size_t)(pool->max_len > 0 ? pool->max_len : 1));
+    sc.vrow = (double*)malloc(sizeof(double) * (size_t)a->head_size);
+    if (!sc.z || !sc.vrow) {
+        pthread_mutex_lock(&pool->lock);
+        pool->failed = 1;
+        pthread_mutex_unlock(&pool->lock);
+        free(sc.z); free(sc.vrow);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&pool->lock);
+        int64_t i = pool->next++;
+        pthread_mutex_unlock(&pool->lock);
+        if (i >= pool->n_items) break;
+        int si = (int)(i / a->num_heads);
+        int h = (int)(i % a->num_heads);
+        int s = a->seq_subset ? a->seq_subset[si] : si;
+        compute_head(a, s, h, &sc);
+    }
+    free(sc.z);
+    free(sc.vrow);
+    return NULL;
+}
+
+int oracle_decode(const oracle_args* a) {
+    if (!a || !a->query || !a->key_cache || !a->value_cache || !a->block_tables ||
+        !a->seq_lens || !a->out)
+        return ORACLE_ERR_ARG;
+    if (a->num_heads <= 0 || a->num_kv_heads <= 0 || a->num_heads % a->num_kv_heads)
+        return ORACLE_ERR_ARG;
+    if (a->head_size <= 0 || a->block_size <= 0 || a->partition_size <= 0)
+        return ORACLE_ERR_ARG;
+    if (a->dtype != ORACLE_F32 && a->dtype != ORACLE_F16 && a->dtype != ORACLE_BF16)
+        return ORACLE_ERR_ARG;
+    if (a->layout == ORACLE_LAYOUT_SPLIT && a->head_size % (16 / elem_bytes(a->dtype)))
+        return ORACLE_ERR_ARG;
+    int n_seq = a->seq_subset ? a->n_subset : a->num_seqs;
+    int max_len = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        int s = a->seq_subset ? a->seq_subset[i] : i;
+        if (s < 0 || s >= a->num_seqs) return ORACLE_ERR_ARG;
+        int len = a->seq_lens[s];
+        if (len < 0) return ORACLE_ERR_ARG;
+        if ((len + a->block_size - 1) / a->block_size > a->max_blocks_per_seq) return ORACLE_ERR_ARG;
+        if ((len + a->partition_size - 1) / a->partition_size > a->max_num_partitions &&
+            (a->max_logits || a->exp_sums || a->tmp_out))
+            return ORACLE_ERR_ARG;
+        int nb = (len + a->block_size - 1) / a->block_size;
+        const int32_t* table = a->block_tables + (int64_t)s * a->max_blocks_per_seq;
+        for (int b = 0; b < nb; ++b)
+            if (table[b] < 0 || table[b] >= a->num_blocks) return ORACLE_ERR_ARG;
+        if (len > max_len) max_len = len;
+    }
+    pool_t pool;
+    pool.a = a;
+    pool.n_items = (int64_t)n_seq * a->num_heads;
+    pool.next = 0;
+    pool.max_len = max_len;
+    pool.failed = 0;
+    pthread_mutex_init(&pool.lock, NULL);
+    int nt = a->num_threads > 0 ? a->num_threads : 1;
+    if (nt > 256) nt = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 0; i < nt; ++i) {
+        if (pthread_create(&th[i], NULL, worker, &pool) != 0) break;
+        ++started;
+    }
+    if (started == 0) worker(&pool);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&pool.lock);
+    return pool.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+int oracle_abi_version(void) { return ORACLE_ABI_VERSION; }

@@ -1,0 +1,295 @@
+"""Seeded synthetic inputs for paged-KV decode attention.
+
+This module is the one piece shared by the CUDA path's tests/bench and by the
+fp64 oracle: it draws the query, the paged K/V pool, the block tables and the
+sequence lengths, rounds them to the storage dtype and lays them out.  It holds
+none of the attention arithmetic.
+
+Workloads (sizes from the paged_attention_v2 problem statement of
+"paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2 implementation"
+and the AttnDispatchConfig defaults of "ex_engine/factors/attn_dispatch.py"):
+
+  tiny         2 seqs, lens {37, 600}, 4 heads / 2 kv heads, d=64, fp32
+  gqa4k        32 x 4096, 28 / 4 heads, d=128, fp16
+  long100k     4 x 100000 (196 partitions of 512), 28 / 4 heads, d=128, bf16
+  ragged       256 seqs, lens log-uniform in [1, 32768], 32 / 8 heads, d=128,
+               fp16, ALiBi slopes 2^(-8(i+1)/32)
+  large_batch  128 x 16384, 64 / 8 heads, d=128, bf16 with Q/K/V scaled x2,
+               logit softcap 30
+
+Recipe: numpy PCG64 streams keyed by (seed, stream name, chunk); values are
+N(0,1) fp32 draws (times the workload's multiplier), rounded to the storage
+dtype with round-to-nearest-even.  Physical blocks are assigned to sequences
+through a seeded permutation of the pool.  Pool blocks that no sequence uses
+and the unused slots of each sequence's last block are filled with NaN, and
+unused block-table entries point at a NaN block, so that any read past the
+valid tokens shows up in the output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+BLOCK_SIZE = 16
+PARTITION_SIZE = 512
+
+DTYPES = ("f32", "f16", "bf16")
+LAYOUTS = ("split", "nhd")
+
+# storage numpy dtype per dtype name (bf16 is carried as raw uint16 bits)
+_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+_ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+
+# blocks generated per RNG chunk; fixed so values do not depend on memory limits
+_CHUNK_BLOCKS = 512
+
+
+@dataclass
+class Spec:
+    name: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    dtype: str
+    seq_lens: Optional[list] = None       # explicit lengths
+    seq_len: Optional[int] = None         # uniform length
+    log_uniform_max: Optional[int] = None # lens = clamp(round(2^(log2(max) u)), 1, max)
+    block_size: int = BLOCK_SIZE
+    pool_blocks: Optional[int] = None     # None: exactly the blocks in use (+1 NaN block if needed)
+    value_mult: float = 1.0
+    alibi: bool = False
+    softcap: float = 0.0
+    seed_index: int = 0
+    poison: bool = True
+
+
+SPECS = {
+    "tiny": Spec("tiny", 2, 4, 2, 64, "f32", seq_lens=[37, 600], pool_blocks=64, seed_index=0),
+    "gqa4k": Spec("gqa4k", 32, 28, 4, 128, "f16", seq_len=4096, seed_index=1),
+    "long100k": Spec("long100k", 4, 28, 4, 128, "bf16", seq_len=100000, seed_index=2),
+    "ragged": Spec("ragged", 256, 32, 8, 128, "f16", log_uniform_max=32768, alibi=True,
+                   seed_index=3),
+    "large_batch": Spec("large_batch", 128, 64, 8, 128, "bf16", seq_len=16384, value_mult=2.0,
+                        softcap=30.0, seed_index=4),
+}
+
+DESCRIPTIONS = {
+    "tiny": "2 seqs, lens {37,600}, 4/2 heads, d=64, fp32, pool 64 blocks (NaN-poisoned spares)",
+    "gqa4k": "GQA decode: 32 seqs x 4096, 28/4 heads, d=128, block 16, fp16",
+    "long100k": "long context: 4 seqs x 100000 (196 partitions), 28/4 heads, d=128, block 16, bf16",
+    "ragged": "ragged batch: 256 seqs, lens log-uniform [1,32768], 32/8 heads, d=128, fp16, ALiBi",
+    "large_batch": "large batch: 128 seqs x 16384, 64/8 heads, d=128, bf16 (x2), softcap 30",
+}
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str
+    layout: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    max_seq_len: int
+    scale: float
+    softcap: float
+    query: np.ndarray
+    key_cache: np.ndarray
+    value_cache: np.ndarray
+    block_tables: np.ndarray
+    seq_lens: np.ndarray
+    alibi_slopes: Optional[np.ndarray]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def elem_bytes(self) -> int:
+        return _ELEM_BYTES[self.dtype]
+
+    @property
+    def max_num_partitions(self) -> int:
+        return max(1, -(-self.max_seq_len // PARTITION_SIZE))
+
+    @property
+    def kv_bytes(self) -> int:
+        """Bytes of K and V the method must read: sum_s len_s * kv_heads * d * 2 * elem."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * \
+            self.head_size * 2 * self.elem_bytes
+
+
+# ---------------------------------------------------------------- rounding
+
+def round_to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round fp32 values to the storage dtype (round-to-nearest-even)."""
+    x = np.asarray(x, dtype=np.float32)
+    if dtype == "f32":
+        return x.copy()
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        u = x.view(np.uint32).astype(np.uint64)
+        r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+        return r.astype(np.uint16)
+    raise ValueError(dtype)
+
+
+def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of storage values to float64 (for tests)."""
+    if dtype in ("f32", "f16"):
+        return a.astype(np.float64)
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def _nan_value(dtype: str):
+    if dtype == "f32":
+        return np.float32(np.nan)
+    if dtype == "f16":
+        return np.uint16(_NAN_BITS["f16"]).view(np.float16)
+    return np.uint16(_NAN_BITS["bf16"])
+
+
+def _rng(seed: int, stream: str, chunk: int = 0) -> np.random.Generator:
+    key = [seed, sum(ord(c) * 131 ** i for i, c in enumerate(stream)) % (2 ** 31), chunk]
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(key)))
+
+
+# ---------------------------------------------------------------- layouts
+
+def logical_to_layout(kv: np.ndarray, which: str, layout: str, dtype: str) -> np.ndarray:
+    """kv: logical [blocks, kv_heads, block_size, d] -> storage layout.
+
+    split key   : [blocks, kv_heads, d/x, block_size, x], x = 16 / elem_bytes
+    split value : [blocks, kv_heads, d, block_size]
+    nhd         : [blocks, kv_heads, block_size, d]
+    """
+    nb, hkv, bs, d = kv.shape
+    if layout == "nhd":
+        return np.ascontiguousarray(kv)
+    if which == "k":
+        x = 16 // _ELEM_BYTES[dtype]
+        return np.ascontiguousarray(kv.reshape(nb, hkv, bs, d // x, x).transpose(0, 1, 3, 2, 4))
+    return np.ascontiguousarray(kv.transpose(0, 1, 3, 2))
+
+
+def layout_shape(which: str, layout: str, dtype: str, nb: int, hkv: int, bs: int, d: int):
+    if layout == "nhd":
+        return (nb, hkv, bs, d)
+    if which == "k":
+        x = 16 // _ELEM_BYTES[dtype]
+        return (nb, hkv, d // x, bs, x)
+    return (nb, hkv, d, bs)
+
+
+# ---------------------------------------------------------------- generation
+
+def _seq_lens(spec: Spec, seed: int) -> np.ndarray:
+    if spec.seq_lens is not None:
+        return np.asarray(spec.seq_lens, dtype=np.int32)
+    if spec.seq_len is not None:
+        return np.full(spec.num_seqs, spec.seq_len, dtype=np.int32)
+    u = _rng(seed, "lens").random(spec.num_seqs)
+    top = math.log2(spec.log_uniform_max)
+    lens = np.clip(np.rint(np.exp2(top * u)), 1, spec.log_uniform_max)
+    return lens.astype(np.int32)
+
+
+def alibi_slopes(num_heads: int) -> np.ndarray:
+    """ALiBi slopes 2^(-8(i+1)/num_heads), fp32."""
+    i = np.arange(num_heads, dtype=np.float64)
+    return np.exp2(-8.0 * (i + 1) / num_heads).astype(np.float32)
+
+
+def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
+                  shuffle_seed: Optional[int] = None) -> Workload:
+    """Build a workload from a Spec or the name of one in SPECS."""
+    if isinstance(spec, str):
+        spec = SPECS[spec]
+    assert layout in LAYOUTS and spec.dtype in DTYPES
+    seed = 1234 + spec.seed_index if seed is None else seed
+    shuffle_seed = 99 + spec.seed_index if shuffle_seed is None else shuffle_seed
+    bs, d, hkv = spec.block_size, spec.head_size, spec.num_kv_heads
+    lens = _seq_lens(spec, seed)
+    max_seq_len = int(lens.max()) if len(lens) else 0
+    max_blocks = max(1, -(-max_seq_len // bs))
+    blocks_per_seq = (lens.astype(np.int64) + bs - 1) // bs
+    used = int(blocks_per_seq.sum())
+    need_spare = spec.poison and bool((blocks_per_seq < max_blocks).any())
+    if spec.pool_blocks is not None:
+        pool = spec.pool_blocks
+        assert pool >= used + (1 if need_spare else 0), "pool too small"
+    else:
+        pool = used + (1 if need_spare else 0)
+    perm = _rng(shuffle_seed, "perm").permutation(pool).astype(np.int32)
+    assigned, spares = perm[:used], perm[used:]
+    tables = np.empty((spec.num_seqs, max_blocks), dtype=np.int32)
+    fill = int(spares[0]) if len(spares) else 0
+    tables[:] = fill
+    # valid slots per physical block (0 = block no sequence uses)
+    valid_slots = np.zeros(pool, dtype=np.int32)
+    off = 0
+    for s in range(spec.num_seqs):
+        nb = int(blocks_per_seq[s])
+        tables[s, :nb] = assigned[off:off + nb]
+        if nb:
+            valid_slots[assigned[off:off + nb]] = bs
+            tail = int(lens[s]) - (nb - 1) * bs
+            valid_slots[assigned[off + nb - 1]] = tail
+        off += nb
+
+    sdt = _STORAGE[spec.dtype]
+    kshape = layout_shape("k", layout, spec.dtype, pool, hkv, bs, d)
+    vshape = layout_shape("v", layout, spec.dtype, pool, hkv, bs, d)
+    key_cache = np.empty(kshape, dtype=sdt)
+    value_cache = np.empty(vshape, dtype=sdt)
+    nan = _nan_value(spec.dtype)
+    for c0 in range(0, pool, _CHUNK_BLOCKS):
+        c1 = min(pool, c0 + _CHUNK_BLOCKS)
+        n = c1 - c0
+        for which, dst in (("k", key_cache), ("v", value_cache)):
+            g = _rng(seed, "kv_" + which, c0 // _CHUNK_BLOCKS)
+            x = g.standard_normal((n, hkv, bs, d), dtype=np.float32)
+            if spec.value_mult != 1.0:
+                x *= np.float32(spec.value_mult)
+            st = round_to_storage(x, spec.dtype)
+            if spec.poison:
+                vs = valid_slots[c0:c1]
+                slot = np.arange(bs)[None, :]
+                bad = slot >= vs[:, None]                     # [n, bs]
+                if bad.any():
+                    st[np.broadcast_to(bad[:, None, :, None], st.shape)] = nan
+            dst[c0:c1] = logical_to_layout(st, which, layout, spec.dtype)
+    q = _rng(seed, "query").standard_normal((spec.num_seqs, spec.num_heads, d), dtype=np.float32)
+    if spec.value_mult != 1.0:
+        q *= np.float32(spec.value_mult)
+    query = round_to_storage(q, spec.dtype)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    return Workload(
+        name=spec.name, dtype=spec.dtype, layout=layout, num_seqs=spec.num_seqs,
+        num_heads=spec.num_heads, num_kv_heads=hkv, head_size=d, block_size=bs,
+        num_blocks=pool, max_blocks_per_seq=max_blocks, max_seq_len=max_seq_len,
+        scale=scale, softcap=float(spec.softcap), query=query, key_cache=key_cache,
+        value_cache=value_cache, block_tables=tables, seq_lens=lens,
+        alibi_slopes=alibi_slopes(spec.num_heads) if spec.alibi else None,
+        meta={"seed": seed, "shuffle_seed": shuffle_seed, "spec": spec},
+    )
+
+
+def small_spec(name="small", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
+               dtype="f16", seq_lens=(1, 513, 1100), alibi=False, softcap=0.0,
+               value_mult=1.0, pool_extra=5, seed_index=7, block_size=BLOCK_SIZE) -> Spec:
+    """A Spec for tests: explicit lengths, a pool with NaN-poisoned spare blocks."""
+    lens = list(seq_lens)
+    used = sum(-(-l // block_size) for l in lens)
+    return Spec(name, num_seqs, num_heads, num_kv_heads, head_size, dtype,
+                seq_lens=lens, pool_blocks=used + pool_extra, alibi=alibi, softcap=softcap,
+                value_mult=value_mult, seed_index=seed_index, block_size=block_size)
