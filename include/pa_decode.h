@@ -1,0 +1,174 @@
+/*
+ * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-KV decode attention library.
+ *
+ * One query token per sequence attends over that sequence's keys and values,
+ * which live in fixed-size pages ("blocks") of a shared cache and are found
+ * through a per-sequence block table.  The operation is the one of
+ * "paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2 implementation"
+ * (function paged_attention_v2_pytorch, Phase 1 per-partition attention and
+ * Phase 2 log-sum-exp reduce), with the NHD cache layout and the `softcap`
+ * field of "ex_engine/factors/attn_dispatch.py" (AttnDispatchConfig,
+ * dispatch_decode).
+ *
+ * For sequence s, query head h (kv head g = h / (num_heads / num_kv_heads))
+ * and token t < seq_lens[s]:
+ *     z_t = scale * <query[s][h], K_g(t)>
+ *     z_t = softcap * tanh(z_t / softcap)          if softcap > 0
+ *     z_t = z_t + alibi_slopes[h] * t              if alibi_slopes != NULL
+ *     out[s][h] = sum_t exp(z_t - max z) V_g(t) / sum_t exp(z_t - max z)
+ * K_g(t) is read from physical block block_tables[s][t / block_size] at slot
+ * t % block_size.  Sequences are cut into partitions of PA_PARTITION_SIZE
+ * tokens; for partition p (tokens [512p, min(512p+512, seq_len))):
+ *     max_logits[s][h][p] = max z_t
+ *     exp_sums[s][h][p]   = sum exp(z_t - max_logits[s][h][p])
+ *     tmp_out[s][h][p][:] = sum exp(z_t - max_logits) V(t) / exp_sums[s][h][p]
+ * and the output is their log-sum-exp merge (equal to the dense softmax).
+ *
+ * Conventions for every entry point below:
+ *  - All tensor pointers are DEVICE pointers (global memory of the current
+ *    device), caller-owned and caller-allocated; the library allocates no
+ *    device memory and keeps no state except per-device cached attributes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on that stream and never synchronise the host.
+ *  - Errors the host can see are returned before anything is launched.
+ *    Data-dependent errors are reported through the optional device word
+ *    `dev_error` (bit flags PA_DEVERR_*), set with atomicOr; the kernels
+ *    clamp the offending value and continue, they never trap.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tokens per partition (module constant _PARTITION_SIZE of
+ * paged_attention_v2_pytorch.py). */
+#define PA_PARTITION_SIZE 512
+
+/* Tokens per cache page supported by this build. */
+#define PA_BLOCK_SIZE 16
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer     */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_size, block_size ... */
+    PA_ERR_WORKSPACE = 3,     /* v2 selected but exp_sums/max_logits/tmp_out NULL */
+    PA_ERR_LAUNCH = 4,        /* CUDA reported an error while launching         */
+    PA_ERR_DEVICE_CHECK = 5,  /* reserved for callers mapping dev_error bits    */
+    PA_ERR_DEVICE_TIMEOUT = 6 /* reserved for callers mapping dev_error bits    */
+} pa_status;
+
+/* Storage type of query, key_cache, value_cache and out (one type for all). */
+typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_F16 = 1, PA_DTYPE_BF16 = 2 } pa_dtype;
+
+/*
+ * Cache layouts.
+ *  PA_LAYOUT_SPLIT: key_cache   [num_blocks][num_kv_heads][head_size/x][block_size][x],
+ *                   x = 16 / sizeof(element) (8 for f16/bf16, 4 for f32);
+ *                   value_cache [num_blocks][num_kv_heads][head_size][block_size]
+ *                   (key_cache / value_cache shape comments of
+ *                   paged_attention_v2_pytorch.py).
+ *  PA_LAYOUT_NHD:   key_cache and value_cache [num_blocks][num_kv_heads][block_size][head_size]
+ *                   (dispatch_decode argument comments of attn_dispatch.py).
+ * All arrays are dense, row-major, without padding.
+ */
+typedef enum pa_layout { PA_LAYOUT_SPLIT = 0, PA_LAYOUT_NHD = 1 } pa_layout;
+
+/*
+ * PA_MODE_V2: partition kernel over (sequence, kv head, 512-token partition)
+ *             tiles, then the log-sum-exp reduce (needs the workspace).
+ * PA_MODE_V1: one pass per (sequence, kv head) over the whole sequence that
+ *             writes `out` directly (no workspace, no statistics).
+ * PA_MODE_AUTO: the library picks (pa_choose_mode).
+ */
+typedef enum pa_mode { PA_MODE_AUTO = 0, PA_MODE_V1 = 1, PA_MODE_V2 = 2 } pa_mode;
+
+/* dev_error bits */
+#define PA_DEVERR_BLOCK_ID   1  /* a block table entry outside [0, num_blocks); page 0 read instead */
+#define PA_DEVERR_SEQ_LEN    2  /* seq_lens[s] < 0 or > max_seq_len; clamped into [0, max_seq_len] */
+#define PA_DEVERR_TIMEOUT    4  /* an internal pipeline wait exceeded its limit; results invalid   */
+
+typedef struct pa_decode_args {
+    /* [num_seqs][num_heads][head_size], dtype; written.  16-byte aligned. */
+    void* out;
+    /* [num_seqs][num_heads][head_size], dtype.  16-byte aligned. */
+    const void* query;
+    /* layout-dependent, see pa_layout; 16-byte aligned. */
+    const void* key_cache;
+    const void* value_cache;
+    /* [num_seqs][max_blocks_per_seq] int32 physical block ids; only the first
+     * ceil(seq_lens[s] / block_size) entries of row s are read. */
+    const int32_t* block_tables;
+    /* [num_seqs] int32 tokens per sequence, each in [0, max_seq_len]. */
+    const int32_t* seq_lens;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_kv_heads;        /* num_heads % num_kv_heads == 0, group <= 16 */
+    int32_t head_size;           /* 64 or 128 */
+    int32_t num_blocks;          /* pages in each cache */
+    int32_t block_size;          /* must be PA_BLOCK_SIZE */
+    int32_t max_seq_len;         /* upper bound of seq_lens; sets max_num_partitions */
+    int32_t max_blocks_per_seq;  /* row stride of block_tables, >= ceil(max_seq_len/block_size) */
+    float scale;                 /* logit scale, e.g. 1/sqrt(head_size) */
+    float softcap;               /* > 0: z = softcap * tanh(z / softcap); <= 0: off */
+    /* [num_heads] fp32 ALiBi slopes, or NULL. */
+    const float* alibi_slopes;
+    int32_t dtype;               /* pa_dtype */
+    int32_t layout;              /* pa_layout */
+    int32_t mode;                /* pa_mode */
+    /* Workspace (required for v2, ignored by v1); P = pa_max_num_partitions(max_seq_len):
+     *   exp_sums, max_logits [num_seqs][num_heads][P] fp32,
+     *   tmp_out [num_seqs][num_heads][P][head_size] fp32 (16-byte aligned).
+     * After a v2 call they hold the Phase 1 statistics of every partition
+     * p < ceil(seq_lens[s]/512); for p beyond that max_logits = -inf and
+     * exp_sums = 0, tmp_out is left unspecified. */
+    float* exp_sums;
+    float* max_logits;
+    float* tmp_out;
+    /* Optional device int32 receiving PA_DEVERR_* bits (never cleared by the library). */
+    int32_t* dev_error;
+    /* Optional cudaEvent_t (as void*) recorded on `stream` immediately before and
+     * after the main (partition or v1) kernel, for timing; NULL = none. */
+    void* event_main_begin;
+    void* event_main_end;
+} pa_decode_args;
+
+/*
+ * Paged decode attention (the whole operation: partition kernel + reduce for
+ * v2, or the single v1 pass).  Returns PA_OK once the work is enqueued.
+ * num_seqs == 0 is a no-op.
+ */
+pa_status pa_decode(const pa_decode_args* args, void* stream);
+
+/* ceil(max_seq_len / PA_PARTITION_SIZE), at least 1 (workspace partition stride). */
+int32_t pa_max_num_partitions(int32_t max_seq_len);
+
+/* Element counts of the v2 workspace: *stats_elems for each of exp_sums and
+ * max_logits, *tmp_elems for tmp_out.  Returns PA_ERR_INVALID_ARG on bad sizes. */
+pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                             int32_t max_seq_len, int64_t* stats_elems, int64_t* tmp_elems);
+
+/*
+ * v1 / v2 choice used by PA_MODE_AUTO, as a pure host function (sm_count is
+ * the device's multiprocessor count).  The pages decide by tiles against SMs
+ * (should_use_paged_v2 in attn_dispatch.py: v2 when num_kv_heads *
+ * ceil(seq_len/512) > 2 * SM_COUNT on a 16-SM part); this build retunes that
+ * rule for GB300, see pa_decode.cu.  Returns PA_MODE_V1 or PA_MODE_V2.
+ */
+int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                       int32_t sm_count);
+
+/* Static string for a pa_status value. */
+const char* pa_status_str(int32_t status);
+
+/* Library version, (major << 16) | minor. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_DECODE_H */

@@ -1,0 +1,120 @@
+"""Paged-KV decode attention for GB300 (sm_103a): Python binding of libpa_decode.so.
+
+This module only marshals torch tensors (device memory and the current CUDA
+stream) into the C ABI of include/pa_decode.h; every step of the computation
+runs in the library's CUDA kernels.  It raises if the library is missing.
+
+    out = torch.empty_like(query)
+    ws = alloc_workspace(num_seqs, num_heads, head_size, max_seq_len, query.device)
+    pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens,
+              num_kv_heads=..., scale=..., max_seq_len=..., layout="split", **ws)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _abi
+from ._abi import (PA_BLOCK_SIZE, PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT,
+                   PA_PARTITION_SIZE, LibraryMissing)
+
+__all__ = ["pa_decode", "alloc_workspace", "max_num_partitions", "choose_mode", "status_str",
+           "PaDecodeError", "PA_PARTITION_SIZE", "PA_BLOCK_SIZE", "PA_DEVERR_BLOCK_ID",
+           "PA_DEVERR_SEQ_LEN", "PA_DEVERR_TIMEOUT", "LibraryMissing", "library"]
+
+_LAYOUTS = {"split": _abi.PA_LAYOUT_SPLIT, "nhd": _abi.PA_LAYOUT_NHD}
+_MODES = {"auto": _abi.PA_MODE_AUTO, "v1": _abi.PA_MODE_V1, "v2": _abi.PA_MODE_V2}
+
+
+class PaDecodeError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(f"pa_decode failed: {status_str(status)} (status {status})")
+        self.status = status
+
+
+def library():
+    return _abi.load()
+
+
+def status_str(status: int) -> str:
+    return library().pa_status_str(int(status)).decode()
+
+
+def max_num_partitions(max_seq_len: int) -> int:
+    return int(library().pa_max_num_partitions(int(max_seq_len)))
+
+
+def choose_mode(num_seqs: int, num_kv_heads: int, max_seq_len: int, sm_count: int) -> str:
+    m = library().pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count)
+    return "v1" if m == _abi.PA_MODE_V1 else "v2"
+
+
+def _dtype_code(t):
+    import torch
+    return {torch.float32: _abi.PA_DTYPE_F32, torch.float16: _abi.PA_DTYPE_F16,
+            torch.bfloat16: _abi.PA_DTYPE_BF16}[t.dtype]
+
+
+def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device):
+    """torch-allocated v2 workspace: dict(exp_sums, max_logits, tmp_out)."""
+    import torch
+    P = max_num_partitions(max_seq_len)
+    return {
+        "exp_sums": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
+        "max_logits": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
+        "tmp_out": torch.empty((num_seqs, num_heads, P, head_size), dtype=torch.float32,
+                               device=device),
+    }
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num_kv_heads: int,
+              scale: float, max_seq_len: int, block_size: int = PA_BLOCK_SIZE,
+              alibi_slopes=None, softcap: float = 0.0, layout: str = "split", mode: str = "auto",
+              exp_sums=None, max_logits=None, tmp_out=None, dev_error=None,
+              event_begin=None, event_end=None) -> _abi.PaDecodeArgs:
+    """Build the C argument struct (no checks beyond shapes; the library validates)."""
+    num_seqs, num_heads, head_size = query.shape
+    num_blocks = key_cache.shape[0]
+    return _abi.PaDecodeArgs(
+        out=_ptr(out), query=_ptr(query), key_cache=_ptr(key_cache),
+        value_cache=_ptr(value_cache), block_tables=_ptr(block_tables), seq_lens=_ptr(seq_lens),
+        num_seqs=num_seqs, num_heads=num_heads, num_kv_heads=num_kv_heads, head_size=head_size,
+        num_blocks=num_blocks, block_size=block_size, max_seq_len=max_seq_len,
+        max_blocks_per_seq=block_tables.shape[1] if block_tables.dim() == 2 else 0,
+        scale=scale, softcap=softcap, alibi_slopes=_ptr(alibi_slopes), dtype=_dtype_code(query),
+        layout=_LAYOUTS[layout], mode=_MODES[mode], exp_sums=_ptr(exp_sums),
+        max_logits=_ptr(max_logits), tmp_out=_ptr(tmp_out), dev_error=_ptr(dev_error),
+        event_main_begin=None if event_begin is None else event_begin.cuda_event,
+        event_main_end=None if event_end is None else event_end.cuda_event,
+    )
+
+
+def pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens, *, stream=None,
+              **kw) -> None:
+    """Enqueue paged decode attention on `stream` (default: torch's current stream).
+
+    Tensors must be contiguous CUDA tensors: query/out [num_seqs, num_heads,
+    head_size] (fp32, fp16 or bf16), key_cache/value_cache in the split or NHD
+    layout, block_tables [num_seqs, max_blocks_per_seq] int32, seq_lens
+    [num_seqs] int32, optional alibi_slopes [num_heads] fp32, v2 workspace from
+    alloc_workspace().  Raises PaDecodeError with the library's status on failure.
+    """
+    import torch
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("pa_decode needs contiguous tensors")
+    args = make_args(out, query, key_cache, value_cache, block_tables, seq_lens, **kw)
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = library().pa_decode(ctypes.byref(args), ctypes.c_void_p(handle))
+    if st != _abi.PA_OK:
+        raise PaDecodeError(st)
+
+
+def decode_args_call(args: _abi.PaDecodeArgs, stream_handle: int) -> int:
+    """Call pa_decode with a prepared argument struct (for tight timing loops)."""
+    return library().pa_decode(ctypes.byref(args), ctypes.c_void_p(stream_handle))

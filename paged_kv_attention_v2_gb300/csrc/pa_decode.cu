@@ -1,0 +1,234 @@
+// pa_decode.cu -- the C ABI of include/pa_decode.h: argument checks, v1/v2
+// choice, grid sizing, tensor maps for the NHD layout, launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_decode.h"
+#include "pa_launch.cuh"
+
+namespace {
+
+using pa::Params;
+
+constexpr int kMaxDevices = pa::kMaxDevices;
+
+// ---------------------------------------------------------------- device info
+
+int sm_count_for_current_device(int* out) {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v);
+    }
+    *out = v;
+    return 0;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// NHD page of one kv head = 16 rows of head_size elements.  The map views a
+// cache as [num_blocks * num_kv_heads * 16 rows][head_size] and moves boxes of
+// 16 rows x 64 elements (128 bytes) with the 128-byte swizzle, so that the
+// ldmatrix reads of the kernel are free of bank conflicts.
+bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_size, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_version(void) { return (1 << 16) | 0; }
+
+int32_t pa_max_num_partitions(int32_t max_seq_len) {
+    if (max_seq_len <= 0) return 1;
+    return (int32_t)(((int64_t)max_seq_len + PA_PARTITION_SIZE - 1) / PA_PARTITION_SIZE);
+}
+
+pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                             int32_t max_seq_len, int64_t* stats_elems, int64_t* tmp_elems) {
+    if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+    const int64_t s = (int64_t)num_seqs * num_heads * pa_max_num_partitions(max_seq_len);
+    if (stats_elems) *stats_elems = s;
+    if (tmp_elems) *tmp_elems = s * head_size;
+    return PA_OK;
+}
+
+/*
+ * v1 / v2 choice.  The pages pick v2 when the v2 tiles of one sequence
+ * (kv heads x partitions) exceed twice the SM count.  Here the choice is
+ * between two grids of the same persistent kernel: v1 makes one tile per
+ * (sequence, kv head) and writes the output directly; v2 makes one tile per
+ * 512-token partition and adds the partition statistics round trip and the
+ * reduce launch.  With a single partition per sequence v2 only adds that
+ * overhead, so v1 is chosen; with longer sequences v1 keeps one CTA busy per
+ * (sequence, kv head), which leaves SMs idle unless there are many such pairs
+ * per SM of equal length, so v2 is chosen.
+ */
+int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                       int32_t sm_count) {
+    (void)num_seqs;
+    (void)num_kv_heads;
+    (void)sm_count;
+    if (max_seq_len <= PA_PARTITION_SIZE) return PA_MODE_V1;
+    return PA_MODE_V2;
+}
+
+const char* pa_status_str(int32_t status) {
+    switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "v2 workspace (exp_sums / max_logits / tmp_out) missing or misaligned";
+    case PA_ERR_LAUNCH: return "CUDA launch failed";
+    case PA_ERR_DEVICE_CHECK: return "device-side argument check failed";
+    case PA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+pa_status pa_decode(const pa_decode_args* a, void* stream) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (a->num_seqs < 0 || a->num_heads <= 0 || a->num_kv_heads <= 0 || a->max_seq_len < 0 ||
+        a->num_blocks < 0 || a->max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_heads % a->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (a->dtype != PA_DTYPE_F32 && a->dtype != PA_DTYPE_F16 && a->dtype != PA_DTYPE_BF16)
+        return PA_ERR_INVALID_ARG;
+    if (a->layout != PA_LAYOUT_SPLIT && a->layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
+    if (a->mode != PA_MODE_AUTO && a->mode != PA_MODE_V1 && a->mode != PA_MODE_V2)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(a->scale) || !std::isfinite(a->softcap)) return PA_ERR_INVALID_ARG;
+    if (a->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
+    if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
+    const int group = a->num_heads / a->num_kv_heads;
+    if (group > 16) return PA_ERR_UNSUPPORTED;
+    if (a->num_seqs == 0) return PA_OK;
+    if (!a->out || !a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_blocks == 0) return PA_ERR_INVALID_ARG;
+    if ((int64_t)a->max_blocks_per_seq * PA_BLOCK_SIZE < (int64_t)a->max_seq_len)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(a->out, 16) || !aligned(a->query, 16) || !aligned(a->key_cache, 16) ||
+        !aligned(a->value_cache, 16) || !aligned(a->block_tables, 4) || !aligned(a->seq_lens, 4) ||
+        !aligned(a->alibi_slopes, 4))
+        return PA_ERR_INVALID_ARG;
+
+    int sm = 0;
+    int mode = a->mode;
+    if (mode == PA_MODE_AUTO) {
+        if (sm_count_for_current_device(&sm) != 0) return PA_ERR_LAUNCH;
+        mode = pa_choose_mode(a->num_seqs, a->num_kv_heads, a->max_seq_len, sm);
+    }
+    const bool v1 = mode == PA_MODE_V1;
+    const int max_parts = pa_max_num_partitions(a->max_seq_len);
+    if (!v1) {
+        if (!a->exp_sums || !a->max_logits || !a->tmp_out) return PA_ERR_WORKSPACE;
+        if (!aligned(a->tmp_out, 16) || !aligned(a->exp_sums, 4) || !aligned(a->max_logits, 4))
+            return PA_ERR_WORKSPACE;
+    }
+    if (sm == 0 && sm_count_for_current_device(&sm) != 0) return PA_ERR_LAUNCH;
+    const int64_t units = (int64_t)a->num_seqs * (v1 ? 1 : max_parts);
+    const int64_t tiles = units * a->num_kv_heads;
+    if (tiles >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
+
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    p.query = a->query;
+    p.key_cache = a->key_cache;
+    p.value_cache = a->value_cache;
+    p.block_tables = a->block_tables;
+    p.seq_lens = a->seq_lens;
+    p.alibi = a->alibi_slopes;
+    p.out = a->out;
+    p.exp_sums = a->exp_sums;
+    p.max_logits = a->max_logits;
+    p.tmp_out = a->tmp_out;
+    p.dev_error = a->dev_error;
+    p.num_seqs = a->num_seqs;
+    p.num_heads = a->num_heads;
+    p.num_kv_heads = a->num_kv_heads;
+    p.group = group;
+    p.num_blocks = a->num_blocks;
+    p.max_blocks_per_seq = a->max_blocks_per_seq;
+    p.max_seq_len = a->max_seq_len;
+    p.max_parts = max_parts;
+    p.scale = a->scale;
+    p.softcap = a->softcap > 0.f ? a->softcap : 0.f;
+    p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
+    p.v1 = v1 ? 1 : 0;
+
+    alignas(64) CUtensorMap tmk, tmv;
+    std::memset(&tmk, 0, sizeof tmk);
+    std::memset(&tmv, 0, sizeof tmv);
+    if (a->layout == PA_LAYOUT_NHD && a->dtype != PA_DTYPE_F32) {
+        const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
+        if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
+        const bool bf = a->dtype == PA_DTYPE_BF16;
+        if (!make_nhd_map(&tmk, a->key_cache, rows, a->head_size, bf) ||
+            !make_nhd_map(&tmv, a->value_cache, rows, a->head_size, bf))
+            return PA_ERR_LAUNCH;
+    }
+
+    pa::LaunchArgs la;
+    la.stream = static_cast<cudaStream_t>(stream);
+    la.tmk = &tmk;
+    la.tmv = &tmv;
+    la.sm_count = sm;
+    la.tiles_upper = tiles;
+    la.group_tiles = group > 8 ? 2 : 1;
+    la.layout = a->layout;
+    la.head_size = a->head_size;
+    la.ev_begin = a->event_main_begin;
+    la.ev_end = a->event_main_end;
+    la.grid_override = 0;
+
+    cudaError_t e;
+    switch (a->dtype) {
+    case PA_DTYPE_F32: e = pa::launch_f32(p, la); break;
+    case PA_DTYPE_F16: e = pa::launch_f16(p, la); break;
+    default: e = pa::launch_bf16(p, la); break;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+}  // extern "C"

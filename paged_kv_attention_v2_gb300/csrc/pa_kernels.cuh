@@ -1,0 +1,903 @@
+// pa_kernels.cuh -- device code of the paged decode attention path (sm_103a).
+//
+// Partition kernel (Phase 1 of "paged_attention_v2_pytorch.py -- BI-V100
+// PagedAttention V2 implementation", and the whole v1 pass):
+//   persistent CTAs walk (sequence, kv head, 512-token partition) tiles; in v1
+//   mode a tile is a whole (sequence, kv head).  Warp NC is the producer: it
+//   walks seq_lens with a warp scan to find its tiles, reads each tile's block
+//   table slice with one coalesced warp load, and streams every K/V page of
+//   the tile into a STAGES-deep shared-memory ring with bulk (TMA) copies,
+//   one mbarrier per stage.  Warps 0..NC-1 consume pages round-robin: the
+//   whole GQA query group of the kv head is packed into the N dimension of
+//   m16n8k16 tensor-core MMAs (tokens on M for Q.K^T, head dims on M for P.V),
+//   so each page is read from HBM once for all heads of the group; the softmax
+//   state stays online in registers.  At the end of a tile the consumer warps
+//   merge their partial (max, sum, acc) through shared memory and write the
+//   partition statistics (v2) or the output row (v1).
+// Reduce kernel (Phase 2): per (sequence, head), M = max_p m_p,
+//   w_p = exp(m_p - M) * e_p, out = sum_p w_p tmp_p / sum_p w_p.
+#pragma once
+
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "pa_decode.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kPart = PA_PARTITION_SIZE;  // tokens per partition
+constexpr int kBS = PA_BLOCK_SIZE;        // tokens per page
+constexpr int kSplit = PA_LAYOUT_SPLIT;
+constexpr int kNHD = PA_LAYOUT_NHD;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Params {
+    const void* query;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const float* alibi;
+    void* out;
+    float* exp_sums;
+    float* max_logits;
+    float* tmp_out;
+    int32_t* dev_error;
+    int num_seqs, num_heads, num_kv_heads, group;
+    int num_blocks, max_blocks_per_seq, max_seq_len, max_parts;
+    float scale, softcap, inv_softcap;
+    int v1;
+};
+
+struct TileDesc {
+    int seq, kvh, part, tok_begin, tok_end, len, flags, pad;
+};
+constexpr int kTileStop = 1;
+
+__device__ __forceinline__ void report(const Params& p, int bits) {
+    if (p.dev_error) atomicOr(p.dev_error, bits);
+}
+
+__device__ __forceinline__ int clamp_len(const Params& p, int raw) {
+    return raw < 0 ? 0 : (raw > p.max_seq_len ? p.max_seq_len : raw);
+}
+
+// ------------------------------------------------------------------ config
+
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+struct Cfg {
+    static constexpr bool kF32 = std::is_same<T, float>::value;
+    static constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    static constexpr int kElem = sizeof(T);
+    static constexpr int kPageBytes = kBS * HEAD * kElem;  // one page of K (or of V)
+    static constexpr int kStageBytes = 2 * kPageBytes;
+    static constexpr int kMaxG = kF32 ? 16 : NT * 8;       // heads per kv head handled
+    static constexpr int kQBytes = kMaxG * HEAD * kElem;
+    static constexpr int kTD = 2;                          // tile descriptor ring depth
+    static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
+    static constexpr int kThreads = (NC + 1) * 32;
+    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32;
+    static constexpr int kScratchFloats = kF32 ? NC * (kBS * 16 + 16) : 0;
+
+    static constexpr int oRing = 0;
+    static constexpr int oQ = oRing + STAGES * kStageBytes;
+    static constexpr int oMerge = oQ + kTD * kQBytes;
+    static constexpr int oML = oMerge + NC * kMaxG * kMergeStride * 4;
+    static constexpr int oScratch = oML + NC * kMaxG * 8;
+    static constexpr int oDesc = oScratch + kScratchFloats * 4;
+    static constexpr int oBar = (oDesc + kTD * (int)sizeof(TileDesc) + 7) & ~7;
+    static constexpr int oAbort = oBar + (2 * STAGES + 2 * kTD + 1) * 8;
+    static constexpr int kSmemBytes = oAbort + 16 + 1024;  // + slack for 1024-B alignment
+
+    static_assert(kPageBytes % 1024 == 0 || !kTensorMap, "swizzled pages need 1024-B alignment");
+    static_assert(kQBytes % 16 == 0, "bulk copy size");
+};
+
+struct Smem {
+    uint32_t ring;       // shared address of stage 0
+    uint32_t q;          // shared address of Q slot 0
+    float* merge;
+    float2* ml;
+    float* scratch;
+    TileDesc* desc;
+    uint32_t full, empty, td_full, td_empty;  // shared addresses of barrier arrays
+    uint32_t merge_bar;  // consumer warps: partial states written / epilogue reads done
+    volatile int* abort;
+};
+
+// Bounded wait by every lane of a warp; the result is the same in all lanes.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Barrier among the NC consumer warps on an mbarrier of count NC (bounded,
+// unlike bar.sync, so a warp that gave up cannot strand the others).
+__device__ __forceinline__ bool consumer_sync(const Smem& sm, uint32_t& phase, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.merge_bar);
+    const bool ok = warp_wait(sm.merge_bar, phase & 1, sm.abort);
+    ++phase;
+    return ok;
+}
+
+// ------------------------------------------------------------------ producer
+
+template <class C, int HEAD, int STAGES>
+__device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk,
+                         const CUtensorMap* tmv, int lane) {
+    const int S = p.num_seqs, Hkv = p.num_kv_heads;
+    const char* kbase = static_cast<const char*>(p.key_cache);
+    const char* vbase = static_cast<const char*>(p.value_cache);
+    const char* qbase = static_cast<const char*>(p.query);
+    const uint32_t qbytes = (uint32_t)(p.group * HEAD * C::kElem);
+
+    // Walk of seq_lens in chunks of 32 sequences: lane i holds sequence cb+i.
+    int cb = 0, cu = 0;  // first sequence of the chunk, tile units before the chunk
+    int c_len = 0, c_units = 0, c_incl = 0, c_total = 0;
+    auto load_chunk = [&](int base) {
+        const int s = base + lane;
+        c_len = 0;
+        c_units = 0;
+        if (s < S) {
+            const int raw = __ldg(p.seq_lens + s);
+            c_len = clamp_len(p, raw);
+            if (c_len != raw) report(p, PA_DEVERR_SEQ_LEN);
+            c_units = p.v1 ? 1 : (c_len + kPart - 1) / kPart;
+        }
+        c_incl = c_units;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, c_incl, o);
+            if (lane >= o) c_incl += v;
+        }
+        c_total = __shfl_sync(0xffffffffu, c_incl, 31);
+    };
+    load_chunk(0);
+
+    uint32_t g = 0;  // pages issued by this CTA
+    int k = 0;       // tiles issued by this CTA
+    bool ok = true;
+    for (int tile = blockIdx.x;; tile += gridDim.x) {
+        const int u = tile / Hkv;
+        const int kvh = tile - u * Hkv;
+        while (cb < S && u >= cu + c_total) {
+            cu += c_total;
+            cb += 32;
+            load_chunk(cb);
+        }
+        if (cb >= S) break;
+        const int rel = u - cu;
+        const unsigned hit = __ballot_sync(0xffffffffu, c_incl > rel);
+        const int j = __ffs(hit) - 1;
+        const int seq = cb + j;
+        const int excl = __shfl_sync(0xffffffffu, c_incl - c_units, j);
+        const int len = __shfl_sync(0xffffffffu, c_len, j);
+        const int part = rel - excl;
+        const int tb = p.v1 ? 0 : part * kPart;
+        const int te = p.v1 ? len : min(len, tb + kPart);
+        const int npages = (te - tb + kBS - 1) / kBS;
+
+        const int slot = k % C::kTD;
+        if (lane == 0) {
+            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, kWaitLimitNs);
+            if (ok) {
+                TileDesc& d = sm.desc[slot];
+                d.seq = seq;
+                d.kvh = kvh;
+                d.part = part;
+                d.tok_begin = tb;
+                d.tok_end = te;
+                d.len = len;
+                d.flags = 0;
+                mbar_arrive_expect_tx(sm.td_full + slot * 8, qbytes);
+                bulk_g2s(sm.q + slot * C::kQBytes,
+                         qbase + ((int64_t)seq * p.num_heads + (int64_t)kvh * p.group) * HEAD * C::kElem,
+                         qbytes, sm.td_full + slot * 8);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+
+        const int32_t* row = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + tb / kBS;
+        for (int pc = 0; pc < npages && ok; pc += 32) {
+            const int n = min(32, npages - pc);
+            int blk = 0;
+            if (lane < n) {
+                blk = __ldg(row + pc + lane);
+                if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                    report(p, PA_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+            }
+            for (int jj = 0; jj < n; ++jj) {
+                const int b = __shfl_sync(0xffffffffu, blk, jj);
+                if (lane == 0) {
+                    const uint32_t st = g % STAGES, ph = (g / STAGES) & 1;
+                    ok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, kWaitLimitNs);
+                    if (ok) {
+                        const uint32_t fb = sm.full + st * 8;
+                        const uint32_t dk = sm.ring + st * C::kStageBytes;
+                        const uint32_t dv = dk + C::kPageBytes;
+                        const int64_t page = (int64_t)b * Hkv + kvh;
+                        mbar_arrive_expect_tx(fb, C::kStageBytes);
+                        if constexpr (C::kTensorMap) {
+                            const int y = (int)(page * kBS);
+#pragma unroll
+                            for (int half = 0; half < HEAD / 64; ++half) {
+                                tensor2d_g2s(dk + half * 2048, tmk, half * 64, y, fb);
+                                tensor2d_g2s(dv + half * 2048, tmv, half * 64, y, fb);
+                            }
+                        } else {
+                            bulk_g2s(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb);
+                            bulk_g2s(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++g;
+            }
+        }
+        if (!ok) break;
+        ++k;
+    }
+
+    if (lane == 0) {
+        if (ok) {
+            const int slot = k % C::kTD;
+            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, kWaitLimitNs);
+            if (ok) {
+                sm.desc[slot].flags = kTileStop;
+                mbar_arrive(sm.td_full + slot * 8);
+            }
+        }
+        if (!ok) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+        }
+        // No bulk copy may still be writing shared memory when the CTA exits:
+        // wait (bounded) for the last phase issued on every stage.
+        for (uint32_t st = 0; st < STAGES && st < g; ++st) {
+            const uint32_t last = g - 1 - ((g - 1 - st) % STAGES);
+            mbar_wait(sm.full + st * 8, (last / STAGES) & 1, sm.abort + 1, kWaitLimitNs);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ epilogue
+
+// Merge the NC consumer warps' partial states of one tile and write either the
+// partition statistics (v2) or the final output row (v1).
+template <class C, typename T, int HEAD, int NC>
+__device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm, int tid) {
+    constexpr int D4 = HEAD / 4;
+    const int G = p.group;
+    for (int idx = tid; idx < G * D4; idx += NC * 32) {
+        const int h = idx / D4, d4 = idx - h * D4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) M = fmaxf(M, sm.ml[w * C::kMaxG + h].x);
+        float L = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+            const float2 e = sm.ml[w * C::kMaxG + h];
+            const float c = (e.x == -INFINITY) ? 0.f : expf(e.x - M);
+            L += c * e.y;
+            const float4 a = *reinterpret_cast<const float4*>(
+                sm.merge + (w * C::kMaxG + h) * C::kMergeStride + 4 * d4);
+            o.x += c * a.x;
+            o.y += c * a.y;
+            o.z += c * a.z;
+            o.w += c * a.w;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        o.x *= inv;
+        o.y *= inv;
+        o.z *= inv;
+        o.w *= inv;
+        const int head = d.kvh * G + h;
+        const int64_t sh = (int64_t)d.seq * p.num_heads + head;
+        if (p.v1) {
+            T* dst = static_cast<T*>(p.out) + sh * HEAD + 4 * d4;
+            if constexpr (C::kF32) {
+                *reinterpret_cast<float4*>(dst) = o;
+            } else {
+                uint2 v;
+                v.x = pack2<C::kBF16>(o.x, o.y);
+                v.y = pack2<C::kBF16>(o.z, o.w);
+                *reinterpret_cast<uint2*>(dst) = v;
+            }
+        } else {
+            const int64_t ps = sh * p.max_parts + d.part;
+            *reinterpret_cast<float4*>(p.tmp_out + ps * HEAD + 4 * d4) = o;
+            if (d4 == 0) {
+                float m = M;
+                // logits are kept relative to the tile's last token; move the
+                // partition max into the sequence frame (last token of the
+                // sequence) -- the reduce kernel finishes the shift to absolute
+                // positions after merging.
+                if (p.alibi) m += __ldg(p.alibi + head) * (float)(d.tok_end - d.len);
+                p.max_logits[ps] = m;
+                p.exp_sums[ps] = L;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ consumers
+
+// Byte offset of this lane's ldmatrix row address inside a K page for k-step kk
+// (A operand of Q.K^T: rows = 16 tokens, columns = head dims 16kk..16kk+15).
+template <int LAYOUT>
+__device__ __forceinline__ uint32_t k_frag_off(int lane, int kk) {
+    const int j = lane >> 3, r = lane & 7;
+    const int tok = r + ((j & 1) << 3);
+    const int c = 2 * kk + (j >> 1);  // 8-element chunk of the head dim
+    if constexpr (LAYOUT == kSplit) {
+        return (uint32_t)((c * kBS + tok) * 16);  // [d/8][token][8]
+    } else {
+        // NHD page staged as [d/64][token][64] with the 128-byte swizzle
+        return (uint32_t)((c >> 3) * 2048 + tok * 128 + (((c & 7) ^ (tok & 7)) << 4));
+    }
+}
+
+// Byte offset of this lane's ldmatrix row address inside a V page for m-tile mt
+// (A operand of P.V: rows = head dims 16mt..16mt+15, columns = 16 tokens).
+template <int LAYOUT>
+__device__ __forceinline__ uint32_t v_frag_off(int lane, int mt) {
+    const int j = lane >> 3, r = lane & 7;
+    if constexpr (LAYOUT == kSplit) {
+        const int d = mt * 16 + r + ((j & 1) << 3);  // [d][token]: row d holds 16 tokens
+        return (uint32_t)(d * 32 + (j >> 1) * 16);
+    } else {
+        const int tok = r + ((j >> 1) << 3);  // stored as token rows: loaded transposed
+        const int c = 2 * mt + (j & 1);
+        return (uint32_t)((c >> 3) * 2048 + tok * 128 + (((c & 7) ^ (tok & 7)) << 4));
+    }
+}
+
+// Zero the V entries of tokens >= valid in a staged 16-bit page so that the
+// P.V product never sees unused slots (which may hold anything, even NaN).
+template <int LAYOUT, int HEAD>
+__device__ __forceinline__ void zero_v_tail16(uint32_t vpage, int valid, int lane) {
+    if constexpr (LAYOUT == kSplit) {
+        for (int d = lane; d < HEAD; d += 32)
+            for (int t = valid; t < kBS; ++t)
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(vpage + (uint32_t)(d * kBS + t) * 2),
+                             "h"((unsigned short)0)
+                             : "memory");
+    } else {
+        const int rows = (kBS - valid) * (HEAD / 64);
+        for (int i = lane; i < rows * 8; i += 32) {
+            const int rowi = i >> 3, chunk = i & 7;
+            const int tok = valid + rowi / (HEAD / 64), half = rowi % (HEAD / 64);
+            const uint32_t a = vpage + (uint32_t)(half * 2048 + tok * 128 + chunk * 16);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+        }
+    }
+}
+
+template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+__device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane) {
+    constexpr bool BF = C::kBF16;
+    constexpr int KT = HEAD / 16;  // k-steps of Q.K^T, m-tiles of P.V
+    const int G = p.group;
+    const int r = lane >> 2, cq = lane & 3;
+    const bool has_alibi = p.alibi != nullptr;
+    const bool has_cap = p.softcap > 0.f;
+    uint32_t gbase = 0;
+    uint32_t mphase = 0;
+    for (int k = 0;; ++k) {
+        const int slot = k % C::kTD;
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        const TileDesc d = sm.desc[slot];
+        if (d.flags & kTileStop) return;
+
+        // Q as B fragments: B[k = head dim][n = head], heads >= G are zero.
+        uint32_t qb[NT][KT][2];
+        const uint32_t qs = sm.q + slot * C::kQBytes;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + r;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t b0 = 0, b1 = 0;
+                if (h < G) {
+                    const uint32_t a = qs + (uint32_t)((h * HEAD + kk * 16 + 2 * cq) * 2);
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b0) : "r"(a));
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b1) : "r"(a + 16));
+                }
+                qb[nt][kk][0] = b0;
+                qb[nt][kk][1] = b1;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // Q and descriptor are in registers
+
+        float sl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = nt * 8 + 2 * cq + e;
+                sl[nt][e] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+            }
+        const int origin = d.tok_end - 1;  // ALiBi positions are taken relative to this token
+
+        float m[NT][2], l[NT][2];
+        float acc[KT][NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+        }
+
+        const int npages = (d.tok_end - d.tok_begin + kBS - 1) / kBS;
+        for (int j = warp; j < npages; j += NC) {
+            const uint32_t gg = gbase + (uint32_t)j;
+            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+                report(p, PA_DEVERR_TIMEOUT);
+                *sm.abort = 1;
+                return;
+            }
+            const uint32_t kp = sm.ring + st * C::kStageBytes;
+            const uint32_t vp = kp + C::kPageBytes;
+            const int tok0 = d.tok_begin + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);
+            if (valid < kBS) {
+                zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // S^T[token][head] = K . Q^T
+            float s[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_16816<BF>(s[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+            }
+
+            // logits, online softmax, P as B fragments of P.V
+            const int tlo = tok0 + r;  // this thread's tokens: tlo (e=0,1), tlo+8 (e=2,3)
+            uint32_t pb[NT][2], pbl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float z[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = s[nt][e] * p.scale;
+                    if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                    if (has_alibi) v += sl[nt][e & 1] * (float)(tlo + ((e >> 1) << 3) - origin);
+                    z[e] = v;
+                }
+                if (r >= valid) z[0] = z[1] = -INFINITY;
+                if (r + 8 >= valid) z[2] = z[3] = -INFINITY;
+                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+                const float al0 = exp2f((m[nt][0] - mn0) * kLog2e);
+                const float al1 = exp2f((m[nt][1] - mn1) * kLog2e);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+                const float p0 = exp2f((z[0] - mn0) * kLog2e);
+                const float p1 = exp2f((z[1] - mn1) * kLog2e);
+                const float p2 = exp2f((z[2] - mn0) * kLog2e);
+                const float p3 = exp2f((z[3] - mn1) * kLog2e);
+                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    acc[mt][nt][0] *= al0;
+                    acc[mt][nt][1] *= al1;
+                    acc[mt][nt][2] *= al0;
+                    acc[mt][nt][3] *= al1;
+                }
+                const uint32_t x0 = pack2<BF>(p0, p1);  // token r,   heads 2cq, 2cq+1
+                const uint32_t x1 = pack2<BF>(p2, p3);  // token r+8
+                pb[nt][0] = movmatrix_trans(x0);         // -> B[k = token 2cq..][n = head r]
+                pb[nt][1] = movmatrix_trans(x1);
+                if constexpr (BF) {
+                    // bf16 keeps 8 significant bits; carry the rounding residue
+                    // of P in a second bf16 term so P.V keeps ~16 bits.
+                    const float2 h0 = unpack2<BF>(x0), h1 = unpack2<BF>(x1);
+                    pbl[nt][0] = movmatrix_trans(pack2<BF>(p0 - h0.x, p1 - h0.y));
+                    pbl[nt][1] = movmatrix_trans(pack2<BF>(p2 - h1.x, p3 - h1.y));
+                }
+            }
+
+            // acc^T[head dim][head] += V^T . P^T
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                if constexpr (LAYOUT == kSplit)
+                    ldsm_x4(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
+                else
+                    ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                    if constexpr (BF) mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pbl[nt][0], pbl[nt][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+        }
+
+        // this warp's partial state -> shared memory
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], o);
+                l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], o);
+            }
+        }
+        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h0 = nt * 8 + 2 * cq;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                const int d0 = mt * 16 + r;
+                mw[h0 * C::kMergeStride + d0] = acc[mt][nt][0];
+                mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][nt][1];
+                mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][nt][2];
+                mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
+            }
+            if (r == 0) {
+                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+            }
+        }
+        if (!consumer_sync(sm, mphase, lane)) {  // all partial states written
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        tile_epilogue<C, T, HEAD, NC>(p, d, sm, warp * 32 + lane);
+        if (!consumer_sync(sm, mphase, lane)) {  // merge buffers free again
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        gbase += (uint32_t)npages;
+    }
+}
+
+// fp32 inputs: CUDA-core arithmetic (tensor cores would round to tf32).
+template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
+__device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane) {
+    constexpr int MAXG = 16, HPL = MAXG / 2, DPL = HEAD / 32;
+    const int G = p.group;
+    const int t = lane & 15, hs = lane >> 4;  // Q.K^T: lane = (token t, heads hs, hs+2, ...)
+    const bool has_alibi = p.alibi != nullptr;
+    const bool has_cap = p.softcap > 0.f;
+    float* pw = sm.scratch + warp * (kBS * MAXG + MAXG);  // p[token][head], alpha[head]
+    uint32_t gbase = 0;
+    uint32_t mphase = 0;
+    for (int k = 0;; ++k) {
+        const int slot = k % C::kTD;
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        const TileDesc d = sm.desc[slot];
+        if (d.flags & kTileStop) return;
+        const float* q = reinterpret_cast<const float*>(
+            __cvta_shared_to_generic(sm.q + slot * C::kQBytes));
+        float sl[HPL];
+#pragma unroll
+        for (int i = 0; i < HPL; ++i) {
+            const int h = hs + 2 * i;
+            sl[i] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+        }
+        const int origin = d.tok_end - 1;
+        float m[HPL], l[HPL], acc[MAXG][DPL];
+#pragma unroll
+        for (int i = 0; i < HPL; ++i) {
+            m[i] = -INFINITY;
+            l[i] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < MAXG; ++h)
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) acc[h][c] = 0.f;
+
+        const int npages = (d.tok_end - d.tok_begin + kBS - 1) / kBS;
+        for (int j = warp; j < npages; j += NC) {
+            const uint32_t gg = gbase + (uint32_t)j;
+            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+                report(p, PA_DEVERR_TIMEOUT);
+                *sm.abort = 1;
+                return;
+            }
+            const float* kp = reinterpret_cast<const float*>(
+                __cvta_shared_to_generic(sm.ring + st * C::kStageBytes));
+            float* vp = const_cast<float*>(kp) + kBS * HEAD;
+            const int tok0 = d.tok_begin + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);
+            if (valid < kBS) {
+                if constexpr (LAYOUT == kSplit) {
+                    for (int dd = lane; dd < HEAD; dd += 32)
+                        for (int tt = valid; tt < kBS; ++tt) vp[dd * kBS + tt] = 0.f;
+                } else {
+                    for (int i = lane; i < (kBS - valid) * HEAD; i += 32) vp[valid * HEAD + i] = 0.f;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            float z[HPL];
+#pragma unroll
+            for (int i = 0; i < HPL; ++i) {
+                const int h = hs + 2 * i;
+                float dot = 0.f;
+                if (h < G) {
+#pragma unroll 8
+                    for (int d4 = 0; d4 < HEAD / 4; ++d4) {
+                        const float4 qv = *reinterpret_cast<const float4*>(q + h * HEAD + 4 * d4);
+                        const float4 kv = (LAYOUT == kSplit)
+                            ? *reinterpret_cast<const float4*>(kp + (d4 * kBS + t) * 4)  // [d/4][token][4]
+                            : *reinterpret_cast<const float4*>(kp + t * HEAD + 4 * d4);
+                        dot = fmaf(qv.x, kv.x, dot);
+                        dot = fmaf(qv.y, kv.y, dot);
+                        dot = fmaf(qv.z, kv.z, dot);
+                        dot = fmaf(qv.w, kv.w, dot);
+                    }
+                }
+                float v = dot * p.scale;
+                if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                if (has_alibi) v += sl[i] * (float)(tok0 + t - origin);
+                z[i] = (t < valid) ? v : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < HPL; ++i) {
+                const int h = hs + 2 * i;
+                float mx = z[i];
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float mn = fmaxf(m[i], mx);
+                const float al = exp2f((m[i] - mn) * kLog2e);
+                const float pv = exp2f((z[i] - mn) * kLog2e);
+                m[i] = mn;
+                l[i] = l[i] * al + pv;
+                if (h < MAXG) {
+                    pw[t * MAXG + h] = pv;
+                    if (t == 0) pw[kBS * MAXG + h] = al;
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < MAXG; ++h) {
+                if (h < G) {
+                    const float al = pw[kBS * MAXG + h];
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) acc[h][c] *= al;
+                }
+            }
+            for (int tt = 0; tt < valid; ++tt) {
+                float vv[DPL];
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) {
+                    const int dd = lane + 32 * c;
+                    vv[c] = (LAYOUT == kSplit) ? vp[dd * kBS + tt] : vp[tt * HEAD + dd];
+                }
+#pragma unroll
+                for (int h = 0; h < MAXG; ++h) {
+                    if (h < G) {
+                        const float pr = pw[tt * MAXG + h];
+#pragma unroll
+                        for (int c = 0; c < DPL; ++c) acc[h][c] = fmaf(pr, vv[c], acc[h][c]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+        }
+        // sum l over the 16 tokens (lanes with the same hs)
+#pragma unroll
+        for (int i = 0; i < HPL; ++i)
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], o);
+        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+#pragma unroll
+        for (int h = 0; h < MAXG; ++h)
+            if (h < G)
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) mw[h * C::kMergeStride + lane + 32 * c] = acc[h][c];
+        if (t == 0) {
+#pragma unroll
+            for (int i = 0; i < HPL; ++i) {
+                const int h = hs + 2 * i;
+                if (h < MAXG) sm.ml[warp * C::kMaxG + h] = make_float2(m[i], l[i]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // done with Q in shared memory
+        if (!consumer_sync(sm, mphase, lane)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        tile_epilogue<C, float, HEAD, NC>(p, d, sm, warp * 32 + lane);
+        if (!consumer_sync(sm, mphase, lane)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        gbase += (uint32_t)npages;
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
+    pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gen = smem_raw + (base - raw);
+
+    Smem sm;
+    sm.ring = base + C::oRing;
+    sm.q = base + C::oQ;
+    sm.merge = reinterpret_cast<float*>(gen + C::oMerge);
+    sm.ml = reinterpret_cast<float2*>(gen + C::oML);
+    sm.scratch = reinterpret_cast<float*>(gen + C::oScratch);
+    sm.desc = reinterpret_cast<TileDesc*>(gen + C::oDesc);
+    sm.full = base + C::oBar;
+    sm.empty = sm.full + STAGES * 8;
+    sm.td_full = sm.empty + STAGES * 8;
+    sm.td_empty = sm.td_full + C::kTD * 8;
+    sm.merge_bar = sm.td_empty + C::kTD * 8;
+    sm.abort = reinterpret_cast<volatile int*>(gen + C::oAbort);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sm.full + s * 8, 1);
+            mbar_init(sm.empty + s * 8, 1);
+        }
+        for (int s = 0; s < C::kTD; ++s) {
+            mbar_init(sm.td_full + s * 8, 1);
+            mbar_init(sm.td_empty + s * 8, NC);
+        }
+        mbar_init(sm.merge_bar, NC);
+        sm.abort[0] = 0;
+        sm.abort[1] = 0;
+        fence_mbar_init();
+    }
+    if constexpr (C::kTensorMap) {
+        if (threadIdx.x == NC * 32) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+    }
+    __syncthreads();
+    pdl_launch_dependents();  // the reduce kernel may be scheduled; it waits for our completion
+    pdl_wait_primary();       // earlier work in the stream (inputs, workspace readers) is done
+
+    if (warp == NC) {
+        producer<C, HEAD, STAGES>(p, sm, &tmk, &tmv, lane);
+    } else if constexpr (C::kF32) {
+        consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+    } else {
+        consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+    }
+}
+
+// Phase 2: one CTA of 128 threads per (sequence, head).
+template <typename T, int HEAD>
+__global__ void __launch_bounds__(128) pa_reduce_kernel(const Params p) {
+    constexpr int D4 = HEAD / 4;          // float4 columns of a partition row
+    constexpr int RPW = 32 / D4;          // partition rows per warp step (1 or 2)
+    constexpr int RSTEP = 4 * RPW;        // partition rows per CTA step
+    __shared__ float red[4];
+    __shared__ float4 part[RSTEP][D4];
+
+    const int bid = blockIdx.x;
+    const int s = bid / p.num_heads, h = bid - s * p.num_heads;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait_primary();
+
+    const int len = clamp_len(p, p.seq_lens[s]);
+    const int P = (len + kPart - 1) / kPart;
+    const int64_t sb = ((int64_t)s * p.num_heads + h) * p.max_parts;
+    float* ml = p.max_logits + sb;
+    float* es = p.exp_sums + sb;
+    const float* tmp = p.tmp_out + sb * HEAD;
+    T* o = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + h) * HEAD;
+
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    if (P > 0) {
+        float M = -INFINITY;
+        for (int q = tid; q < P; q += 128) M = fmaxf(M, ml[q]);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (lane == 0) red[warp] = M;
+        __syncthreads();
+        M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        __syncthreads();
+
+        const int rowi = warp * RPW + lane / D4, d4 = lane % D4;
+        for (int q = rowi; q < P; q += RSTEP) {
+            const float c = expf(ml[q] - M) * es[q];
+            const float4 t4 = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD + 4 * d4);
+            a.x += c * t4.x;
+            a.y += c * t4.y;
+            a.z += c * t4.z;
+            a.w += c * t4.w;
+        }
+        for (int q = tid; q < P; q += 128) W += expf(ml[q] - M) * es[q];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+        if (lane == 0) red[warp] = W;
+        part[rowi][d4] = a;
+        __syncthreads();
+        W = (red[0] + red[1]) + (red[2] + red[3]);
+        if (tid < D4) {
+            float4 sum = part[0][tid];
+            for (int i = 1; i < RSTEP; ++i) {
+                const float4 v = part[i][tid];
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const float inv = 1.f / W;
+            a = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+        }
+        // statistics: sequence frame -> absolute ALiBi positions
+        if (p.alibi) {
+            const float shift = __ldg(p.alibi + h) * (float)(len - 1);
+            for (int q = tid; q < P; q += 128) ml[q] += shift;
+        }
+    }
+    if (tid < D4) {
+        T* dst = o + 4 * tid;
+        if constexpr (std::is_same<T, float>::value) {
+            *reinterpret_cast<float4*>(dst) = a;
+        } else {
+            constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+            uint2 v;
+            v.x = pack2<BF>(a.x, a.y);
+            v.y = pack2<BF>(a.z, a.w);
+            *reinterpret_cast<uint2*>(dst) = v;
+        }
+    }
+    for (int q = P + tid; q < p.max_parts; q += 128) {
+        ml[q] = -INFINITY;
+        es[q] = 0.f;
+    }
+}
+
+}  // namespace pa

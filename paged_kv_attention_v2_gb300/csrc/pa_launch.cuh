@@ -1,0 +1,116 @@
+// pa_launch.cuh -- host-side launch of the partition (or v1) kernel and of the
+// reduce kernel for one (dtype, head size) family.  Included by the
+// per-dtype translation units so they compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "pa_kernels.cuh"
+
+namespace pa {
+
+struct LaunchArgs {
+    cudaStream_t stream;
+    const CUtensorMap* tmk;  // NHD 16-bit only (otherwise unused placeholders)
+    const CUtensorMap* tmv;
+    int sm_count;
+    int64_t tiles_upper;     // upper bound on tiles (persistent grid never exceeds it)
+    int group_tiles;         // 1 or 2: n-tiles of 8 query heads
+    int layout;
+    int head_size;
+    void* ev_begin;
+    void* ev_end;
+    int grid_override;       // > 0: use this many CTAs (tests / sweeps)
+};
+
+constexpr int kMaxDevices = 64;
+
+template <typename T, int HEAD, int NT, int LAYOUT>
+cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
+    constexpr int STAGES = std::is_same<T, float>::value ? 4 : 8;
+    constexpr int NC = 4;
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
+    auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC>;
+
+    static std::atomic<int> occ_cache[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int occ = (dev >= 0 && dev < kMaxDevices) ? occ_cache[dev].load() : 0;
+    if (occ <= 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < kMaxDevices) occ_cache[dev].store(occ);
+    }
+    int64_t grid = (int64_t)la.sm_count * occ;
+    if (la.grid_override > 0) grid = la.grid_override;
+    if (grid > la.tiles_upper) grid = la.tiles_upper;
+    if (grid < 1) grid = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = la.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (la.ev_begin) {
+        e = cudaEventRecord(static_cast<cudaEvent_t>(la.ev_begin), la.stream);
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, p, *la.tmk, *la.tmv);
+    if (e != cudaSuccess) return e;
+    if (la.ev_end) e = cudaEventRecord(static_cast<cudaEvent_t>(la.ev_end), la.stream);
+    return e;
+}
+
+template <typename T, int HEAD>
+cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)p.num_seqs * p.num_heads));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = la.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD>, p);
+}
+
+template <typename T, int HEAD, int NT>
+cudaError_t launch_layout(const Params& p, const LaunchArgs& la) {
+    return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD>(p, la)
+                             : launch_main<T, HEAD, NT, kSplit>(p, la);
+}
+
+// Whole operation for one storage type.
+template <typename T>
+cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
+    constexpr bool F32 = std::is_same<T, float>::value;
+    cudaError_t e;
+    if constexpr (F32) {  // one fp32 consumer handles up to 16 heads
+        e = la.head_size == 128 ? launch_layout<T, 128, 2>(p, la) : launch_layout<T, 64, 2>(p, la);
+    } else if (la.head_size == 128) {
+        e = la.group_tiles == 2 ? launch_layout<T, 128, 2>(p, la) : launch_layout<T, 128, 1>(p, la);
+    } else {
+        e = la.group_tiles == 2 ? launch_layout<T, 64, 2>(p, la) : launch_layout<T, 64, 1>(p, la);
+    }
+    if (e != cudaSuccess || p.v1) return e;
+    return la.head_size == 128 ? launch_reduce<T, 128>(p, la) : launch_reduce<T, 64>(p, la);
+}
+
+cudaError_t launch_f32(const Params& p, const LaunchArgs& la);
+cudaError_t launch_f16(const Params& p, const LaunchArgs& la);
+cudaError_t launch_bf16(const Params& p, const LaunchArgs& la);
+
+}  // namespace pa

@@ -1,0 +1,116 @@
+"""Helpers for the GPU parity tests: move a workloads.Workload to the device, run
+the CUDA path through the C ABI, and compare with the fp64 oracle element by
+element.
+
+Tolerances (stated for the method's inputs and fp32 accumulation):
+  output and tmp_out, fp16/bf16 inputs:  |gpu - ref| <= 2e-3 + 1e-2 |ref|
+  output and tmp_out, fp32 inputs:       |gpu - ref| <= 1e-5 + 1e-5 |ref|
+  max_logits and exp_sums:               |gpu - ref| <= 1e-4 max(|ref|, 1)
+  unused partitions:                     max_logits == -inf, exp_sums == 0 exactly
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import paged_kv_attention_v2_gb300 as pa
+
+OUT_TOL = {"f32": (1e-5, 1e-5), "f16": (2e-3, 1e-2), "bf16": (2e-3, 1e-2)}
+STAT_TOL = 1e-4
+
+
+def torch_dtype(dtype: str):
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+
+def to_torch(a: np.ndarray, dtype: str) -> torch.Tensor:
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def to_device(w, device="cuda:0"):
+    d = {
+        "query": to_torch(w.query, w.dtype).to(device),
+        "key_cache": to_torch(w.key_cache, w.dtype).to(device),
+        "value_cache": to_torch(w.value_cache, w.dtype).to(device),
+        "block_tables": torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
+        "seq_lens": torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(device),
+        "alibi_slopes": None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(device),
+    }
+    return d
+
+
+def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_lens=None,
+            block_tables=None, poison_workspace=True):
+    """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error."""
+    dev = dev or to_device(w, device)
+    msl = w.max_seq_len if max_seq_len is None else max_seq_len
+    S, H, d = w.num_seqs, w.num_heads, w.head_size
+    out = torch.full((S, H, d), float("nan"), dtype=torch_dtype(w.dtype), device=device)
+    ws = pa.alloc_workspace(S, H, d, msl, device)
+    if poison_workspace:
+        for t in ws.values():
+            t.fill_(float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"],
+                 dev["block_tables"] if block_tables is None else block_tables,
+                 dev["seq_lens"] if seq_lens is None else seq_lens,
+                 num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
+                 alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout, mode=mode,
+                 dev_error=err, **ws)
+    torch.cuda.synchronize(device)
+    return {
+        "out": out.double().cpu().numpy(),
+        "max_logits": ws["max_logits"].double().cpu().numpy(),
+        "exp_sums": ws["exp_sums"].double().cpu().numpy(),
+        "tmp_out": ws["tmp_out"].double().cpu().numpy(),
+        "dev_error": int(err.item()),
+    }
+
+
+def _violations(gpu, ref, atol, rtol):
+    gpu = np.asarray(gpu)
+    ref = np.asarray(ref)
+    bad = ~(np.abs(gpu - ref) <= atol + rtol * np.abs(ref))  # NaN counts as bad
+    return bad
+
+
+def check_out(w, gpu_out, ref_out, seqs=None, what="out"):
+    atol, rtol = OUT_TOL[w.dtype]
+    sel = slice(None) if seqs is None else np.asarray(seqs)
+    g, r = gpu_out[sel], ref_out[sel]
+    bad = _violations(g, r, atol, rtol)
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        err = np.nanmax(np.abs(g - r) - rtol * np.abs(r))
+        raise AssertionError(f"{w.name}/{w.layout} {what}: {int(bad.sum())} of {bad.size} "
+                             f"elements out of tolerance; first at {idx}: gpu {g[idx]!r} "
+                             f"ref {r[idx]!r}; worst excess {err:.3e}")
+
+
+def check_stats(w, gpu, ref, seqs=None):
+    """max_logits / exp_sums / tmp_out of every used partition; padding exactly -inf / 0."""
+    atol, rtol = OUT_TOL[w.dtype]
+    seqs = range(w.num_seqs) if seqs is None else seqs
+    for s in seqs:
+        P = -(-int(min(max(int(w.seq_lens[s]), 0), w.max_seq_len)) // 512)
+        for key in ("max_logits", "exp_sums"):
+            g = gpu[key][s, :, :P]
+            r = ref[key][s, :, :P]
+            bad = ~(np.abs(g - r) <= STAT_TOL * np.maximum(np.abs(r), 1.0))
+            if bad.any():
+                idx = tuple(np.argwhere(bad)[0])
+                raise AssertionError(f"{w.name}/{w.layout} {key} seq {s} at {idx}: gpu {g[idx]!r} "
+                                     f"ref {r[idx]!r}")
+        pad_ml = gpu["max_logits"][s, :, P:]
+        pad_es = gpu["exp_sums"][s, :, P:]
+        assert np.all(np.isneginf(pad_ml)), f"{w.name} seq {s}: max_logits padding not -inf"
+        assert np.all(pad_es == 0.0), f"{w.name} seq {s}: exp_sums padding not 0"
+        g = gpu["tmp_out"][s, :, :P]
+        r = ref["tmp_out"][s, :, :P]
+        bad = _violations(g, r, atol, rtol)
+        if bad.any():
+            idx = tuple(np.argwhere(bad)[0])
+            raise AssertionError(f"{w.name}/{w.layout} tmp_out seq {s} at {idx}: gpu {g[idx]!r} "
+                                 f"ref {r[idx]!r}")

@@ -1,0 +1,134 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and exports
+every function include/pa_decode.h declares, the size helpers, the v1/v2
+choice, and the argument checks that return before anything is launched."""
+import ctypes
+import json
+import math
+import pathlib
+import re
+
+import pytest
+
+import paged_kv_attention_v2_gb300 as pa
+from paged_kv_attention_v2_gb300 import _abi
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+GOLDEN = json.loads((ROOT / "tests" / "golden" / "pages_facts.json").read_text())
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_v2_gb300 import build
+    build.build()
+    return _abi.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        text = h.read_text()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(pa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_function(lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(_abi.EXPORTED), declared ^ set(_abi.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.pa_version() >> 16 == 1
+
+
+def test_partition_counts(lib):
+    assert lib.pa_max_num_partitions(0) == 1
+    assert lib.pa_max_num_partitions(1) == 1
+    assert lib.pa_max_num_partitions(512) == 1
+    assert lib.pa_max_num_partitions(513) == 2
+    g = GOLDEN["partitions_at_100k"]
+    assert lib.pa_max_num_partitions(g["seq_len"]) == g["num_partitions"]
+    assert g["full_partitions"] * 512 + g["last_partition_tokens"] == g["seq_len"]
+
+
+def test_workspace_elems(lib):
+    s, t = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.pa_workspace_elems(4, 28, 128, 100000, ctypes.byref(s), ctypes.byref(t)) == 0
+    assert s.value == 4 * 28 * 196 and t.value == 4 * 28 * 196 * 128
+    assert lib.pa_workspace_elems(-1, 28, 128, 10, ctypes.byref(s), ctypes.byref(t)) == 1
+
+
+def test_choose_mode(lib):
+    assert pa.choose_mode(32, 4, 512, 152) == "v1"
+    assert pa.choose_mode(32, 4, 4096, 152) == "v2"
+    assert pa.choose_mode(4, 4, 100000, 152) == "v2"
+
+
+def test_pages_dispatch_rule_worked_example():
+    """The page's own rule and worked example (16-SM part, 4 kv heads): v2 iff
+    num_kv_heads * ceil(seq_len / 512) > 2 * 16, i.e. seq_len > 4096."""
+    g = GOLDEN["dispatch_rule_bi_v100"]
+
+    def pages_rule(seq_len):
+        return g["num_kv_heads"] * math.ceil(seq_len / 512) > g["threshold_factor"] * g["sm_count"]
+
+    for seq_len, expect in g["cases"]:
+        assert pages_rule(seq_len) == expect
+    assert not pages_rule(g["page_threshold_seq_len"]) and pages_rule(g["page_threshold_seq_len"] + 1)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.pa_status_str(code)
+    assert pa.status_str(0) == "ok"
+
+
+def _args(**over):
+    a = _abi.PaDecodeArgs(
+        out=16, query=16, key_cache=16, value_cache=16, block_tables=16, seq_lens=16,
+        num_seqs=2, num_heads=8, num_kv_heads=2, head_size=128, num_blocks=10, block_size=16,
+        max_seq_len=100, max_blocks_per_seq=7, scale=0.1, softcap=0.0, alibi_slopes=None,
+        dtype=_abi.PA_DTYPE_F16, layout=_abi.PA_LAYOUT_SPLIT, mode=_abi.PA_MODE_V2,
+        exp_sums=16, max_logits=16, tmp_out=16)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,expect", [
+    ({"num_heads": 7}, _abi.PA_ERR_INVALID_ARG),           # not a multiple of kv heads
+    ({"num_kv_heads": 0}, _abi.PA_ERR_INVALID_ARG),
+    ({"num_seqs": -1}, _abi.PA_ERR_INVALID_ARG),
+    ({"head_size": 96}, _abi.PA_ERR_UNSUPPORTED),
+    ({"block_size": 32}, _abi.PA_ERR_UNSUPPORTED),
+    ({"num_heads": 34, "num_kv_heads": 2}, _abi.PA_ERR_UNSUPPORTED),   # group 17
+    ({"dtype": 7}, _abi.PA_ERR_INVALID_ARG),
+    ({"layout": 5}, _abi.PA_ERR_INVALID_ARG),
+    ({"mode": 9}, _abi.PA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, _abi.PA_ERR_INVALID_ARG),
+    ({"query": None}, _abi.PA_ERR_INVALID_ARG),
+    ({"block_tables": None}, _abi.PA_ERR_INVALID_ARG),
+    ({"out": 8}, _abi.PA_ERR_INVALID_ARG),                 # misaligned
+    ({"max_blocks_per_seq": 6}, _abi.PA_ERR_INVALID_ARG),  # 6 * 16 < 100
+    ({"num_blocks": 0}, _abi.PA_ERR_INVALID_ARG),
+    ({"tmp_out": None}, _abi.PA_ERR_WORKSPACE),
+    ({"exp_sums": None}, _abi.PA_ERR_WORKSPACE),
+    ({"tmp_out": 24}, _abi.PA_ERR_WORKSPACE),              # misaligned workspace
+    ({"num_seqs": 0}, _abi.PA_OK),                         # empty batch: no-op
+])
+def test_host_argument_checks(lib, over, expect):
+    a = _args(**over)
+    assert lib.pa_decode(ctypes.byref(a), None) == expect
+
+
+def test_null_args(lib):
+    assert lib.pa_decode(None, None) == _abi.PA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(_abi.LibraryMissing):
+        _abi.load(tmp_path / "missing.so")

@@ -1,0 +1,143 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element on the same seeded inputs.
+
+Covers every workload (tiny, gqa4k, long100k, ragged at full size; large_batch
+at full size on sampled sequences the oracle computes one by one), both cache
+layouts, v1 / v2 / auto, and the edge cases: empty and one-token sequences,
+page and partition boundaries, GQA groups from 1 to 16 (two n-tiles),
+head size 64, fp32 / fp16 / bf16, ALiBi, softcap, out-of-range block ids and
+sequence lengths (device error bits, no fault), NaN in unused cache slots.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from parity_util import check_out, check_stats, run_gpu, to_device  # noqa: E402
+
+
+@functools.lru_cache(maxsize=2)
+def _workload(name, layout):
+    return W.make_workload(name, layout)
+
+
+FULL = [("tiny", "split"), ("tiny", "nhd"), ("gqa4k", "split"), ("gqa4k", "nhd"),
+        ("long100k", "split"), ("long100k", "nhd"), ("ragged", "split"), ("ragged", "nhd")]
+
+
+@pytest.mark.parametrize("name,layout", FULL, ids=[f"{n}-{l}" for n, l in FULL])
+def test_workload_parity(name, layout):
+    """Full-size workload, every output and partition statistic, v1 / v2 / auto."""
+    w = _workload(name, layout)
+    ref = oracle.oracle_decode(w)
+    dev = to_device(w)
+    for mode in ("auto", "v1", "v2"):
+        g = run_gpu(w, mode=mode, dev=dev)
+        assert g["dev_error"] == 0, (mode, g["dev_error"])
+        check_out(w, g["out"], ref["out"], what=f"out[{mode}]")
+        if mode == "v2" or (mode == "auto" and w.max_seq_len > 512):
+            check_stats(w, g, ref)
+    del dev
+    torch.cuda.empty_cache()
+
+
+def test_large_batch_sampled():
+    """128 x 16384 bf16 with softcap 30 at full size; the oracle checks sampled
+    sequences, every output row is checked for finiteness and boundedness."""
+    for layout in ("split", "nhd"):
+        w = W.make_workload("large_batch", layout)
+        sample = [0, 41, 86, 127]
+        ref = oracle.oracle_decode(w, seq_subset=sample)
+        g = run_gpu(w, mode="auto")
+        assert g["dev_error"] == 0
+        check_out(w, g["out"], ref["out"], seqs=sample)
+        check_stats(w, g, ref, seqs=sample)
+        vmax = float(np.abs(W.storage_to_f64(w.value_cache[:1024], w.dtype)).max())
+        assert np.all(np.isfinite(g["out"]))
+        ml = g["max_logits"]
+        assert np.nanmax(ml) <= 30.0 + 1e-3  # softcap bounds every logit
+        assert np.abs(g["out"]).max() <= 4 * vmax
+        del w
+
+
+def test_v1_equals_v2():
+    """The page's correctness claim: the partitioned result equals the single pass."""
+    for name in ("gqa4k", "ragged"):
+        w = _workload(name, "split")
+        a = run_gpu(w, mode="v1")["out"]
+        b = run_gpu(w, mode="v2")["out"]
+        atol = 2e-3
+        assert np.all(np.abs(a - b) <= atol + 1e-2 * np.abs(b))
+
+
+EDGE = [
+    # name, dtype, layout, H, Hkv, d, lens, alibi, softcap, mult
+    ("lens_boundaries", "f16", "split", 8, 2, 128, (1, 15, 16, 17, 511, 512, 513, 1024, 1025), False, 0.0, 1.0),
+    ("with_empty", "f16", "nhd", 4, 2, 128, (0, 37, 0, 600), False, 0.0, 1.0),
+    ("group1", "bf16", "split", 4, 4, 128, (100, 700), False, 0.0, 1.0),
+    ("group8", "f16", "nhd", 16, 2, 128, (300, 1500), True, 0.0, 1.0),
+    ("group9_two_ntiles", "f16", "split", 18, 2, 128, (33, 900), False, 0.0, 1.0),
+    ("group16", "bf16", "nhd", 32, 2, 128, (1, 2000), False, 20.0, 2.0),
+    ("head64_f16", "f16", "split", 8, 4, 64, (17, 530, 1200), True, 0.0, 1.0),
+    ("head64_bf16_nhd", "bf16", "nhd", 6, 3, 64, (5, 1030), False, 10.0, 3.0),
+    ("f32_head128", "f32", "split", 6, 2, 128, (40, 555), True, 0.0, 1.0),
+    ("f32_nhd_g16", "f32", "nhd", 16, 1, 64, (3, 1100), False, 5.0, 2.0),
+    ("alibi_softcap", "bf16", "split", 8, 2, 128, (511, 2049), True, 30.0, 2.0),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
+@pytest.mark.parametrize("mode", ["v1", "v2"])
+def test_edge_cases(case, mode):
+    name, dtype, layout, H, Hkv, d, lens, alibi, cap, mult = case
+    spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
+                        head_size=d, dtype=dtype, seq_lens=lens, alibi=alibi, softcap=cap,
+                        value_mult=mult)
+    w = W.make_workload(spec, layout)
+    ref = oracle.oracle_decode(w)
+    g = run_gpu(w, mode=mode)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], ref["out"])
+    if mode == "v2":
+        check_stats(w, g, ref)
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    spec = W.small_spec(name="badblk", num_seqs=2, num_heads=4, num_kv_heads=2, head_size=128,
+                        dtype="f16", seq_lens=(40, 600))
+    w = W.make_workload(spec, "split")
+    dev = to_device(w)
+    bt = dev["block_tables"].clone()
+    bt[1, 3] = w.num_blocks + 7
+    bt[0, 0] = -5
+    for mode in ("v1", "v2"):
+        g = run_gpu(w, mode=mode, dev=dev, block_tables=bt)
+        assert g["dev_error"] & 1, g["dev_error"]
+    # the rest of the batch is still computed: a clean run afterwards matches
+    g = run_gpu(w, mode="v2", dev=dev)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], oracle.oracle_decode(w)["out"])
+
+
+def test_seq_len_beyond_max_is_clamped_and_flagged():
+    spec = W.small_spec(name="badlen", num_seqs=2, num_heads=4, num_kv_heads=2, head_size=128,
+                        dtype="bf16", seq_lens=(700, 1200))
+    w = W.make_workload(spec, "nhd")
+    dev = to_device(w)
+    # max_seq_len 1024 < 1200: sequence 1 is clamped to 1024 tokens
+    for mode in ("v1", "v2"):
+        g = run_gpu(w, mode=mode, dev=dev, max_seq_len=1024)
+        assert g["dev_error"] & 2
+        w2 = W.make_workload(spec, "nhd")
+        w2.seq_lens = np.array([700, 1024], dtype=np.int32)
+        w2.max_seq_len = 1024
+        ref = oracle.oracle_decode(w2)
+        check_out(w2, g["out"], ref["out"])

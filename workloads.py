@@ -28,6 +28,8 @@ valid tokens shows up in the output.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 from typing import Optional
 
@@ -135,8 +137,8 @@ def round_to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f16":
         return x.astype(np.float16)
     if dtype == "bf16":
-        u = x.view(np.uint32).astype(np.uint64)
-        r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+        u = x.view(np.uint32)  # finite inputs: the rounding add cannot overflow 32 bits
+        r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
         return r.astype(np.uint16)
     raise ValueError(dtype)
 
@@ -156,6 +158,14 @@ def _nan_value(dtype: str):
     if dtype == "f16":
         return np.uint16(_NAN_BITS["f16"]).view(np.float16)
     return np.uint16(_NAN_BITS["bf16"])
+
+
+def _gen_threads() -> int:
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        n = os.cpu_count() or 1
+    return max(1, min(32, n))
 
 
 def _rng(seed: int, stream: str, chunk: int = 0) -> np.random.Generator:
@@ -252,22 +262,25 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
     key_cache = np.empty(kshape, dtype=sdt)
     value_cache = np.empty(vshape, dtype=sdt)
     nan = _nan_value(spec.dtype)
-    for c0 in range(0, pool, _CHUNK_BLOCKS):
+
+    def fill(job):
+        c0, which = job
+        dst = key_cache if which == "k" else value_cache
         c1 = min(pool, c0 + _CHUNK_BLOCKS)
         n = c1 - c0
-        for which, dst in (("k", key_cache), ("v", value_cache)):
-            g = _rng(seed, "kv_" + which, c0 // _CHUNK_BLOCKS)
-            x = g.standard_normal((n, hkv, bs, d), dtype=np.float32)
-            if spec.value_mult != 1.0:
-                x *= np.float32(spec.value_mult)
-            st = round_to_storage(x, spec.dtype)
-            if spec.poison:
-                vs = valid_slots[c0:c1]
-                slot = np.arange(bs)[None, :]
-                bad = slot >= vs[:, None]                     # [n, bs]
-                if bad.any():
-                    st[np.broadcast_to(bad[:, None, :, None], st.shape)] = nan
-            dst[c0:c1] = logical_to_layout(st, which, layout, spec.dtype)
+        g = _rng(seed, "kv_" + which, c0 // _CHUNK_BLOCKS)
+        x = g.standard_normal((n, hkv, bs, d), dtype=np.float32)
+        if spec.value_mult != 1.0:
+            x *= np.float32(spec.value_mult)
+        st = round_to_storage(x, spec.dtype)
+        if spec.poison:
+            for i in np.nonzero(valid_slots[c0:c1] < bs)[0]:
+                st[i, :, valid_slots[c0 + i]:, :] = nan
+        dst[c0:c1] = logical_to_layout(st, which, layout, spec.dtype)
+
+    jobs = [(c0, which) for c0 in range(0, pool, _CHUNK_BLOCKS) for which in ("k", "v")]
+    with ThreadPoolExecutor(max_workers=_gen_threads()) as ex:
+        list(ex.map(fill, jobs))
     q = _rng(seed, "query").standard_normal((spec.num_seqs, spec.num_heads, d), dtype=np.float32)
     if spec.value_mult != 1.0:
         q *= np.float32(spec.value_mult)
