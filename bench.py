@@ -249,33 +249,35 @@ def run_ours(args, world, rank, local):
     for a, b in kev:  # torch creates events lazily: record once so the handles exist
         a.record(stream)
         b.record(stream)
-    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+
+    # timed region: exactly K steps back to back (value, ms_per_step)
     barrier()
     torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
     e0.record(stream)
     for j in range(K):
-        step(j, kev[j])
+        step(j)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     t_wall1 = time.time()
     ms_total = e0.elapsed_time(e1)
-    kernel_ms = [a.elapsed_time(b) for a, b in kev]
 
-    # the same K steps without the per-kernel events (diagnostic: event overhead)
+    # the same K steps with CUDA events around the main kernel of every step
+    # (roofline.achieved); the events split the programmatic overlap of the two
+    # kernels, so this pass is reported separately and not used for `value`.
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
     e2.record(stream)
     for j in range(K):
-        step(j)
+        step(j, kev[j])
     e3.record(stream)
     torch.cuda.synchronize(dev)
-    ms_total_plain = e2.elapsed_time(e3)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    ms_total_instrumented = e2.elapsed_time(e3)
     time.sleep(0.15)
     sampler.stop()
-    clocks = sampler.summary(t_soak, t_wall1 + 0.1)
+    clocks = sampler.summary(t_soak, time.time())
 
     derr = int(err.item())
     if derr:
@@ -370,7 +372,7 @@ def run_ours(args, world, rank, local):
                    "l2": f"rotate {copies} KV pools ({copies * pool_bytes} B >= 4x L2 {l2} B)"
                    if copies * pool_bytes >= 4 * l2 else f"{copies} KV pools of {pool_bytes} B",
                    "parallelism": f"replicas x{world}", "clock_soak_s": 0.0 if args.no_soak else 1.0,
-                   "ms_per_step_without_kernel_events": round(ms_total_plain / K, 6)},
+                   "ms_per_step_with_kernel_events": round(ms_total_instrumented / K, 6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "kernel": "pa_partition_kernel" if mode == "v2" else "pa_partition_kernel (v1)",
