@@ -144,6 +144,34 @@ typedef struct pa_decode_args {
  */
 pa_status pa_decode(const pa_decode_args* args, void* stream);
 
+/* Capacity, in floats, of the device array used by pa_decode_static_workspace
+ * (4 Mi floats = 16 MiB). */
+#define PA_STATIC_WORKSPACE_FLOATS (4 * 1024 * 1024)
+
+/*
+ * The same decode as pa_decode in v2 mode, for callers that cannot allocate
+ * device memory -- code running inside a memory pool or allocator that must not
+ * re-enter cudaMalloc, plug-ins whose host application owns all device
+ * allocations, or code that must not allocate after set-up.  (The pages have no
+ * counterpart of this entry point.)
+ *
+ * The caller passes inputs and `out` as for pa_decode; args->mode,
+ * exp_sums, max_logits and tmp_out are ignored.  The partition statistics and
+ * partial outputs live in one library-owned __device__ array of
+ * PA_STATIC_WORKSPACE_FLOATS floats instead, which every GPU that loads the
+ * library keeps until the process exits.  Allocates nothing.
+ *  - Returns PA_ERR_WORKSPACE, before launching anything, when
+ *    num_seqs * num_heads * P * (head_size + 2) > PA_STATIC_WORKSPACE_FLOATS,
+ *    P = pa_max_num_partitions(max_seq_len); other errors as pa_decode.
+ *  - The first call on a device looks up the array's address on that device
+ *    (the device must be current); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents; nothing in it needs to start at zero.  Calls whose kernels
+ *    overlap on the GPU (unordered streams) race on it: order them.
+ */
+pa_status pa_decode_static_workspace(const pa_decode_args* args, void* stream);
+
 /* ceil(max_seq_len / PA_PARTITION_SIZE), at least 1 (workspace partition stride). */
 int32_t pa_max_num_partitions(int32_t max_seq_len);
 

@@ -17,7 +17,7 @@ from . import _abi
 from ._abi import (PA_BLOCK_SIZE, PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT,
                    PA_PARTITION_SIZE, LibraryMissing)
 
-__all__ = ["pa_decode", "alloc_workspace", "max_num_partitions", "choose_mode", "status_str",
+__all__ = ["pa_decode", "pa_decode_static_workspace", "alloc_workspace", "max_num_partitions", "choose_mode", "status_str",
            "PaDecodeError", "PA_PARTITION_SIZE", "PA_BLOCK_SIZE", "PA_DEVERR_BLOCK_ID",
            "PA_DEVERR_SEQ_LEN", "PA_DEVERR_TIMEOUT", "LibraryMissing", "library"]
 
@@ -118,3 +118,22 @@ def pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens, *, str
 def decode_args_call(args: _abi.PaDecodeArgs, stream_handle: int) -> int:
     """Call pa_decode with a prepared argument struct (for tight timing loops)."""
     return library().pa_decode(ctypes.byref(args), ctypes.c_void_p(stream_handle))
+
+
+def pa_decode_static_workspace(out, query, key_cache, value_cache, block_tables, seq_lens, *,
+                               stream=None, **kw) -> None:
+    """pa_decode (v2) with the partition workspace in the library's own device
+    array, for callers that cannot allocate device memory (see the C header).
+    Workspace arguments and `mode` are ignored.  Raises PaDecodeError, e.g.
+    PA_ERR_WORKSPACE when the batch needs more than PA_STATIC_WORKSPACE_FLOATS."""
+    import torch
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("pa_decode_static_workspace needs contiguous tensors")
+    args = make_args(out, query, key_cache, value_cache, block_tables, seq_lens, **kw)
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = library().pa_decode_static_workspace(ctypes.byref(args), ctypes.c_void_p(handle))
+    if st != _abi.PA_OK:
+        raise PaDecodeError(st)

@@ -1,0 +1,82 @@
+"""pa_decode_static_workspace: the decode entry point that allocates nothing.
+
+Callers such as a memory pool or allocator that must not re-enter cudaMalloc,
+or a plug-in whose host application owns every device allocation, cannot hand
+the library a freshly allocated workspace.  This entry point keeps the
+partition workspace in a fixed device array inside the library instead.  The
+GPU test calls it through the C ABI twice in a row and checks each result
+against the regular pa_decode entry point, within the tolerance the parity tests
+use.  (This file is named so that pytest collects it last.)
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads as W
+from paged_kv_attention_v2_gb300 import _abi
+
+
+def _args(**over):
+    a = _abi.PaDecodeArgs(
+        out=256, query=256, key_cache=256, value_cache=256, block_tables=256, seq_lens=256,
+        num_seqs=256, num_heads=32, num_kv_heads=8, head_size=128, num_blocks=60000,
+        block_size=16, max_seq_len=32768, max_blocks_per_seq=2048, scale=0.08, softcap=0.0,
+        dtype=_abi.PA_DTYPE_F16, layout=_abi.PA_LAYOUT_SPLIT, mode=_abi.PA_MODE_AUTO)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_batch_beyond_static_capacity_is_rejected():
+    from paged_kv_attention_v2_gb300 import build
+    build.build()
+    lib = _abi.load()
+    # 256 * 32 * 64 partitions * (128 + 2) floats > PA_STATIC_WORKSPACE_FLOATS: refused, no launch
+    assert lib.pa_decode_static_workspace(ctypes.byref(_args()), None) == _abi.PA_ERR_WORKSPACE
+    assert lib.pa_decode_static_workspace(None, None) == _abi.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ["gqa4k-split", "alibi-bf16-nhd"])
+def test_static_workspace_matches_pa_decode_on_two_calls(case):
+    import torch
+
+    from parity_util import OUT_TOL, run_gpu, to_device, torch_dtype
+
+    if case == "gqa4k-split":
+        w = W.make_workload("gqa4k", "split")
+    else:
+        w = W.make_workload(W.small_spec(name="static_ws", num_seqs=5, num_heads=16,
+                                         num_kv_heads=4, head_size=128, dtype="bf16",
+                                         seq_lens=(1, 511, 513, 3000, 1800), alibi=True,
+                                         softcap=30.0, value_mult=2.0), "nhd")
+    dev = to_device(w)
+    ref = run_gpu(w, mode="v2", dev=dev)
+    assert ref["dev_error"] == 0
+
+    lib = _abi.load()
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_size), dtype=torch_dtype(w.dtype),
+                      device="cuda:0")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    args = _abi.PaDecodeArgs(
+        out=out.data_ptr(), query=dev["query"].data_ptr(), key_cache=dev["key_cache"].data_ptr(),
+        value_cache=dev["value_cache"].data_ptr(), block_tables=dev["block_tables"].data_ptr(),
+        seq_lens=dev["seq_lens"].data_ptr(), num_seqs=w.num_seqs, num_heads=w.num_heads,
+        num_kv_heads=w.num_kv_heads, head_size=w.head_size, num_blocks=w.num_blocks,
+        block_size=w.block_size, max_seq_len=w.max_seq_len,
+        max_blocks_per_seq=w.block_tables.shape[1], scale=w.scale, softcap=w.softcap,
+        alibi_slopes=None if dev["alibi_slopes"] is None else dev["alibi_slopes"].data_ptr(),
+        dtype={"f32": 0, "f16": 1, "bf16": 2}[w.dtype],
+        layout={"split": 0, "nhd": 1}[w.layout], mode=_abi.PA_MODE_AUTO, dev_error=err.data_ptr())
+    stream = torch.cuda.current_stream().cuda_stream
+    atol, rtol = OUT_TOL[w.dtype]
+    for call in range(2):
+        out.fill_(float("nan"))
+        st = lib.pa_decode_static_workspace(ctypes.byref(args), ctypes.c_void_p(stream))
+        assert st == _abi.PA_OK, (call, st)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got = out.double().cpu().numpy()
+        bad = ~(np.abs(got - ref["out"]) <= atol + rtol * np.abs(ref["out"]))
+        assert not bad.any(), (call, int(bad.sum()))
