@@ -34,6 +34,26 @@ constexpr int kNHD = PA_LAYOUT_NHD;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Build-time shape of the partition kernel (overridable with -D for sweeps).
+#ifndef PA_STAGES_16BIT
+#define PA_STAGES_16BIT 8      // ring stages (one 16-token page of K and V each), 16-bit caches
+#endif
+#ifndef PA_STAGES_F32
+#define PA_STAGES_F32 4        // ring stages, fp32 caches
+#endif
+#ifndef PA_CONSUMER_WARPS
+#define PA_CONSUMER_WARPS 4    // consumer warps per CTA
+#endif
+#ifndef PA_MIN_CTAS_PER_SM
+#define PA_MIN_CTAS_PER_SM 1   // __launch_bounds__ minimum resident CTAs
+#endif
+#ifndef PA_MAX_CTAS_PER_SM
+#define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
+#endif
+#ifndef PA_REDUCE_WARPS
+#define PA_REDUCE_WARPS 8      // warps per reduce CTA
+#endif
+
 struct Params {
     const void* query;
     const void* key_cache;
@@ -93,6 +113,14 @@ struct Cfg {
     static constexpr int kSmemBytes = oAbort + 16 + 1024;  // + slack for 1024-B alignment
 
     static_assert(kPageBytes % 1024 == 0 || !kTensorMap, "swizzled pages need 1024-B alignment");
+    // Within a tile, page j goes to consumer warp j % NC and to ring stage
+    // (base + j) % STAGES.  With STAGES a multiple of NC every page of a stage
+    // inside one tile belongs to the same warp, so no warp ever waits on a
+    // stage's full barrier more than one phase ahead (a parity wait cannot
+    // tell phase n from phase n + 2).  Across tiles the tile-end barrier of
+    // the consumer warps gives the same guarantee.
+    static_assert(STAGES % NC == 0, "ring stages must be a multiple of the consumer warps");
+    static_assert(STAGES <= 32, "one producer lane per stage");
     static_assert(kQBytes % 16 == 0, "bulk copy size");
 };
 
@@ -126,6 +154,11 @@ __device__ __forceinline__ bool consumer_sync(const Smem& sm, uint32_t& phase, i
 
 // ------------------------------------------------------------------ producer
 
+struct ProducerTile {
+    int seq, kvh, part, tb, te, len, npages;
+    bool valid;
+};
+
 template <class C, int HEAD, int STAGES>
 __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk,
                          const CUtensorMap* tmv, int lane) {
@@ -158,71 +191,95 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     };
     load_chunk(0);
 
-    uint32_t g = 0;  // pages issued by this CTA
-    int k = 0;       // tiles issued by this CTA
-    bool ok = true;
-    for (int tile = blockIdx.x;; tile += gridDim.x) {
+    // Tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ... (kv head fastest).
+    int tile = blockIdx.x;
+    auto next_tile = [&]() {
+        ProducerTile t;
+        t.valid = false;
+        t.seq = t.part = t.tb = t.te = t.len = t.npages = 0;
         const int u = tile / Hkv;
-        const int kvh = tile - u * Hkv;
+        t.kvh = tile - u * Hkv;
+        tile += gridDim.x;
         while (cb < S && u >= cu + c_total) {
             cu += c_total;
             cb += 32;
             load_chunk(cb);
         }
-        if (cb >= S) break;
+        if (cb >= S) return t;
         const int rel = u - cu;
         const unsigned hit = __ballot_sync(0xffffffffu, c_incl > rel);
         const int j = __ffs(hit) - 1;
-        const int seq = cb + j;
+        t.seq = cb + j;
         const int excl = __shfl_sync(0xffffffffu, c_incl - c_units, j);
-        const int len = __shfl_sync(0xffffffffu, c_len, j);
-        const int part = rel - excl;
-        const int tb = p.v1 ? 0 : part * kPart;
-        const int te = p.v1 ? len : min(len, tb + kPart);
-        const int npages = (te - tb + kBS - 1) / kBS;
+        t.len = __shfl_sync(0xffffffffu, c_len, j);
+        t.part = rel - excl;
+        t.tb = p.v1 ? 0 : t.part * kPart;
+        t.te = p.v1 ? t.len : min(t.len, t.tb + kPart);
+        t.npages = (t.te - t.tb + kBS - 1) / kBS;
+        t.valid = true;
+        return t;
+    };
+    // Block ids of pages [pc, pc + 32) of tile t, one per lane (range-checked).
+    auto load_ids = [&](const ProducerTile& t, int pc) {
+        int blk = 0;
+        if (t.valid && pc + lane < t.npages) {
+            blk = __ldg(p.block_tables + (int64_t)t.seq * p.max_blocks_per_seq + t.tb / kBS + pc + lane);
+            if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                report(p, PA_DEVERR_BLOCK_ID);
+                blk = 0;
+            }
+        }
+        return blk;
+    };
+
+    uint32_t g = 0;  // pages issued by this CTA
+    int k = 0;       // tiles issued by this CTA
+    bool ok = true;
+    ProducerTile cur = next_tile();
+    int ids = load_ids(cur, 0);
+    while (ok && cur.valid) {
+        const ProducerTile nxt = next_tile();  // walk ahead while this tile's pages stream
 
         const int slot = k % C::kTD;
         if (lane == 0) {
             ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, kWaitLimitNs);
             if (ok) {
                 TileDesc& d = sm.desc[slot];
-                d.seq = seq;
-                d.kvh = kvh;
-                d.part = part;
-                d.tok_begin = tb;
-                d.tok_end = te;
-                d.len = len;
+                d.seq = cur.seq;
+                d.kvh = cur.kvh;
+                d.part = cur.part;
+                d.tok_begin = cur.tb;
+                d.tok_end = cur.te;
+                d.len = cur.len;
                 d.flags = 0;
                 mbar_arrive_expect_tx(sm.td_full + slot * 8, qbytes);
                 bulk_g2s(sm.q + slot * C::kQBytes,
-                         qbase + ((int64_t)seq * p.num_heads + (int64_t)kvh * p.group) * HEAD * C::kElem,
+                         qbase + ((int64_t)cur.seq * p.num_heads + (int64_t)cur.kvh * p.group) * HEAD * C::kElem,
                          qbytes, sm.td_full + slot * 8);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
 
-        const int32_t* row = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + tb / kBS;
-        for (int pc = 0; pc < npages && ok; pc += 32) {
-            const int n = min(32, npages - pc);
-            int blk = 0;
-            if (lane < n) {
-                blk = __ldg(row + pc + lane);
-                if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                    report(p, PA_DEVERR_BLOCK_ID);
-                    blk = 0;
-                }
-            }
-            for (int jj = 0; jj < n; ++jj) {
-                const int b = __shfl_sync(0xffffffffu, blk, jj);
-                if (lane == 0) {
-                    const uint32_t st = g % STAGES, ph = (g / STAGES) & 1;
-                    ok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, kWaitLimitNs);
-                    if (ok) {
+        for (int pc = 0; pc < cur.npages && ok; pc += 32) {
+            const int n = min(32, cur.npages - pc);
+            // block ids of the next 32 pages (this tile or the next one), loaded early
+            const int ids_next = (pc + 32 < cur.npages) ? load_ids(cur, pc + 32) : load_ids(nxt, 0);
+            // Issue in batches of up to STAGES pages, one page per lane: the
+            // pages of a batch sit in distinct stages, so each lane waits for
+            // exactly the previous use of its own stage.
+            for (int b0 = 0; b0 < n && ok; b0 += STAGES) {
+                const int nb = min(STAGES, n - b0);
+                const int b = __shfl_sync(0xffffffffu, ids, (b0 + lane) & 31);
+                bool lok = true;
+                if (lane < nb) {
+                    const uint32_t gg = g + (uint32_t)lane;
+                    const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+                    lok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, kWaitLimitNs);
+                    if (lok) {
                         const uint32_t fb = sm.full + st * 8;
                         const uint32_t dk = sm.ring + st * C::kStageBytes;
                         const uint32_t dv = dk + C::kPageBytes;
-                        const int64_t page = (int64_t)b * Hkv + kvh;
+                        const int64_t page = (int64_t)b * Hkv + cur.kvh;
                         mbar_arrive_expect_tx(fb, C::kStageBytes);
                         if constexpr (C::kTensorMap) {
                             const int y = (int)(page * kBS);
@@ -237,13 +294,14 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                         }
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                ++g;
+                ok = __all_sync(0xffffffffu, lok);
+                g += (uint32_t)nb;
             }
+            ids = ids_next;
         }
-        if (!ok) break;
+        if (cur.npages == 0) ids = load_ids(nxt, 0);
         ++k;
+        cur = nxt;
     }
 
     if (lane == 0) {
@@ -465,17 +523,28 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             }
 
             // S^T[token][head] = K . Q^T
-            float s[NT][4];
+            // two accumulator chains (even / odd k-steps) for MMA latency hiding
+            float s[NT][4], s2[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_16816<BF>(s[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (kk & 1)
+                        mma_16816<BF>(s2[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                    else
+                        mma_16816<BF>(s[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
 
             // logits, online softmax, P as B fragments of P.V
             const int tlo = tok0 + r;  // this thread's tokens: tlo (e=0,1), tlo+8 (e=2,3)
@@ -757,7 +826,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 // ------------------------------------------------------------------ kernels
 
 template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32, 1)
+__global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
@@ -814,13 +883,18 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     }
 }
 
-// Phase 2: one CTA of 128 threads per (sequence, head).
-template <typename T, int HEAD>
-__global__ void __launch_bounds__(128) pa_reduce_kernel(const Params p) {
+// Phase 2: one CTA of 32*WARPS threads per (sequence, head).  Each lane owns
+// four head dims (a float4 column) of one partition row and keeps U partition
+// rows in flight, so a long sequence (hundreds of partitions) is read with
+// WARPS*U*(32/(HEAD/4)) independent 512-byte row loads per round.
+template <typename T, int HEAD, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     constexpr int D4 = HEAD / 4;          // float4 columns of a partition row
-    constexpr int RPW = 32 / D4;          // partition rows per warp step (1 or 2)
-    constexpr int RSTEP = 4 * RPW;        // partition rows per CTA step
-    __shared__ float red[4];
+    constexpr int RPW = 32 / D4;          // partition rows per warp (1 or 2)
+    constexpr int RSTEP = WARPS * RPW;    // partition rows per CTA round
+    constexpr int U = 4;                  // rounds in flight
+    constexpr int NT = WARPS * 32;
+    __shared__ float red[WARPS];
     __shared__ float4 part[RSTEP][D4];
 
     const int bid = blockIdx.x;
@@ -837,35 +911,58 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const Params p) {
     T* o = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + h) * HEAD;
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    float W = 0.f;
     if (P > 0) {
         float M = -INFINITY;
-        for (int q = tid; q < P; q += 128) M = fmaxf(M, ml[q]);
+        for (int q = tid; q < P; q += NT) M = fmaxf(M, ml[q]);
 #pragma unroll
         for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         if (lane == 0) red[warp] = M;
         __syncthreads();
-        M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        M = red[0];
+#pragma unroll
+        for (int w = 1; w < WARPS; ++w) M = fmaxf(M, red[w]);
         __syncthreads();
 
-        const int rowi = warp * RPW + lane / D4, d4 = lane % D4;
-        for (int q = rowi; q < P; q += RSTEP) {
-            const float c = expf(ml[q] - M) * es[q];
-            const float4 t4 = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD + 4 * d4);
-            a.x += c * t4.x;
-            a.y += c * t4.y;
-            a.z += c * t4.z;
-            a.w += c * t4.w;
+        const int row = warp * RPW + lane / D4, d4 = lane % D4;
+        float W = 0.f;  // sum of weights (kept by the d4 == 0 lane of each row)
+        for (int q0 = row; q0 < P; q0 += RSTEP * U) {
+            float mq[U], eq[U];
+            float4 t[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int q = q0 + u * RSTEP;
+                if (q < P) {
+                    mq[u] = ml[q];
+                    eq[u] = es[q];
+                    t[u] = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD + 4 * d4);
+                } else {
+                    mq[u] = -INFINITY;
+                    eq[u] = 0.f;
+                    t[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float c = (mq[u] == -INFINITY) ? 0.f : expf(mq[u] - M) * eq[u];
+                a.x += c * t[u].x;
+                a.y += c * t[u].y;
+                a.z += c * t[u].z;
+                a.w += c * t[u].w;
+                W += c;
+            }
         }
-        for (int q = tid; q < P; q += 128) W += expf(ml[q] - M) * es[q];
+        if (d4 != 0) W = 0.f;
 #pragma unroll
         for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
         if (lane == 0) red[warp] = W;
-        part[rowi][d4] = a;
+        part[row][d4] = a;
         __syncthreads();
-        W = (red[0] + red[1]) + (red[2] + red[3]);
+        W = 0.f;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) W += red[w];
         if (tid < D4) {
             float4 sum = part[0][tid];
+#pragma unroll
             for (int i = 1; i < RSTEP; ++i) {
                 const float4 v = part[i][tid];
                 sum.x += v.x;
@@ -879,7 +976,7 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const Params p) {
         // statistics: sequence frame -> absolute ALiBi positions
         if (p.alibi) {
             const float shift = __ldg(p.alibi + h) * (float)(len - 1);
-            for (int q = tid; q < P; q += 128) ml[q] += shift;
+            for (int q = tid; q < P; q += NT) ml[q] += shift;
         }
     }
     if (tid < D4) {
@@ -894,7 +991,7 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const Params p) {
             *reinterpret_cast<uint2*>(dst) = v;
         }
     }
-    for (int q = P + tid; q < p.max_parts; q += 128) {
+    for (int q = P + tid; q < p.max_parts; q += NT) {
         ml[q] = -INFINITY;
         es[q] = 0.f;
     }

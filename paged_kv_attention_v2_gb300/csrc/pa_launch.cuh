@@ -29,8 +29,8 @@ constexpr int kMaxDevices = 64;
 
 template <typename T, int HEAD, int NT, int LAYOUT>
 cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
-    constexpr int STAGES = std::is_same<T, float>::value ? 4 : 8;
-    constexpr int NC = 4;
+    constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32 : PA_STAGES_16BIT;
+    constexpr int NC = PA_CONSUMER_WARPS;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
     auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC>;
 
@@ -47,6 +47,7 @@ cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
         if (occ < 1) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < kMaxDevices) occ_cache[dev].store(occ);
     }
+    if (PA_MAX_CTAS_PER_SM > 0 && occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
     int64_t grid = (int64_t)la.sm_count * occ;
     if (la.grid_override > 0) grid = la.grid_override;
     if (grid > la.tiles_upper) grid = la.tiles_upper;
@@ -76,7 +77,7 @@ template <typename T, int HEAD>
 cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((int64_t)p.num_seqs * p.num_heads));
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(PA_REDUCE_WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = la.stream;
     cudaLaunchAttribute attr[1];
@@ -84,7 +85,7 @@ cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD>, p);
+    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD, PA_REDUCE_WARPS>, p);
 }
 
 template <typename T, int HEAD, int NT>
