@@ -205,6 +205,7 @@ def run_ours(args, world, rank, local):
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     mode = args.mode if args.mode != "auto" else pa.choose_mode(w.num_seqs, w.num_kv_heads,
                                                                  w.max_seq_len, sm_count)
+    fused = False  # no partition counters: v2 always launches the reduce kernel
     common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
                   alibi_slopes=al, softcap=w.softcap, layout=w.layout, mode=mode,
                   dev_error=err, **ws)
@@ -368,7 +369,8 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: seeded N(0,1) inputs rounded to the storage dtype, shuffled block tables",
         "config": {"workload": W.DESCRIPTIONS[w.name], "name": w.name, "layout": w.layout,
-                   "mode": mode, "kv_bytes_per_step": kv, "total_bytes_per_step": int(total_bytes),
+                   "mode": mode, "merge": ("in the partition kernel" if fused else "reduce kernel")
+                   if mode == "v2" else "none (v1)", "kv_bytes_per_step": kv, "total_bytes_per_step": int(total_bytes),
                    "l2": f"rotate {copies} KV pools ({copies * pool_bytes} B >= 4x L2 {l2} B)"
                    if copies * pool_bytes >= 4 * l2 else f"{copies} KV pools of {pool_bytes} B",
                    "parallelism": f"replicas x{world}", "clock_soak_s": 0.0 if args.no_soak else 1.0,
@@ -380,7 +382,7 @@ def run_ours(args, world, rank, local):
                      "traffic": recorded_traffic(w.name, w.layout, mode)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (2 if mode == "v2" else 1),
+        "gpu_launches": K * (2 if mode == "v2" and not fused else 1),
         "clocks": clocks,
     }
     return line

@@ -135,7 +135,23 @@ typedef struct pa_decode_args {
      * after the main (partition or v1) kernel, for timing; NULL = none. */
     void* event_main_begin;
     void* event_main_end;
+    /* Optional [num_seqs][num_kv_heads] int32 partition counters, all zero
+     * before the first call.  When given, the v2 path has at most
+     * PA_FUSED_MAX_PARTITIONS partitions per sequence and the whole batch fits
+     * in one round of the persistent grid (num_seqs * num_kv_heads * P no more
+     * than the resident CTAs), the Phase 2 merge of a (sequence, kv head) is
+     * done inside the partition kernel by the CTA that finishes its last
+     * partition, and no second kernel is launched; otherwise the counters are
+     * not touched.  Each completed call leaves every counter at zero again;
+     * after a PA_DEVERR_TIMEOUT the caller must zero them.  Calls that share
+     * counters must not overlap on the GPU.  NULL = separate reduce kernel. */
+    int32_t* partition_counters;
 } pa_decode_args;
+
+/* Largest partition count per sequence for which the merge runs inside the
+ * partition kernel (longer sequences use the separate reduce kernel, whose
+ * many CTAs read the partitions of one sequence in parallel). */
+#define PA_FUSED_MAX_PARTITIONS 8
 
 /*
  * Paged decode attention (the whole operation: partition kernel + reduce for

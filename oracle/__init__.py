@@ -52,6 +52,7 @@ class OracleArgs(ctypes.Structure):
         ("layout", ctypes.c_int32),
         ("scale", ctypes.c_double),
         ("softcap", ctypes.c_double),
+        ("window_left", ctypes.c_int32),
         ("seq_subset", ctypes.c_void_p),
         ("n_subset", ctypes.c_int32),
         ("num_threads", ctypes.c_int32),
@@ -151,6 +152,7 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
         max_blocks_per_seq=bt.shape[1], partition_size=partition_size,
         max_num_partitions=P, dtype=DTYPE_CODE[w.dtype], layout=LAYOUT_CODE[w.layout],
         scale=float(w.scale), softcap=float(w.softcap),
+        window_left=int(getattr(w, "window_left", -1)),
         seq_subset=_ptr(sub), n_subset=0 if sub is None else len(sub),
         num_threads=threads or default_threads(),
         out=_ptr(res["out"]),

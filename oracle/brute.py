@@ -70,13 +70,18 @@ def brute_decode(w, partition_size: int = 512):
             continue
         keys, values = _gather(w, s)
         n_parts = (L + partition_size - 1) // partition_size
+        # sliding window: the query (position L-1) sees keys t >= L-1-window_left
+        wl = getattr(w, "window_left", -1)
+        lo = max(0, L - 1 - wl) if wl >= 0 else 0
         for h in range(H):
             kvh = h // group            # repeat_interleave of kv heads
             q = [float(v) for v in q_all[s, h]]
             slope = None if w.alibi_slopes is None else float(w.alibi_slopes[h])
             part_max, part_sum, part_out = [], [], []
             for p in range(n_parts):
-                start, end = p * partition_size, min((p + 1) * partition_size, L)
+                start, end = max(p * partition_size, lo), min((p + 1) * partition_size, L)
+                if start >= end:
+                    continue  # partition wholly before the window: unused
                 scores = []
                 for t in range(start, end):
                     z = w.scale * sum(q[i] * keys[t][kvh][i] for i in range(d))
@@ -102,6 +107,6 @@ def brute_decode(w, partition_size: int = 512):
             gmax = max(part_max)
             resc = [math.exp(m - gmax) * e for m, e in zip(part_max, part_sum)]
             total = sum(resc)
-            out[s][h] = [sum(resc[p] * part_out[p][i] for p in range(n_parts)) / total
+            out[s][h] = [sum(resc[j] * part_out[j][i] for j in range(len(part_out))) / total
                          for i in range(d)]
     return {"out": out, "max_logits": ml, "exp_sums": es, "tmp_out": tmp}

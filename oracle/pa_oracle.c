@@ -30,6 +30,11 @@
  *    softmax -- so the dense result out = sum exp(z - Z) v / sum exp(z - Z)
  *    is computed independently and both are returned.
  *  - Unused partitions (p >= ceil(seq_len/512)): m = -inf, e = 0, tmp = 0.
+ *  - "ex_engine/factors/attn_dispatch.py", AttnDispatchConfig window_left /
+ *    window_right (-1 = no window), passed to the decode call: the single
+ *    query token sits at position seq_len - 1 and attends the keys
+ *    t >= seq_len - 1 - window_left (window_right cannot matter: no key lies
+ *    after the query).  Partitions with no key inside the window are unused.
  *
  * Readings where the pages are silent or inconsistent (each is listed in
  * the design doc as well):
@@ -132,9 +137,13 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
     double* out_v2 = a->out_v2 ? a->out_v2 + qoff : NULL;
     const int64_t stat_off = ((int64_t)s * a->num_heads + h) * P_max;
     const int num_parts = (len + PS - 1) / PS;
+    /* first key inside the sliding window (0 without a window) */
+    int t_lo = 0;
+    if (a->window_left >= 0 && len - 1 - a->window_left > 0) t_lo = len - 1 - a->window_left;
 
-    /* unused partitions */
-    for (int p = num_parts; p < P_max; ++p) {
+    /* unused partitions: beyond the sequence, or wholly before the window */
+    for (int p = 0; p < P_max; ++p) {
+        if (p < num_parts && (p + 1) * PS > t_lo) continue;
         if (a->max_logits) a->max_logits[stat_off + p] = -INFINITY;
         if (a->exp_sums) a->exp_sums[stat_off + p] = 0.0;
         if (a->tmp_out)
@@ -148,7 +157,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
 
     /* logits */
     double Z = -INFINITY;
-    for (int t = 0; t < len; ++t) {
+    for (int t = t_lo; t < len; ++t) {
         int64_t blk = table[t / a->block_size];
         int o = t % a->block_size;
         double dot = 0.0;
@@ -165,7 +174,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
     /* dense softmax-weighted sum of V */
     double denom = 0.0;
     for (int d = 0; d < d_sz; ++d) out[d] = 0.0;
-    for (int t = 0; t < len; ++t) {
+    for (int t = t_lo; t < len; ++t) {
         int64_t blk = table[t / a->block_size];
         int o = t % a->block_size;
         double w = exp(sc->z[t] - Z);
@@ -181,6 +190,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
     double M = -INFINITY;
     for (int p = 0; p < num_parts; ++p) {
         int t0 = p * PS, t1 = t0 + PS < len ? t0 + PS : len;
+        if (t0 < t_lo) t0 = t_lo;
         double m = -INFINITY;
         for (int t = t0; t < t1; ++t) if (sc->z[t] > m) m = sc->z[t];
         if (m > M) M = m;
@@ -189,6 +199,8 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
     if (out_v2) for (int d = 0; d < d_sz; ++d) out_v2[d] = 0.0;
     for (int p = 0; p < num_parts; ++p) {
         int t0 = p * PS, t1 = t0 + PS < len ? t0 + PS : len;
+        if (t0 < t_lo) t0 = t_lo;
+        if (t0 >= t1) continue;   /* wholly before the window: unused (written above) */
         double m = -INFINITY;
         for (int t = t0; t < t1; ++t) if (sc->z[t] > m) m = sc->z[t];
         double e = 0.0;

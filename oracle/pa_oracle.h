@@ -31,6 +31,7 @@ typedef struct oracle_args {
     int32_t partition_size, max_num_partitions;
     int32_t dtype, layout;
     double scale, softcap;
+    int32_t window_left;          /* < 0: no window; else keys t >= seq_len - 1 - window_left */
     /* optional subset of sequences to evaluate (NULL = all) */
     const int32_t* seq_subset;
     int32_t n_subset;

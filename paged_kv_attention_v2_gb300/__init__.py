@@ -54,11 +54,17 @@ def _dtype_code(t):
             torch.bfloat16: _abi.PA_DTYPE_BF16}[t.dtype]
 
 
-def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device):
-    """torch-allocated v2 workspace: dict(exp_sums, max_logits, tmp_out)."""
+def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device,
+                    num_kv_heads: int | None = None):
+    """torch-allocated v2 workspace: dict(exp_sums, max_logits, tmp_out), plus
+    zeroed partition_counters when num_kv_heads is given (fused merge)."""
     import torch
     P = max_num_partitions(max_seq_len)
-    return {
+    extra = {}
+    if num_kv_heads is not None:
+        extra["partition_counters"] = torch.zeros((num_seqs, num_kv_heads), dtype=torch.int32,
+                                                  device=device)
+    return {**extra,
         "exp_sums": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
         "max_logits": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
         "tmp_out": torch.empty((num_seqs, num_heads, P, head_size), dtype=torch.float32,
@@ -74,7 +80,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               scale: float, max_seq_len: int, block_size: int = PA_BLOCK_SIZE,
               alibi_slopes=None, softcap: float = 0.0, layout: str = "split", mode: str = "auto",
               exp_sums=None, max_logits=None, tmp_out=None, dev_error=None,
-              event_begin=None, event_end=None) -> _abi.PaDecodeArgs:
+              event_begin=None, event_end=None, partition_counters=None) -> _abi.PaDecodeArgs:
     """Build the C argument struct (no checks beyond shapes; the library validates)."""
     num_seqs, num_heads, head_size = query.shape
     num_blocks = key_cache.shape[0]
@@ -89,6 +95,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         max_logits=_ptr(max_logits), tmp_out=_ptr(tmp_out), dev_error=_ptr(dev_error),
         event_main_begin=None if event_begin is None else event_begin.cuda_event,
         event_main_end=None if event_end is None else event_end.cuda_event,
+        partition_counters=_ptr(partition_counters),
     )
 
 

@@ -35,6 +35,7 @@ EXPORTED = ("pa_decode", "pa_max_num_partitions", "pa_workspace_elems", "pa_choo
             "pa_status_str", "pa_version", "pa_decode_static_workspace")
 
 PA_STATIC_WORKSPACE_FLOATS = 4 * 1024 * 1024
+PA_FUSED_MAX_PARTITIONS = 8
 
 
 class PaDecodeArgs(ctypes.Structure):
@@ -65,6 +66,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("dev_error", ctypes.c_void_p),
         ("event_main_begin", ctypes.c_void_p),
         ("event_main_end", ctypes.c_void_p),
+        ("partition_counters", ctypes.c_void_p),
     ]
 
 

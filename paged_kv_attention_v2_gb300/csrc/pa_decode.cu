@@ -150,7 +150,7 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
         return PA_ERR_INVALID_ARG;
     if (!aligned(a->out, 16) || !aligned(a->query, 16) || !aligned(a->key_cache, 16) ||
         !aligned(a->value_cache, 16) || !aligned(a->block_tables, 4) || !aligned(a->seq_lens, 4) ||
-        !aligned(a->alibi_slopes, 4))
+        !aligned(a->alibi_slopes, 4) || !aligned(a->partition_counters, 4))
         return PA_ERR_INVALID_ARG;
 
     int sm = 0;
@@ -196,6 +196,8 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.softcap = a->softcap > 0.f ? a->softcap : 0.f;
     p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
     p.v1 = v1 ? 1 : 0;
+    p.counters = a->partition_counters;
+    p.fused = 0;  // decided at launch, once the persistent grid size is known
 
     alignas(64) CUtensorMap tmk, tmv;
     std::memset(&tmk, 0, sizeof tmk);

@@ -50,9 +50,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 #ifndef PA_MAX_CTAS_PER_SM
 #define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
 #endif
-#ifndef PA_REDUCE_WARPS
-#define PA_REDUCE_WARPS 8      // warps per reduce CTA
-#endif
 
 struct Params {
     const void* query;
@@ -70,6 +67,8 @@ struct Params {
     int num_blocks, max_blocks_per_seq, max_seq_len, max_parts;
     float scale, softcap, inv_softcap;
     int v1;
+    int32_t* counters;  // [num_seqs][num_kv_heads] finished partitions (fused v2 only)
+    int fused;          // v2 with the log-sum-exp merge done by the last CTA of each (seq, kv head)
 };
 
 struct TileDesc {
@@ -133,7 +132,7 @@ struct Smem {
     TileDesc* desc;
     uint32_t full, empty, td_full, td_empty;  // shared addresses of barrier arrays
     uint32_t merge_bar;  // consumer warps: partial states written / epilogue reads done
-    volatile int* abort;
+    volatile int* abort;     // [0] give-up flag, [1] never set (drain waits), [2] last-arriver flag
 };
 
 // Bounded wait by every lane of a warp; the result is the same in all lanes.
@@ -179,7 +178,10 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
             const int raw = __ldg(p.seq_lens + s);
             c_len = clamp_len(p, raw);
             if (c_len != raw) report(p, PA_DEVERR_SEQ_LEN);
+            // v1: one tile per sequence; v2: one per partition (fused v2 keeps one
+            // empty tile for an empty sequence so that its output row is written)
             c_units = p.v1 ? 1 : (c_len + kPart - 1) / kPart;
+            if (p.fused && c_units == 0) c_units = 1;
         }
         c_incl = c_units;
 #pragma unroll
@@ -385,6 +387,120 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
             }
         }
     }
+}
+
+// Fused v2 merge, run by the NC consumer warps of the CTA that finished the
+// last partition of (d.seq, d.kvh): Phase 2 for the group's heads, reading the
+// partition statistics the other CTAs wrote (L2 loads: never a stale L1 line).
+template <typename T, int HEAD, int NC>
+__device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
+    constexpr int D4 = HEAD / 4;
+    const int G = p.group;
+    const int P = (d.len + kPart - 1) / kPart;
+    for (int idx = tid; idx < G * D4; idx += NC * 32) {
+        const int h = idx / D4, d4 = idx - h * D4;
+        const int64_t sh = (int64_t)d.seq * p.num_heads + d.kvh * G + h;
+        const float* ml = p.max_logits + sh * p.max_parts;
+        const float* es = p.exp_sums + sh * p.max_parts;
+        const float* tmp = p.tmp_out + sh * p.max_parts * HEAD + 4 * d4;
+        float M = -INFINITY, W = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < P; q0 += 4) {
+            float mq[4], eq[4];
+            float4 t[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + u;
+                if (q < P) {
+                    mq[u] = __ldcg(ml + q);
+                    eq[u] = __ldcg(es + q);
+                    t[u] = __ldcg(reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD));
+                } else {
+                    mq[u] = -INFINITY;
+                    eq[u] = 0.f;
+                    t[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (mq[u] == -INFINITY) continue;
+                if (mq[u] > M) {  // online rescale to the new running max
+                    const float sc = (M == -INFINITY) ? 0.f : expf(M - mq[u]);
+                    a.x *= sc;
+                    a.y *= sc;
+                    a.z *= sc;
+                    a.w *= sc;
+                    W *= sc;
+                    M = mq[u];
+                }
+                const float c = expf(mq[u] - M) * eq[u];
+                a.x += c * t[u].x;
+                a.y += c * t[u].y;
+                a.z += c * t[u].z;
+                a.w += c * t[u].w;
+                W += c;
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        T* dst = static_cast<T*>(p.out) + sh * HEAD + 4 * d4;
+        if constexpr (std::is_same<T, float>::value) {
+            *reinterpret_cast<float4*>(dst) = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+        } else {
+            constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+            uint2 v;
+            v.x = pack2<BF>(a.x * inv, a.y * inv);
+            v.y = pack2<BF>(a.z * inv, a.w * inv);
+            *reinterpret_cast<uint2*>(dst) = v;
+        }
+    }
+}
+
+// After the merge: statistics to absolute ALiBi positions, padding of the
+// unused partitions, counter back to zero for the next call.
+template <int NC>
+__device__ void fused_finish_stats(const Params& p, const TileDesc& d, int tid) {
+    const int G = p.group, Pm = p.max_parts;
+    const int P = (d.len + kPart - 1) / kPart;
+    for (int idx = tid; idx < G * Pm; idx += NC * 32) {
+        const int h = idx / Pm, q = idx - h * Pm;
+        const int head = d.kvh * G + h;
+        const int64_t o = ((int64_t)d.seq * p.num_heads + head) * Pm + q;
+        if (q < P) {
+            if (p.alibi) p.max_logits[o] += __ldg(p.alibi + head) * (float)(d.len - 1);
+        } else {
+            p.max_logits[o] = -INFINITY;
+            p.exp_sums[o] = 0.f;
+        }
+    }
+    if (tid == 0) p.counters[(int64_t)d.seq * p.num_kv_heads + d.kvh] = 0;
+}
+
+// End of a tile for the consumer warps: epilogue (merge of the warps' partial
+// states, partition statistics or output row), then in fused v2 mode the
+// arrival count of the (sequence, kv head) and, for its last partition, the
+// Phase 2 merge.  Returns false if a bounded wait gave up.
+template <class C, typename T, int HEAD, int NC>
+__device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, int warp, int lane,
+                            uint32_t& mphase) {
+    const int tid = warp * 32 + lane;
+    tile_epilogue<C, T, HEAD, NC>(p, d, sm, tid);
+    if (!consumer_sync(sm, mphase, lane)) return false;  // epilogue done, merge buffers free
+    if (!p.fused || p.v1) return true;
+    if (tid == 0) {
+        __threadfence();  // this CTA's partition results before its arrival
+        const int P = (d.len + kPart - 1) / kPart;
+        const int units = P > 0 ? P : 1;
+        const int old = atomicAdd(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
+        sm.abort[2] = (old == units - 1) ? 1 : 0;
+    }
+    if (!consumer_sync(sm, mphase, lane)) return false;
+    if (sm.abort[2]) {
+        __threadfence();  // the other CTAs' partition results, seen through their arrivals
+        fused_merge<T, HEAD, NC>(p, d, tid);
+        if (!consumer_sync(sm, mphase, lane)) return false;  // statistics read before rewritten
+        fused_finish_stats<NC>(p, d, tid);
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ consumers
@@ -647,8 +763,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             *sm.abort = 1;
             return;
         }
-        tile_epilogue<C, T, HEAD, NC>(p, d, sm, warp * 32 + lane);
-        if (!consumer_sync(sm, mphase, lane)) {  // merge buffers free again
+        if (!tile_finish<C, T, HEAD, NC>(p, d, sm, warp, lane, mphase)) {  // merge buffers free again
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -813,8 +928,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
             *sm.abort = 1;
             return;
         }
-        tile_epilogue<C, float, HEAD, NC>(p, d, sm, warp * 32 + lane);
-        if (!consumer_sync(sm, mphase, lane)) {
+        if (!tile_finish<C, float, HEAD, NC>(p, d, sm, warp, lane, mphase)) {
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -862,6 +976,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
         mbar_init(sm.merge_bar, NC);
         sm.abort[0] = 0;
         sm.abort[1] = 0;
+        sm.abort[2] = 0;
         fence_mbar_init();
     }
     if constexpr (C::kTensorMap) {
@@ -883,19 +998,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     }
 }
 
-// Phase 2: one CTA of 32*WARPS threads per (sequence, head).  Each lane owns
-// four head dims (a float4 column) of one partition row and keeps U partition
-// rows in flight, so a long sequence (hundreds of partitions) is read with
-// WARPS*U*(32/(HEAD/4)) independent 512-byte row loads per round.
-template <typename T, int HEAD, int WARPS>
+// Phase 2: one CTA of 32*WARPS threads per (sequence, head), one pass.  Each
+// lane owns four head dims (a float4 column) of one partition row and keeps U
+// partition rows in flight; it carries its own running max, so no separate
+// pass over max_logits is needed.  The rows are then combined with the usual
+// max rescale in shared memory.
+template <typename T, int HEAD, int WARPS, int U>
 __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     constexpr int D4 = HEAD / 4;          // float4 columns of a partition row
     constexpr int RPW = 32 / D4;          // partition rows per warp (1 or 2)
-    constexpr int RSTEP = WARPS * RPW;    // partition rows per CTA round
-    constexpr int U = 4;                  // rounds in flight
+    constexpr int RSTEP = WARPS * RPW;    // partition rows per CTA round (U rounds in flight)
     constexpr int NT = WARPS * 32;
-    __shared__ float red[WARPS];
     __shared__ float4 part[RSTEP][D4];
+    __shared__ float rowm[RSTEP], roww[RSTEP];
 
     const int bid = blockIdx.x;
     const int s = bid / p.num_heads, h = bid - s * p.num_heads;
@@ -912,19 +1027,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (P > 0) {
-        float M = -INFINITY;
-        for (int q = tid; q < P; q += NT) M = fmaxf(M, ml[q]);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        if (lane == 0) red[warp] = M;
-        __syncthreads();
-        M = red[0];
-#pragma unroll
-        for (int w = 1; w < WARPS; ++w) M = fmaxf(M, red[w]);
-        __syncthreads();
-
         const int row = warp * RPW + lane / D4, d4 = lane % D4;
-        float W = 0.f;  // sum of weights (kept by the d4 == 0 lane of each row)
+        float M = -INFINITY, W = 0.f;
         for (int q0 = row; q0 < P; q0 += RSTEP * U) {
             float mq[U], eq[U];
             float4 t[U];
@@ -943,7 +1047,17 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const float c = (mq[u] == -INFINITY) ? 0.f : expf(mq[u] - M) * eq[u];
+                if (mq[u] == -INFINITY) continue;
+                if (mq[u] > M) {
+                    const float sc = (M == -INFINITY) ? 0.f : expf(M - mq[u]);
+                    a.x *= sc;
+                    a.y *= sc;
+                    a.z *= sc;
+                    a.w *= sc;
+                    W *= sc;
+                    M = mq[u];
+                }
+                const float c = expf(mq[u] - M) * eq[u];
                 a.x += c * t[u].x;
                 a.y += c * t[u].y;
                 a.z += c * t[u].z;
@@ -951,29 +1065,34 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
                 W += c;
             }
         }
-        if (d4 != 0) W = 0.f;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-        if (lane == 0) red[warp] = W;
         part[row][d4] = a;
+        if (d4 == 0) {
+            rowm[row] = M;
+            roww[row] = W;
+        }
         __syncthreads();
-        W = 0.f;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) W += red[w];
         if (tid < D4) {
-            float4 sum = part[0][tid];
+            float Mg = -INFINITY;
 #pragma unroll
-            for (int i = 1; i < RSTEP; ++i) {
+            for (int i = 0; i < RSTEP; ++i) Mg = fmaxf(Mg, rowm[i]);
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            float Wg = 0.f;
+#pragma unroll
+            for (int i = 0; i < RSTEP; ++i) {
+                if (rowm[i] == -INFINITY) continue;
+                const float c = expf(rowm[i] - Mg);
                 const float4 v = part[i][tid];
-                sum.x += v.x;
-                sum.y += v.y;
-                sum.z += v.z;
-                sum.w += v.w;
+                sum.x += c * v.x;
+                sum.y += c * v.y;
+                sum.z += c * v.z;
+                sum.w += c * v.w;
+                Wg += c * roww[i];
             }
-            const float inv = 1.f / W;
+            const float inv = 1.f / Wg;
             a = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
         }
-        // statistics: sequence frame -> absolute ALiBi positions
+        // statistics: sequence frame -> absolute ALiBi positions (every read of
+        // max_logits above happened before the barrier)
         if (p.alibi) {
             const float shift = __ldg(p.alibi + h) * (float)(len - 1);
             for (int q = tid; q < P; q += NT) ml[q] += shift;

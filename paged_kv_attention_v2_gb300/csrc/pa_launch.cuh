@@ -27,8 +27,15 @@ struct LaunchArgs {
 
 constexpr int kMaxDevices = 64;
 
+// Launch the partition (or v1) kernel.  *fused reports whether the Phase 2
+// merge runs inside it: only with partition counters, a v2 batch that fits in
+// one round of the persistent grid (each CTA finishes at most one tile, so at
+// most one merge) and at most PA_FUSED_MAX_PARTITIONS partitions per sequence
+// (a short merge).  With several rounds the CTA that merges falls behind and
+// becomes the last arriver of the next group too, so merges pile up on a few
+// CTAs; the separate reduce kernel spreads them over the whole GPU instead.
 template <typename T, int HEAD, int NT, int LAYOUT>
-cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
+cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32 : PA_STAGES_16BIT;
     constexpr int NC = PA_CONSUMER_WARPS;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
@@ -52,6 +59,10 @@ cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
     if (la.grid_override > 0) grid = la.grid_override;
     if (grid > la.tiles_upper) grid = la.tiles_upper;
     if (grid < 1) grid = 1;
+    Params p = p_in;
+    p.fused = (!p.v1 && p.counters && p.max_parts <= PA_FUSED_MAX_PARTITIONS &&
+               la.tiles_upper <= grid) ? 1 : 0;
+    *fused = p.fused != 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -73,11 +84,14 @@ cudaError_t launch_main(const Params& p, const LaunchArgs& la) {
     return e;
 }
 
-template <typename T, int HEAD>
-cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
+// Reduce shape by partition count: few partitions need one round of rows,
+// long sequences (hundreds of partitions, few (sequence, head) CTAs) want as
+// many independent row loads in flight per CTA as possible.
+template <typename T, int HEAD, int WARPS, int U>
+cudaError_t launch_reduce_shape(const Params& p, const LaunchArgs& la) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((int64_t)p.num_seqs * p.num_heads));
-    cfg.blockDim = dim3(PA_REDUCE_WARPS * 32);
+    cfg.blockDim = dim3(WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = la.stream;
     cudaLaunchAttribute attr[1];
@@ -85,13 +99,19 @@ cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD, PA_REDUCE_WARPS>, p);
+    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD, WARPS, U>, p);
+}
+
+template <typename T, int HEAD>
+cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
+    if (p.max_parts > 32) return launch_reduce_shape<T, HEAD, 16, 8>(p, la);
+    return launch_reduce_shape<T, HEAD, 8, 4>(p, la);
 }
 
 template <typename T, int HEAD, int NT>
-cudaError_t launch_layout(const Params& p, const LaunchArgs& la) {
-    return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD>(p, la)
-                             : launch_main<T, HEAD, NT, kSplit>(p, la);
+cudaError_t launch_layout(const Params& p, const LaunchArgs& la, bool* fused) {
+    return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD>(p, la, fused)
+                             : launch_main<T, HEAD, NT, kSplit>(p, la, fused);
 }
 
 // Whole operation for one storage type.
@@ -99,14 +119,18 @@ template <typename T>
 cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
     constexpr bool F32 = std::is_same<T, float>::value;
     cudaError_t e;
+    bool fused = false;
     if constexpr (F32) {  // one fp32 consumer handles up to 16 heads
-        e = la.head_size == 128 ? launch_layout<T, 128, 2>(p, la) : launch_layout<T, 64, 2>(p, la);
+        e = la.head_size == 128 ? launch_layout<T, 128, 2>(p, la, &fused)
+                                : launch_layout<T, 64, 2>(p, la, &fused);
     } else if (la.head_size == 128) {
-        e = la.group_tiles == 2 ? launch_layout<T, 128, 2>(p, la) : launch_layout<T, 128, 1>(p, la);
+        e = la.group_tiles == 2 ? launch_layout<T, 128, 2>(p, la, &fused)
+                                : launch_layout<T, 128, 1>(p, la, &fused);
     } else {
-        e = la.group_tiles == 2 ? launch_layout<T, 64, 2>(p, la) : launch_layout<T, 64, 1>(p, la);
+        e = la.group_tiles == 2 ? launch_layout<T, 64, 2>(p, la, &fused)
+                                : launch_layout<T, 64, 1>(p, la, &fused);
     }
-    if (e != cudaSuccess || p.v1) return e;
+    if (e != cudaSuccess || p.v1 || fused) return e;
     return la.head_size == 128 ? launch_reduce<T, 128>(p, la) : launch_reduce<T, 64>(p, la);
 }
 

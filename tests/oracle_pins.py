@@ -390,11 +390,57 @@ def pin_partitions_at_100k(run):
     assert int(np.sum(np.isfinite(r["max_logits"][0, 0]))) == g["num_partitions"]
 
 
+def pin_sliding_window(run):
+    """Sliding window (query at position L-1 sees keys t >= L-1-W): matches the
+    brute force; W >= L-1 is bit-identical to no window; W = 0 returns the last
+    V row with exp_sum 1 in the last partition and every other partition unused;
+    q = 0 gives the mean of V over the window and exp_sum = in-window tokens."""
+    from oracle.brute import brute_decode
+    spec = _spec(name="win", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=8,
+                 dtype="f16", seq_lens=(1, 513, 1100), alibi=True)
+    base = W.make_workload(spec, "split")
+    for wl in (0, 5, 511, 600, 2000):
+        w = _clone(base, window_left=wl)
+        r = run(w)
+        b = brute_decode(w)
+        _close(r["out"], b["out"], what=f"window {wl} out")
+        _close(r["max_logits"], b["max_logits"], what=f"window {wl} max_logits")
+        _close(r["exp_sums"], b["exp_sums"], what=f"window {wl} exp_sums")
+    r_none = run(base)
+    r_big = run(_clone(base, window_left=1099))
+    for key in ("out", "max_logits", "exp_sums"):
+        assert np.array_equal(r_none[key], r_big[key], equal_nan=True), key
+    r0 = run(_clone(base, window_left=0))
+    _, v_log = _logical_kv(base)
+    group = base.num_heads // base.num_kv_heads
+    for s in range(base.num_seqs):
+        L = int(base.seq_lens[s])
+        blk = int(base.block_tables[s, (L - 1) // base.block_size])
+        P = -(-L // 512)
+        for h in range(base.num_heads):
+            _close(r0["out"][s, h], v_log[blk, h // group, (L - 1) % base.block_size],
+                   what="window 0 out")
+            _close(r0["exp_sums"][s, h, P - 1], 1.0, what="window 0 exp_sum")
+            assert np.all(r0["exp_sums"][s, h, :P - 1] == 0.0)
+            assert np.all(np.isneginf(r0["max_logits"][s, h, :P - 1]))
+    wq = _clone(base, query=np.zeros_like(base.query), alibi_slopes=None, window_left=600)
+    rq = run(wq)
+    for s in range(base.num_seqs):
+        L = int(base.seq_lens[s])
+        lo = max(0, L - 1 - 600)
+        nb = -(-L // base.block_size)
+        vs = v_log[base.block_tables[s, :nb], 0].reshape(nb * base.block_size, -1)[lo:L]
+        _close(rq["out"][s, 0], vs.mean(axis=0), rtol=1e-12, atol=1e-14, what="window q=0 mean")
+        for p in range(-(-L // 512)):
+            n = max(0, min(512 * p + 512, L) - max(512 * p, lo))
+            _close(rq["exp_sums"][s, 0, p], float(n), what="window q=0 exp_sum")
+
+
 ALL_PINS = [
     pin_brute, pin_sdpa, pin_partitioned_equals_dense, pin_seq_len_one,
     pin_identical_v_rows, pin_pool_permutation, pin_split_equals_nhd, pin_zero_query,
     pin_exp_sum_bounds, pin_softcap, pin_two_token_softmax, pin_alibi_closed_form,
-    pin_gqa_mapping, pin_poison_never_read, pin_partitions_at_100k,
+    pin_gqa_mapping, pin_poison_never_read, pin_partitions_at_100k, pin_sliding_window,
 ]
 
 

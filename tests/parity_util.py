@@ -42,9 +42,18 @@ def to_device(w, device="cuda:0"):
 
 
 def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_lens=None,
-            block_tables=None, poison_workspace=True):
-    """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error."""
+            block_tables=None, poison_workspace=True, counters=None, calls=1):
+    """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error.
+
+    mode "v2f" is v2 with partition counters (the merge inside the partition
+    kernel when the partition count allows it); `counters` may pass an existing
+    counter tensor, which must be all zero again after every call."""
     dev = dev or to_device(w, device)
+    fused = mode == "v2f"
+    if fused:
+        mode = "v2"
+        if counters is None:
+            counters = torch.zeros((w.num_seqs, w.num_kv_heads), dtype=torch.int32, device=device)
     msl = w.max_seq_len if max_seq_len is None else max_seq_len
     S, H, d = w.num_seqs, w.num_heads, w.head_size
     out = torch.full((S, H, d), float("nan"), dtype=torch_dtype(w.dtype), device=device)
@@ -53,13 +62,16 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
         for t in ws.values():
             t.fill_(float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device=device)
-    pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"],
-                 dev["block_tables"] if block_tables is None else block_tables,
-                 dev["seq_lens"] if seq_lens is None else seq_lens,
-                 num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
-                 alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout, mode=mode,
-                 dev_error=err, **ws)
+    for _ in range(calls):
+        pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"],
+                     dev["block_tables"] if block_tables is None else block_tables,
+                     dev["seq_lens"] if seq_lens is None else seq_lens,
+                     num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
+                     alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
+                     mode=mode, dev_error=err, partition_counters=counters, **ws)
     torch.cuda.synchronize(device)
+    if counters is not None:
+        assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"
     return {
         "out": out.double().cpu().numpy(),
         "max_logits": ws["max_logits"].double().cpu().numpy(),

@@ -53,6 +53,8 @@ MUTATIONS = [
     ("reduce_weight_without_exp_sum", "double r = exp(m - M) * e;", "double r = exp(m - M);", 0),
     ("half_exponent_bias", "v = ldexp((double)(1024 + f), e - 25);",
      "v = ldexp((double)(1024 + f), e - 24);", 0),
+    ("window_off_by_one", "t_lo = len - 1 - a->window_left;", "t_lo = len - a->window_left;", 0),
+    ("window_ignored", "    if (a->window_left >= 0 && len - 1 - a->window_left > 0) t_lo = len - 1 - a->window_left;\n", "", 0),
     ("unused_partition_sum_one", "if (a->exp_sums) a->exp_sums[stat_off + p] = 0.0;",
      "if (a->exp_sums) a->exp_sums[stat_off + p] = 1.0;", 0),
 ]

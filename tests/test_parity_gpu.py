@@ -39,11 +39,11 @@ def test_workload_parity(name, layout):
     w = _workload(name, layout)
     ref = oracle.oracle_decode(w)
     dev = to_device(w)
-    for mode in ("auto", "v1", "v2"):
-        g = run_gpu(w, mode=mode, dev=dev)
+    for mode in ("auto", "v1", "v2", "v2f"):
+        g = run_gpu(w, mode=mode, dev=dev, calls=2 if mode == "v2f" else 1)
         assert g["dev_error"] == 0, (mode, g["dev_error"])
         check_out(w, g["out"], ref["out"], what=f"out[{mode}]")
-        if mode == "v2" or (mode == "auto" and w.max_seq_len > 512):
+        if mode in ("v2", "v2f") or (mode == "auto" and w.max_seq_len > 512):
             check_stats(w, g, ref)
     del dev
     torch.cuda.empty_cache()
@@ -56,7 +56,7 @@ def test_large_batch_sampled():
         w = W.make_workload("large_batch", layout)
         sample = [0, 41, 86, 127]
         ref = oracle.oracle_decode(w, seq_subset=sample)
-        g = run_gpu(w, mode="auto")
+        g = run_gpu(w, mode="v2f")
         assert g["dev_error"] == 0
         check_out(w, g["out"], ref["out"], seqs=sample)
         check_stats(w, g, ref, seqs=sample)
@@ -95,7 +95,7 @@ EDGE = [
 
 
 @pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
-@pytest.mark.parametrize("mode", ["v1", "v2"])
+@pytest.mark.parametrize("mode", ["v1", "v2", "v2f"])
 def test_edge_cases(case, mode):
     name, dtype, layout, H, Hkv, d, lens, alibi, cap, mult = case
     spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
@@ -103,10 +103,10 @@ def test_edge_cases(case, mode):
                         value_mult=mult)
     w = W.make_workload(spec, layout)
     ref = oracle.oracle_decode(w)
-    g = run_gpu(w, mode=mode)
+    g = run_gpu(w, mode=mode, calls=2)
     assert g["dev_error"] == 0
     check_out(w, g["out"], ref["out"])
-    if mode == "v2":
+    if mode in ("v2", "v2f"):
         check_stats(w, g, ref)
 
 
@@ -141,3 +141,22 @@ def test_seq_len_beyond_max_is_clamped_and_flagged():
         w2.max_seq_len = 1024
         ref = oracle.oracle_decode(w2)
         check_out(w2, g["out"], ref["out"])
+
+
+@pytest.mark.parametrize("lens", [(4096, 0, 1, 3000, 0, 513), (32768, 0, 1, 20000, 0, 513)],
+                         ids=["merge-in-kernel", "beyond-fused-limit"])
+def test_partition_counters_with_empty_sequences(lens):
+    """Counters given: the first batch (at most 8 partitions per sequence, one
+    round of tiles) merges inside the partition kernel, the second exceeds the
+    limit and uses the reduce kernel.  Empty sequences in the batch, counters
+    reused over several calls and back at zero after each."""
+    spec = W.small_spec(name="counters", num_seqs=6, num_heads=8, num_kv_heads=2, head_size=128,
+                        dtype="bf16", seq_lens=lens, alibi=True)
+    w = W.make_workload(spec, "split")
+    ref = oracle.oracle_decode(w)
+    counters = torch.zeros((w.num_seqs, w.num_kv_heads), dtype=torch.int32, device="cuda:0")
+    for _ in range(2):
+        g = run_gpu(w, mode="v2f", counters=counters, calls=3)
+        assert g["dev_error"] == 0
+        check_out(w, g["out"], ref["out"])
+        check_stats(w, g, ref)

@@ -111,6 +111,7 @@ class Workload:
     seq_lens: np.ndarray
     alibi_slopes: Optional[np.ndarray]
     meta: dict = field(default_factory=dict)
+    window_left: int = -1  # sliding window: keys t >= seq_len - 1 - window_left (-1 = none)
 
     @property
     def elem_bytes(self) -> int:
