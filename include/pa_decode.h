@@ -16,6 +16,7 @@
  *     z_t = softcap * tanh(z_t / softcap)          if softcap > 0
  *     z_t = z_t + alibi_slopes[h] * t              if alibi_slopes != NULL
  *     out[s][h] = sum_t exp(z_t - max z) V_g(t) / sum_t exp(z_t - max z)
+ * (t restricted to the last sliding_window keys when sliding_window > 0).
  * K_g(t) is read from physical block block_tables[s][t / block_size] at slot
  * t % block_size.  Sequences are cut into partitions of PA_PARTITION_SIZE
  * tokens; for partition p (tokens [512p, min(512p+512, seq_len))):
@@ -146,6 +147,14 @@ typedef struct pa_decode_args {
      * after a PA_DEVERR_TIMEOUT the caller must zero them.  Calls that share
      * counters must not overlap on the GPU.  NULL = separate reduce kernel. */
     int32_t* partition_counters;
+    /* Sliding window, in keys visible to the query including its own token:
+     * 0 (or < 0) = off, so a zero-initialised struct has no window; otherwise
+     * the query, at position seq_lens[s] - 1, attends the keys
+     * t >= seq_lens[s] - sliding_window.  This is window_left + 1 for the
+     * window_left of AttnDispatchConfig in attn_dispatch.py (-1 there = off).
+     * Partitions with no key in the window are skipped (unused: max_logits
+     * -inf, exp_sums 0). */
+    int32_t sliding_window;
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the

@@ -80,8 +80,12 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               scale: float, max_seq_len: int, block_size: int = PA_BLOCK_SIZE,
               alibi_slopes=None, softcap: float = 0.0, layout: str = "split", mode: str = "auto",
               exp_sums=None, max_logits=None, tmp_out=None, dev_error=None,
-              event_begin=None, event_end=None, partition_counters=None) -> _abi.PaDecodeArgs:
-    """Build the C argument struct (no checks beyond shapes; the library validates)."""
+              event_begin=None, event_end=None, partition_counters=None,
+              window_left: int = -1) -> _abi.PaDecodeArgs:
+    """Build the C argument struct (no checks beyond shapes; the library validates).
+
+    window_left follows AttnDispatchConfig (-1 = no window; the query sees the
+    keys t >= seq_len - 1 - window_left) and becomes sliding_window = window_left + 1."""
     num_seqs, num_heads, head_size = query.shape
     num_blocks = key_cache.shape[0]
     return _abi.PaDecodeArgs(
@@ -96,6 +100,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         event_main_begin=None if event_begin is None else event_begin.cuda_event,
         event_main_end=None if event_end is None else event_end.cuda_event,
         partition_counters=_ptr(partition_counters),
+        sliding_window=int(window_left) + 1 if window_left >= 0 else 0,
     )
 
 

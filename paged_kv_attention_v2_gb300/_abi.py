@@ -67,6 +67,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("event_main_begin", ctypes.c_void_p),
         ("event_main_end", ctypes.c_void_p),
         ("partition_counters", ctypes.c_void_p),
+        ("sliding_window", ctypes.c_int32),
     ]
 
 

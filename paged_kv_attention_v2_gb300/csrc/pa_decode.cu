@@ -197,6 +197,7 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
     p.v1 = v1 ? 1 : 0;
     p.counters = a->partition_counters;
+    p.window_left = a->sliding_window > 0 ? a->sliding_window - 1 : -1;
     p.fused = 0;  // decided at launch, once the persistent grid size is known
 
     alignas(64) CUtensorMap tmk, tmv;

@@ -68,6 +68,7 @@ struct Params {
     float scale, softcap, inv_softcap;
     int v1;
     int32_t* counters;  // [num_seqs][num_kv_heads] finished partitions (fused v2 only)
+    int window_left;    // < 0: no window; else keys t >= len - 1 - window_left
     int fused;          // v2 with the log-sum-exp merge done by the last CTA of each (seq, kv head)
 };
 
@@ -82,6 +83,18 @@ __device__ __forceinline__ void report(const Params& p, int bits) {
 
 __device__ __forceinline__ int clamp_len(const Params& p, int raw) {
     return raw < 0 ? 0 : (raw > p.max_seq_len ? p.max_seq_len : raw);
+}
+
+// First key inside the sliding window of a sequence of len tokens (0 without one).
+__device__ __forceinline__ int window_lo(const Params& p, int len) {
+    if (p.window_left < 0) return 0;
+    const int lo = len - 1 - p.window_left;
+    return lo > 0 ? lo : 0;
+}
+
+// Pages covering tokens [tb, te): from page tb/16 to page ceil(te/16) - 1.
+__device__ __forceinline__ int tile_pages(int tb, int te) {
+    return te > tb ? (te + kBS - 1) / kBS - tb / kBS : 0;
 }
 
 // ------------------------------------------------------------------ config
@@ -169,18 +182,21 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
 
     // Walk of seq_lens in chunks of 32 sequences: lane i holds sequence cb+i.
     int cb = 0, cu = 0;  // first sequence of the chunk, tile units before the chunk
-    int c_len = 0, c_units = 0, c_incl = 0, c_total = 0;
+    int c_len = 0, c_units = 0, c_p0 = 0, c_incl = 0, c_total = 0;
     auto load_chunk = [&](int base) {
         const int s = base + lane;
         c_len = 0;
         c_units = 0;
+        c_p0 = 0;
         if (s < S) {
             const int raw = __ldg(p.seq_lens + s);
             c_len = clamp_len(p, raw);
             if (c_len != raw) report(p, PA_DEVERR_SEQ_LEN);
-            // v1: one tile per sequence; v2: one per partition (fused v2 keeps one
-            // empty tile for an empty sequence so that its output row is written)
-            c_units = p.v1 ? 1 : (c_len + kPart - 1) / kPart;
+            // v1: one tile per sequence; v2: one per partition that has keys in
+            // the window (fused v2 keeps one empty tile for an empty sequence so
+            // that its output row is written)
+            c_p0 = window_lo(p, c_len) / kPart;
+            c_units = p.v1 ? 1 : (c_len + kPart - 1) / kPart - c_p0;
             if (p.fused && c_units == 0) c_units = 1;
         }
         c_incl = c_units;
@@ -214,10 +230,11 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         t.seq = cb + j;
         const int excl = __shfl_sync(0xffffffffu, c_incl - c_units, j);
         t.len = __shfl_sync(0xffffffffu, c_len, j);
-        t.part = rel - excl;
-        t.tb = p.v1 ? 0 : t.part * kPart;
-        t.te = p.v1 ? t.len : min(t.len, t.tb + kPart);
-        t.npages = (t.te - t.tb + kBS - 1) / kBS;
+        const int lo = window_lo(p, t.len);
+        t.part = __shfl_sync(0xffffffffu, c_p0, j) + rel - excl;
+        t.tb = p.v1 ? lo : max(t.part * kPart, lo);
+        t.te = p.v1 ? t.len : min(t.len, t.part * kPart + kPart);
+        t.npages = tile_pages(t.tb, t.te);
         t.valid = true;
         return t;
     };
@@ -397,6 +414,7 @@ __device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
     constexpr int D4 = HEAD / 4;
     const int G = p.group;
     const int P = (d.len + kPart - 1) / kPart;
+    const int p0 = window_lo(p, d.len) / kPart;  // partitions before p0: outside the window
     for (int idx = tid; idx < G * D4; idx += NC * 32) {
         const int h = idx / D4, d4 = idx - h * D4;
         const int64_t sh = (int64_t)d.seq * p.num_heads + d.kvh * G + h;
@@ -405,7 +423,7 @@ __device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
         const float* tmp = p.tmp_out + sh * p.max_parts * HEAD + 4 * d4;
         float M = -INFINITY, W = 0.f;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = 0; q0 < P; q0 += 4) {
+        for (int q0 = p0; q0 < P; q0 += 4) {
             float mq[4], eq[4];
             float4 t[4];
 #pragma unroll
@@ -461,11 +479,12 @@ template <int NC>
 __device__ void fused_finish_stats(const Params& p, const TileDesc& d, int tid) {
     const int G = p.group, Pm = p.max_parts;
     const int P = (d.len + kPart - 1) / kPart;
+    const int p0 = window_lo(p, d.len) / kPart;
     for (int idx = tid; idx < G * Pm; idx += NC * 32) {
         const int h = idx / Pm, q = idx - h * Pm;
         const int head = d.kvh * G + h;
         const int64_t o = ((int64_t)d.seq * p.num_heads + head) * Pm + q;
-        if (q < P) {
+        if (q < P && q >= p0) {
             if (p.alibi) p.max_logits[o] += __ldg(p.alibi + head) * (float)(d.len - 1);
         } else {
             p.max_logits[o] = -INFINITY;
@@ -488,7 +507,7 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     if (!p.fused || p.v1) return true;
     if (tid == 0) {
         __threadfence();  // this CTA's partition results before its arrival
-        const int P = (d.len + kPart - 1) / kPart;
+        const int P = (d.len + kPart - 1) / kPart - window_lo(p, d.len) / kPart;
         const int units = P > 0 ? P : 1;
         const int old = atomicAdd(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
         sm.abort[2] = (old == units - 1) ? 1 : 0;
@@ -619,7 +638,8 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
         }
 
-        const int npages = (d.tok_end - d.tok_begin + kBS - 1) / kBS;
+        const int npages = tile_pages(d.tok_begin, d.tok_end);
+        const int page0 = d.tok_begin / kBS * kBS;  // first token of the tile's first page
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
@@ -630,8 +650,9 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             }
             const uint32_t kp = sm.ring + st * C::kStageBytes;
             const uint32_t vp = kp + C::kPageBytes;
-            const int tok0 = d.tok_begin + j * kBS;
-            const int valid = min(kBS, d.tok_end - tok0);
+            const int tok0 = page0 + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
+            const int skip = d.tok_begin - tok0;          // slots < skip: before the window
             if (valid < kBS) {
                 zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
@@ -675,8 +696,8 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tlo + ((e >> 1) << 3) - origin);
                     z[e] = v;
                 }
-                if (r >= valid) z[0] = z[1] = -INFINITY;
-                if (r + 8 >= valid) z[2] = z[3] = -INFINITY;
+                if (r >= valid || r < skip) z[0] = z[1] = -INFINITY;
+                if (r + 8 >= valid || r + 8 < skip) z[2] = z[3] = -INFINITY;
                 float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
@@ -812,7 +833,8 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int c = 0; c < DPL; ++c) acc[h][c] = 0.f;
 
-        const int npages = (d.tok_end - d.tok_begin + kBS - 1) / kBS;
+        const int npages = tile_pages(d.tok_begin, d.tok_end);
+        const int page0 = d.tok_begin / kBS * kBS;  // first token of the tile's first page
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
@@ -824,8 +846,9 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
             const float* kp = reinterpret_cast<const float*>(
                 __cvta_shared_to_generic(sm.ring + st * C::kStageBytes));
             float* vp = const_cast<float*>(kp) + kBS * HEAD;
-            const int tok0 = d.tok_begin + j * kBS;
-            const int valid = min(kBS, d.tok_end - tok0);
+            const int tok0 = page0 + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
+            const int skip = d.tok_begin - tok0;          // slots < skip: before the window
             if (valid < kBS) {
                 if constexpr (LAYOUT == kSplit) {
                     for (int dd = lane; dd < HEAD; dd += 32)
@@ -857,7 +880,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                 float v = dot * p.scale;
                 if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
                 if (has_alibi) v += sl[i] * (float)(tok0 + t - origin);
-                z[i] = (t < valid) ? v : -INFINITY;
+                z[i] = (t < valid && t >= skip) ? v : -INFINITY;
             }
 #pragma unroll
             for (int i = 0; i < HPL; ++i) {
@@ -884,7 +907,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                     for (int c = 0; c < DPL; ++c) acc[h][c] *= al;
                 }
             }
-            for (int tt = 0; tt < valid; ++tt) {
+            for (int tt = skip > 0 ? skip : 0; tt < valid; ++tt) {
                 float vv[DPL];
 #pragma unroll
                 for (int c = 0; c < DPL; ++c) {
@@ -1019,6 +1042,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
 
     const int len = clamp_len(p, p.seq_lens[s]);
     const int P = (len + kPart - 1) / kPart;
+    const int p0 = window_lo(p, len) / kPart;  // partitions before p0: outside the window
     const int64_t sb = ((int64_t)s * p.num_heads + h) * p.max_parts;
     float* ml = p.max_logits + sb;
     float* es = p.exp_sums + sb;
@@ -1029,7 +1053,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     if (P > 0) {
         const int row = warp * RPW + lane / D4, d4 = lane % D4;
         float M = -INFINITY, W = 0.f;
-        for (int q0 = row; q0 < P; q0 += RSTEP * U) {
+        for (int q0 = p0 + row; q0 < P; q0 += RSTEP * U) {
             float mq[U], eq[U];
             float4 t[U];
 #pragma unroll
@@ -1095,7 +1119,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
         // max_logits above happened before the barrier)
         if (p.alibi) {
             const float shift = __ldg(p.alibi + h) * (float)(len - 1);
-            for (int q = tid; q < P; q += NT) ml[q] += shift;
+            for (int q = p0 + tid; q < P; q += NT) ml[q] += shift;
         }
     }
     if (tid < D4) {
@@ -1111,6 +1135,10 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
         }
     }
     for (int q = P + tid; q < p.max_parts; q += NT) {
+        ml[q] = -INFINITY;
+        es[q] = 0.f;
+    }
+    for (int q = tid; q < p0 && q < P; q += NT) {
         ml[q] = -INFINITY;
         es[q] = 0.f;
     }

@@ -68,7 +68,8 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                      dev["seq_lens"] if seq_lens is None else seq_lens,
                      num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
                      alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
-                     mode=mode, dev_error=err, partition_counters=counters, **ws)
+                     mode=mode, dev_error=err, partition_counters=counters,
+                     window_left=getattr(w, "window_left", -1), **ws)
     torch.cuda.synchronize(device)
     if counters is not None:
         assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"
@@ -107,9 +108,13 @@ def check_stats(w, gpu, ref, seqs=None):
     seqs = range(w.num_seqs) if seqs is None else seqs
     for s in seqs:
         P = -(-int(min(max(int(w.seq_lens[s]), 0), w.max_seq_len)) // 512)
+        # partitions the oracle marks unused (before a sliding window): exactly -inf / 0
+        unused = np.isneginf(ref["max_logits"][s, :, :P])
+        assert np.all(np.isneginf(gpu["max_logits"][s, :, :P][unused])), f"{w.name} seq {s}"
+        assert np.all(gpu["exp_sums"][s, :, :P][unused] == 0.0), f"{w.name} seq {s}"
         for key in ("max_logits", "exp_sums"):
-            g = gpu[key][s, :, :P]
-            r = ref[key][s, :, :P]
+            g = np.where(unused, 0.0, gpu[key][s, :, :P])
+            r = np.where(unused, 0.0, ref[key][s, :, :P])
             bad = ~(np.abs(g - r) <= STAT_TOL * np.maximum(np.abs(r), 1.0))
             if bad.any():
                 idx = tuple(np.argwhere(bad)[0])
@@ -121,7 +126,7 @@ def check_stats(w, gpu, ref, seqs=None):
         assert np.all(pad_es == 0.0), f"{w.name} seq {s}: exp_sums padding not 0"
         g = gpu["tmp_out"][s, :, :P]
         r = ref["tmp_out"][s, :, :P]
-        bad = _violations(g, r, atol, rtol)
+        bad = _violations(g, r, atol, rtol) & ~unused[:, :, None]
         if bad.any():
             idx = tuple(np.argwhere(bad)[0])
             raise AssertionError(f"{w.name}/{w.layout} tmp_out seq {s} at {idx}: gpu {g[idx]!r} "

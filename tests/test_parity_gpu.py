@@ -160,3 +160,48 @@ def test_partition_counters_with_empty_sequences(lens):
         assert g["dev_error"] == 0
         check_out(w, g["out"], ref["out"])
         check_stats(w, g, ref)
+
+
+WINDOWS = [
+    # name, dtype, layout, H, Hkv, d, lens, alibi, softcap, window_left
+    ("w0", "f16", "split", 8, 2, 128, (1, 17, 700), False, 0.0, 0),
+    ("w15_page_edge", "bf16", "nhd", 8, 2, 128, (16, 33, 1025), True, 0.0, 15),
+    ("w100", "f16", "nhd", 14, 2, 128, (99, 101, 2000), False, 0.0, 100),
+    ("w511_partition_edge", "bf16", "split", 8, 1, 128, (512, 1024, 1537), False, 30.0, 511),
+    ("w600_alibi", "f16", "split", 32, 8, 128, (1, 600, 601, 5000), True, 0.0, 600),
+    ("w_beyond_len", "f16", "split", 4, 2, 64, (40, 900), False, 0.0, 5000),
+    ("w_f32", "f32", "nhd", 6, 2, 128, (300, 1100), True, 0.0, 333),
+]
+
+
+@pytest.mark.parametrize("case", WINDOWS, ids=[c[0] for c in WINDOWS])
+@pytest.mark.parametrize("mode", ["v1", "v2", "v2f"])
+def test_sliding_window(case, mode):
+    name, dtype, layout, H, Hkv, d, lens, alibi, cap, wl = case
+    spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
+                        head_size=d, dtype=dtype, seq_lens=lens, alibi=alibi, softcap=cap)
+    w = W.make_workload(spec, layout)
+    w.window_left = wl
+    ref = oracle.oracle_decode(w)
+    g = run_gpu(w, mode=mode, calls=2)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], ref["out"])
+    if mode in ("v2", "v2f"):
+        check_stats(w, g, ref)
+
+
+def test_sliding_window_ragged_full_size():
+    """The ragged workload (256 sequences up to 32768 tokens, ALiBi) with a
+    4096-key window: partitions wholly before the window are skipped."""
+    w = _workload("ragged", "split")
+    w.window_left = 4095
+    try:
+        ref = oracle.oracle_decode(w)
+        for mode in ("v1", "v2"):
+            g = run_gpu(w, mode=mode)
+            assert g["dev_error"] == 0
+            check_out(w, g["out"], ref["out"])
+            if mode == "v2":
+                check_stats(w, g, ref)
+    finally:
+        w.window_left = -1
