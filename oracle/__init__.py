@@ -26,7 +26,7 @@ _LIB_PATH = _BUILD / "libpa_oracle.so"
 _lock = threading.Lock()
 _libs = {}
 
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3, "e5m2": 4}
 LAYOUT_CODE = {"split": 0, "nhd": 1}
 PARTITION_SIZE = 512
 
@@ -53,6 +53,9 @@ class OracleArgs(ctypes.Structure):
         ("scale", ctypes.c_double),
         ("softcap", ctypes.c_double),
         ("window_left", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_double),
+        ("v_scale", ctypes.c_double),
         ("seq_subset", ctypes.c_void_p),
         ("n_subset", ctypes.c_int32),
         ("num_threads", ctypes.c_int32),
@@ -153,6 +156,8 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
         max_num_partitions=P, dtype=DTYPE_CODE[w.dtype], layout=LAYOUT_CODE[w.layout],
         scale=float(w.scale), softcap=float(w.softcap),
         window_left=int(getattr(w, "window_left", -1)),
+        kv_dtype=DTYPE_CODE[w.kv_dtype] if getattr(w, "kv_dtype", None) else -1,
+        k_scale=float(getattr(w, "k_scale", 1.0)), v_scale=float(getattr(w, "v_scale", 1.0)),
         seq_subset=_ptr(sub), n_subset=0 if sub is None else len(sub),
         num_threads=threads or default_threads(),
         out=_ptr(res["out"]),

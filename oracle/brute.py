@@ -20,13 +20,18 @@ import numpy as np
 def _decode(a: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype in ("e4m3", "e5m2"):  # fp8 caches: torch's own conversion
+        import torch
+        tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+        return torch.from_numpy(np.ascontiguousarray(a)).view(tdt).double().numpy()
     return a.astype(np.float64)
 
 
 def _gather(w, s):
     """keys[t][kvh][d], values[t][kvh][d] for sequence s (Python lists)."""
-    kc = _decode(w.key_cache, w.dtype)
-    vc = _decode(w.value_cache, w.dtype)
+    cdt = getattr(w, "kv_dtype", None) or w.dtype
+    kc = _decode(w.key_cache, cdt)
+    vc = _decode(w.value_cache, cdt)
     bs, d, hkv = w.block_size, w.head_size, w.num_kv_heads
     L = int(w.seq_lens[s])
     nblk = (L + bs - 1) // bs
@@ -69,6 +74,12 @@ def brute_decode(w, partition_size: int = 512):
         if L == 0:
             continue
         keys, values = _gather(w, s)
+        # "Apply k_scale if needed": dequantisation scales of the gathered keys / values
+        ks, vs = getattr(w, "k_scale", 1.0), getattr(w, "v_scale", 1.0)
+        if ks != 1.0:
+            keys = [[[x * ks for x in row] for row in tok] for tok in keys]
+        if vs != 1.0:
+            values = [[[x * vs for x in row] for row in tok] for tok in values]
         n_parts = (L + partition_size - 1) // partition_size
         # sliding window: the query (position L-1) sees keys t >= L-1-window_left
         wl = getattr(w, "window_left", -1)

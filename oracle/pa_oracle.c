@@ -30,6 +30,11 @@
  *    softmax -- so the dense result out = sum exp(z - Z) v / sum exp(z - Z)
  *    is computed independently and both are returned.
  *  - Unused partitions (p >= ceil(seq_len/512)): m = -inf, e = 0, tmp = 0.
+ *  - same page, arguments kv_cache_dtype / k_scale / v_scale: the gathered
+ *    keys are multiplied by k_scale and the values by v_scale.  Reading: an
+ *    fp8 cache ("fp8_e4m3" / "fp8_e5m2") holds the keys / values divided by
+ *    their scale, so K = k_scale * decode(K8), V = v_scale * decode(V8); the
+ *    query and the output keep the query's type.
  *  - "ex_engine/factors/attn_dispatch.py", AttnDispatchConfig window_left /
  *    window_right (-1 = no window), passed to the decode call: the single
  *    query token sits at position seq_len - 1 and attends the keys
@@ -82,16 +87,48 @@ static double bf16_bits_to_double(uint16_t b) {
     return (double)f;
 }
 
+/* OCP FP8 E4M3 (the "FN" variant): 1 sign, 4 exponent bits (bias 7), 3
+ * fraction bits, no infinities, S.1111.111 is NaN, largest finite 448. */
+static double e4m3_bits_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) v = ldexp((double)f, -9);             /* subnormal: f/8 * 2^-6 */
+    else v = ldexp((double)(8 + f), e - 10);          /* (1.f) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* OCP FP8 E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits, IEEE-style
+ * infinities and NaNs. */
+static double e5m2_bits_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int f = b & 0x3;
+    double v;
+    if (e == 31) v = f ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)f, -16);       /* subnormal: f/4 * 2^-14 */
+    else v = ldexp((double)(4 + f), e - 17);          /* (1.f) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
 static double load_elem(const void* base, int64_t idx, int dtype) {
     switch (dtype) {
     case ORACLE_F32: return (double)((const float*)base)[idx];
     case ORACLE_F16: return half_bits_to_double(((const uint16_t*)base)[idx]);
     case ORACLE_BF16: return bf16_bits_to_double(((const uint16_t*)base)[idx]);
+    case ORACLE_FP8_E4M3: return e4m3_bits_to_double(((const uint8_t*)base)[idx]);
+    case ORACLE_FP8_E5M2: return e5m2_bits_to_double(((const uint8_t*)base)[idx]);
     default: return NAN;
     }
 }
 
-static int elem_bytes(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+static int elem_bytes(int dtype) {
+    return dtype == ORACLE_F32 ? 4 : (dtype == ORACLE_FP8_E4M3 || dtype == ORACLE_FP8_E5M2) ? 1 : 2;
+}
+
+static int cache_dtype(const oracle_args* a) { return a->kv_dtype < 0 ? a->dtype : a->kv_dtype; }
 
 /* ---- page addressing ----------------------------------------------------- */
 
@@ -100,7 +137,7 @@ static int elem_bytes(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
 static int64_t key_index(const oracle_args* a, int64_t blk, int kvh, int o, int d) {
     int64_t base = (blk * a->num_kv_heads + kvh) * (int64_t)a->head_size * a->block_size;
     if (a->layout == ORACLE_LAYOUT_SPLIT) {
-        int x = 16 / elem_bytes(a->dtype);
+        int x = 16 / elem_bytes(cache_dtype(a));
         /* [head_size/x][block_size][x] */
         return base + ((int64_t)(d / x) * a->block_size + o) * x + (d % x);
     }
@@ -163,7 +200,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
         double dot = 0.0;
         for (int d = 0; d < d_sz; ++d)
             dot += load_elem(a->query, qoff + d, a->dtype) *
-                   load_elem(a->key_cache, key_index(a, blk, kvh, o, d), a->dtype);
+                   (a->k_scale * load_elem(a->key_cache, key_index(a, blk, kvh, o, d), cache_dtype(a)));
         double z = a->scale * dot;
         if (a->softcap > 0.0) z = a->softcap * tanh(z / a->softcap);
         if (a->alibi_slopes) z += (double)a->alibi_slopes[h] * (double)t;
@@ -180,7 +217,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
         double w = exp(sc->z[t] - Z);
         denom += w;
         for (int d = 0; d < d_sz; ++d)
-            out[d] += w * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), a->dtype);
+            out[d] += w * (a->v_scale * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), cache_dtype(a)));
     }
     for (int d = 0; d < d_sz; ++d) out[d] /= denom;
 
@@ -211,7 +248,7 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
             double w = exp(sc->z[t] - m);
             e += w;
             for (int d = 0; d < d_sz; ++d)
-                sc->vrow[d] += w * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), a->dtype);
+                sc->vrow[d] += w * (a->v_scale * load_elem(a->value_cache, value_index(a, blk, kvh, o, d), cache_dtype(a)));
         }
         for (int d = 0; d < d_sz; ++d) sc->vrow[d] /= e;      /* tmp_p, normalised */
         if (a->max_logits) a->max_logits[stat_off + p] = m;
@@ -274,7 +311,10 @@ int oracle_decode(const oracle_args* a) {
         return ORACLE_ERR_ARG;
     if (a->dtype != ORACLE_F32 && a->dtype != ORACLE_F16 && a->dtype != ORACLE_BF16)
         return ORACLE_ERR_ARG;
-    if (a->layout == ORACLE_LAYOUT_SPLIT && a->head_size % (16 / elem_bytes(a->dtype)))
+    if (a->kv_dtype >= 0 && a->kv_dtype != ORACLE_FP8_E4M3 && a->kv_dtype != ORACLE_FP8_E5M2 &&
+        a->kv_dtype != a->dtype)
+        return ORACLE_ERR_ARG;
+    if (a->layout == ORACLE_LAYOUT_SPLIT && a->head_size % (16 / elem_bytes(cache_dtype(a))))
         return ORACLE_ERR_ARG;
     int n_seq = a->seq_subset ? a->n_subset : a->num_seqs;
     int max_len = 0;

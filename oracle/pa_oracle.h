@@ -15,7 +15,7 @@ extern "C" {
 #define ORACLE_ABI_VERSION 1
 
 enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_NOMEM = 2 };
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8_E4M3 = 3, ORACLE_FP8_E5M2 = 4 };
 enum { ORACLE_LAYOUT_SPLIT = 0, ORACLE_LAYOUT_NHD = 1 };
 
 typedef struct oracle_args {
@@ -32,6 +32,8 @@ typedef struct oracle_args {
     int32_t dtype, layout;
     double scale, softcap;
     int32_t window_left;          /* < 0: no window; else keys t >= seq_len - 1 - window_left */
+    int32_t kv_dtype;             /* storage type of the caches; < 0: same as dtype */
+    double k_scale, v_scale;      /* dequantisation scales of the caches (1.0 = none) */
     /* optional subset of sequences to evaluate (NULL = all) */
     const int32_t* seq_subset;
     int32_t n_subset;

@@ -436,11 +436,58 @@ def pin_sliding_window(run):
             _close(rq["exp_sums"][s, 0, p], float(n), what="window q=0 exp_sum")
 
 
+def pin_fp8_cache(run):
+    """fp8 caches: every bit pattern decodes as torch's fp8 conversion does
+    (seq_len 1, q = 0: the output is v_scale * the V row); k_scale scales the
+    logits and v_scale the output linearly; an fp8 cache gives the result of an
+    fp32 cache holding its decoded, scaled values; the brute force agrees."""
+    import torch
+    from oracle.brute import brute_decode
+    for kind, tdt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        spec = _spec(name="fp8bits", num_seqs=16, num_heads=1, num_kv_heads=1, head_size=16,
+                     dtype="f16", seq_lens=(1,) * 16, kv_dtype=kind)
+        spec.poison = False
+        w = W.make_workload(spec, "nhd")
+        bits = np.arange(256, dtype=np.uint8).reshape(16, 16)
+        vc = np.zeros_like(w.value_cache)
+        for s in range(16):
+            vc[w.block_tables[s, 0], 0, 0, :] = bits[s]
+        w = _clone(w, value_cache=vc, query=np.zeros_like(w.query), v_scale=1.0)
+        r = run(w)
+        expect = torch.from_numpy(bits.copy()).view(tdt).double().numpy()
+        got = r["out"][:, 0, :]
+        assert np.array_equal(np.isnan(got), np.isnan(expect)), kind
+        fin = ~np.isnan(expect)
+        assert np.array_equal(got[fin], expect[fin]), kind
+    spec = _spec(name="fp8", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=16, dtype="bf16",
+                 seq_lens=(1, 300, 700), kv_dtype="e4m3", k_scale=2.0 ** -5, v_scale=2.0 ** -4)
+    w = W.make_workload(spec, "split")
+    r = run(w)
+    b = brute_decode(w)
+    _close(r["out"], b["out"], what="fp8 brute out")
+    _close(r["max_logits"], b["max_logits"], what="fp8 brute max_logits")
+    # linearity in the scales: seq_len 1 logit ~ k_scale, output ~ v_scale
+    r2 = run(_clone(w, k_scale=2 * w.k_scale, v_scale=3 * w.v_scale))
+    _close(r2["max_logits"][0], 2 * r["max_logits"][0], rtol=1e-14, what="k_scale linear")
+    _close(r2["out"][0], 3 * r["out"][0], rtol=1e-14, what="v_scale linear")
+    # same logical values in an fp32 cache (split layout with x = 4)
+    k8 = W.storage_to_f64(w.key_cache, "e4m3").transpose(0, 1, 3, 2, 4).reshape(
+        w.num_blocks, 2, w.block_size, 16) * w.k_scale
+    v8 = W.storage_to_f64(w.value_cache, "e4m3").transpose(0, 1, 3, 2) * w.v_scale
+    q32 = W.storage_to_f64(w.query, "bf16").astype(np.float32)
+    w32 = _clone(w, dtype="f32", kv_dtype=None, k_scale=1.0, v_scale=1.0, query=q32)
+    w32 = _from_logical(w32, k8, v8)
+    r32 = run(w32)
+    _close(r["out"], r32["out"], rtol=1e-12, what="fp8 vs decoded fp32 cache")
+    _close(r["exp_sums"], r32["exp_sums"], rtol=1e-12, what="fp8 vs decoded fp32 exp_sums")
+
+
 ALL_PINS = [
     pin_brute, pin_sdpa, pin_partitioned_equals_dense, pin_seq_len_one,
     pin_identical_v_rows, pin_pool_permutation, pin_split_equals_nhd, pin_zero_query,
     pin_exp_sum_bounds, pin_softcap, pin_two_token_softmax, pin_alibi_closed_form,
     pin_gqa_mapping, pin_poison_never_read, pin_partitions_at_100k, pin_sliding_window,
+    pin_fp8_cache,
 ]
 
 

@@ -55,6 +55,10 @@ MUTATIONS = [
      "v = ldexp((double)(1024 + f), e - 24);", 0),
     ("window_off_by_one", "t_lo = len - 1 - a->window_left;", "t_lo = len - a->window_left;", 0),
     ("window_ignored", "    if (a->window_left >= 0 && len - 1 - a->window_left > 0) t_lo = len - 1 - a->window_left;\n", "", 0),
+    ("scales_swapped", "(a->k_scale * load_elem(a->key_cache", "(a->v_scale * load_elem(a->key_cache", 0),
+    ("e4m3_bias", "else v = ldexp((double)(8 + f), e - 10);", "else v = ldexp((double)(8 + f), e - 11);", 0),
+    ("e5m2_subnormal", "v = ldexp((double)f, -16);", "v = ldexp((double)f, -15);", 0),
+    ("fp8_split_packing", "int x = 16 / elem_bytes(cache_dtype(a));", "int x = 16 / elem_bytes(a->dtype);", 0),
     ("unused_partition_sum_one", "if (a->exp_sums) a->exp_sums[stat_off + p] = 0.0;",
      "if (a->exp_sums) a->exp_sums[stat_off + p] = 1.0;", 0),
 ]

@@ -42,9 +42,11 @@ DTYPES = ("f32", "f16", "bf16")
 LAYOUTS = ("split", "nhd")
 
 # storage numpy dtype per dtype name (bf16 is carried as raw uint16 bits)
-_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
-_ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
-_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+_STORAGE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "e4m3": np.uint8,
+            "e5m2": np.uint8}
+_ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1}
+_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F, "e5m2": 0x7E}
+KV_FP8 = ("e4m3", "e5m2")
 
 # blocks generated per RNG chunk; fixed so values do not depend on memory limits
 _CHUNK_BLOCKS = 512
@@ -68,6 +70,9 @@ class Spec:
     softcap: float = 0.0
     seed_index: int = 0
     poison: bool = True
+    kv_dtype: Optional[str] = None        # "e4m3" / "e5m2": fp8 cache holding K / k_scale, V / v_scale
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
 
 SPECS = {
@@ -78,6 +83,11 @@ SPECS = {
                    seed_index=3),
     "large_batch": Spec("large_batch", 128, 64, 8, 128, "bf16", seq_len=16384, value_mult=2.0,
                         softcap=30.0, seed_index=4),
+    # fp8 KV caches (kv_cache_dtype / k_scale / v_scale): the 4K and 100K workloads
+    "gqa4k_fp8": Spec("gqa4k_fp8", 32, 28, 4, 128, "f16", seq_len=4096, seed_index=5,
+                      kv_dtype="e4m3", k_scale=2.0 ** -6, v_scale=2.0 ** -6),
+    "long100k_fp8": Spec("long100k_fp8", 4, 28, 4, 128, "bf16", seq_len=100000, seed_index=6,
+                         kv_dtype="e4m3", k_scale=2.0 ** -6, v_scale=2.0 ** -6),
 }
 
 DESCRIPTIONS = {
@@ -86,6 +96,8 @@ DESCRIPTIONS = {
     "long100k": "long context: 4 seqs x 100000 (196 partitions), 28/4 heads, d=128, block 16, bf16",
     "ragged": "ragged batch: 256 seqs, lens log-uniform [1,32768], 32/8 heads, d=128, fp16, ALiBi",
     "large_batch": "large batch: 128 seqs x 16384, 64/8 heads, d=128, bf16 (x2), softcap 30",
+    "gqa4k_fp8": "GQA decode, fp8 e4m3 KV cache (scales 2^-6): 32 seqs x 4096, 28/4 heads, d=128, fp16 query",
+    "long100k_fp8": "long context, fp8 e4m3 KV cache (scales 2^-6): 4 seqs x 100000, 28/4 heads, d=128, bf16 query",
 }
 
 
@@ -112,10 +124,18 @@ class Workload:
     alibi_slopes: Optional[np.ndarray]
     meta: dict = field(default_factory=dict)
     window_left: int = -1  # sliding window: keys t >= seq_len - 1 - window_left (-1 = none)
+    kv_dtype: Optional[str] = None  # fp8 cache type, None = same as dtype
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def cache_dtype(self) -> str:
+        return self.kv_dtype or self.dtype
 
     @property
     def elem_bytes(self) -> int:
-        return _ELEM_BYTES[self.dtype]
+        """Bytes per element of the K / V caches."""
+        return _ELEM_BYTES[self.cache_dtype]
 
     @property
     def max_num_partitions(self) -> int:
@@ -144,12 +164,25 @@ def round_to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+def quantize_fp8(x: np.ndarray, kind: str) -> np.ndarray:
+    """fp32 values -> fp8 bits (uint8) with torch's casts (saturated to the finite range)."""
+    import torch
+    lim = 448.0 if kind == "e4m3" else 57344.0
+    t = torch.from_numpy(np.clip(np.asarray(x, dtype=np.float32), -lim, lim))
+    tdt = torch.float8_e4m3fn if kind == "e4m3" else torch.float8_e5m2
+    return t.to(tdt).view(torch.uint8).numpy()
+
+
 def storage_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
     """Exact widening of storage values to float64 (for tests)."""
     if dtype in ("f32", "f16"):
         return a.astype(np.float64)
     if dtype == "bf16":
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype in KV_FP8:
+        import torch
+        tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+        return torch.from_numpy(np.ascontiguousarray(a)).view(tdt).double().numpy()
     raise ValueError(dtype)
 
 
@@ -158,6 +191,8 @@ def _nan_value(dtype: str):
         return np.float32(np.nan)
     if dtype == "f16":
         return np.uint16(_NAN_BITS["f16"]).view(np.float16)
+    if dtype in KV_FP8:
+        return np.uint8(_NAN_BITS[dtype])
     return np.uint16(_NAN_BITS["bf16"])
 
 
@@ -257,12 +292,13 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
             valid_slots[assigned[off + nb - 1]] = tail
         off += nb
 
-    sdt = _STORAGE[spec.dtype]
-    kshape = layout_shape("k", layout, spec.dtype, pool, hkv, bs, d)
-    vshape = layout_shape("v", layout, spec.dtype, pool, hkv, bs, d)
+    cdt = spec.kv_dtype or spec.dtype  # storage type of the caches
+    sdt = _STORAGE[cdt]
+    kshape = layout_shape("k", layout, cdt, pool, hkv, bs, d)
+    vshape = layout_shape("v", layout, cdt, pool, hkv, bs, d)
     key_cache = np.empty(kshape, dtype=sdt)
     value_cache = np.empty(vshape, dtype=sdt)
-    nan = _nan_value(spec.dtype)
+    nan = _nan_value(cdt)
 
     def fill(job):
         c0, which = job
@@ -273,11 +309,15 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
         x = g.standard_normal((n, hkv, bs, d), dtype=np.float32)
         if spec.value_mult != 1.0:
             x *= np.float32(spec.value_mult)
-        st = round_to_storage(x, spec.dtype)
+        if spec.kv_dtype:
+            sc = spec.k_scale if which == "k" else spec.v_scale
+            st = quantize_fp8(x / np.float32(sc), spec.kv_dtype)
+        else:
+            st = round_to_storage(x, spec.dtype)
         if spec.poison:
             for i in np.nonzero(valid_slots[c0:c1] < bs)[0]:
                 st[i, :, valid_slots[c0 + i]:, :] = nan
-        dst[c0:c1] = logical_to_layout(st, which, layout, spec.dtype)
+        dst[c0:c1] = logical_to_layout(st, which, layout, cdt)
 
     jobs = [(c0, which) for c0 in range(0, pool, _CHUNK_BLOCKS) for which in ("k", "v")]
     with ThreadPoolExecutor(max_workers=_gen_threads()) as ex:
@@ -295,15 +335,19 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
         value_cache=value_cache, block_tables=tables, seq_lens=lens,
         alibi_slopes=alibi_slopes(spec.num_heads) if spec.alibi else None,
         meta={"seed": seed, "shuffle_seed": shuffle_seed, "spec": spec},
+        kv_dtype=spec.kv_dtype, k_scale=float(np.float32(spec.k_scale)),
+        v_scale=float(np.float32(spec.v_scale)),
     )
 
 
 def small_spec(name="small", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
                dtype="f16", seq_lens=(1, 513, 1100), alibi=False, softcap=0.0,
-               value_mult=1.0, pool_extra=5, seed_index=7, block_size=BLOCK_SIZE) -> Spec:
+               value_mult=1.0, pool_extra=5, seed_index=7, block_size=BLOCK_SIZE,
+               kv_dtype=None, k_scale=1.0, v_scale=1.0) -> Spec:
     """A Spec for tests: explicit lengths, a pool with NaN-poisoned spare blocks."""
     lens = list(seq_lens)
     used = sum(-(-l // block_size) for l in lens)
     return Spec(name, num_seqs, num_heads, num_kv_heads, head_size, dtype,
                 seq_lens=lens, pool_blocks=used + pool_extra, alibi=alibi, softcap=softcap,
-                value_mult=value_mult, seed_index=seed_index, block_size=block_size)
+                value_mult=value_mult, seed_index=seed_index, block_size=block_size,
+                kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
