@@ -185,17 +185,20 @@ def run_ours(args, world, rank, local):
     w = W.make_workload(args.config, args.layout)
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
 
-    def t_(a):
-        if w.dtype == "bf16":
+    def t_(a, dtype=None):
+        dtype = dtype or w.dtype
+        if dtype == "bf16":
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(a))
+        return torch.from_numpy(np.ascontiguousarray(a))  # fp8 caches: raw bytes
+
+    cdt = w.cache_dtype
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     pool_bytes = w.key_cache.nbytes + w.value_cache.nbytes
     copies = max(1, min(8, -(-4 * l2 // pool_bytes)))
     q = t_(w.query).to(dev)
-    kcs = [t_(w.key_cache).to(dev) for _ in range(copies)]
-    vcs = [t_(w.value_cache).to(dev) for _ in range(copies)]
+    kcs = [t_(w.key_cache, cdt).to(dev) for _ in range(copies)]
+    vcs = [t_(w.value_cache, cdt).to(dev) for _ in range(copies)]
     bt = torch.from_numpy(w.block_tables).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
     al = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(dev)
@@ -207,6 +210,7 @@ def run_ours(args, world, rank, local):
                                                                  w.max_seq_len, sm_count)
     fused = False  # no partition counters: v2 always launches the reduce kernel
     common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
+                  kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
                   alibi_slopes=al, softcap=w.softcap, layout=w.layout, mode=mode,
                   dev_error=err, **ws)
     cargs = [pa.make_args(out, q, kcs[i], vcs[i], bt, sl, **common) for i in range(copies)]
@@ -306,8 +310,8 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         hq = t_(w.query).pin_memory()
-        hk = t_(w.key_cache).pin_memory()
-        hv = t_(w.value_cache).pin_memory()
+        hk = t_(w.key_cache, cdt).pin_memory()
+        hv = t_(w.value_cache, cdt).pin_memory()
         hbt = torch.from_numpy(w.block_tables).pin_memory()
         hsl = torch.from_numpy(w.seq_lens).pin_memory()
         hal = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).pin_memory()

@@ -63,13 +63,21 @@ typedef enum pa_status {
     PA_ERR_DEVICE_TIMEOUT = 6 /* reserved for callers mapping dev_error bits    */
 } pa_status;
 
-/* Storage type of query, key_cache, value_cache and out (one type for all). */
+/* Storage type of query and out (and of the caches unless kv_dtype says otherwise). */
 typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_F16 = 1, PA_DTYPE_BF16 = 2 } pa_dtype;
+
+/* Storage type of key_cache / value_cache (kv_cache_dtype / k_scale / v_scale of
+ * paged_attention_v2_pytorch.py): the caches hold K / k_scale and V / v_scale. */
+typedef enum pa_kv_dtype {
+    PA_KV_SAME = 0,      /* same as dtype */
+    PA_KV_FP8_E4M3 = 3,  /* OCP fp8 E4M3 (bias 7, no infinities); split layout, f16/bf16 query */
+    PA_KV_FP8_E5M2 = 4   /* OCP fp8 E5M2 (bias 15); split layout, f16/bf16 query */
+} pa_kv_dtype;
 
 /*
  * Cache layouts.
  *  PA_LAYOUT_SPLIT: key_cache   [num_blocks][num_kv_heads][head_size/x][block_size][x],
- *                   x = 16 / sizeof(element) (8 for f16/bf16, 4 for f32);
+ *                   x = 16 / sizeof(element) (16 for fp8, 8 for f16/bf16, 4 for f32);
  *                   value_cache [num_blocks][num_kv_heads][head_size][block_size]
  *                   (key_cache / value_cache shape comments of
  *                   paged_attention_v2_pytorch.py).
@@ -155,6 +163,13 @@ typedef struct pa_decode_args {
      * Partitions with no key in the window are skipped (unused: max_logits
      * -inf, exp_sums 0). */
     int32_t sliding_window;
+    /* pa_kv_dtype of the caches (0 = same as dtype).  For fp8 caches the split
+     * key layout packs x = 16 elements per 16 bytes. */
+    int32_t kv_dtype;
+    /* Dequantisation scales of fp8 caches: K = k_scale * fp8(K), V = v_scale *
+     * fp8(V); values <= 0 mean 1.0 (so a zero-initialised struct has none). */
+    float k_scale;
+    float v_scale;
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the

@@ -23,6 +23,7 @@ __all__ = ["pa_decode", "pa_decode_static_workspace", "alloc_workspace", "max_nu
 
 _LAYOUTS = {"split": _abi.PA_LAYOUT_SPLIT, "nhd": _abi.PA_LAYOUT_NHD}
 _MODES = {"auto": _abi.PA_MODE_AUTO, "v1": _abi.PA_MODE_V1, "v2": _abi.PA_MODE_V2}
+_KV = {None: _abi.PA_KV_SAME, "e4m3": _abi.PA_KV_FP8_E4M3, "e5m2": _abi.PA_KV_FP8_E5M2}
 
 
 class PaDecodeError(RuntimeError):
@@ -81,11 +82,14 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               alibi_slopes=None, softcap: float = 0.0, layout: str = "split", mode: str = "auto",
               exp_sums=None, max_logits=None, tmp_out=None, dev_error=None,
               event_begin=None, event_end=None, partition_counters=None,
-              window_left: int = -1) -> _abi.PaDecodeArgs:
+              window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> _abi.PaDecodeArgs:
     """Build the C argument struct (no checks beyond shapes; the library validates).
 
     window_left follows AttnDispatchConfig (-1 = no window; the query sees the
-    keys t >= seq_len - 1 - window_left) and becomes sliding_window = window_left + 1."""
+    keys t >= seq_len - 1 - window_left) and becomes sliding_window = window_left + 1.
+    kv_dtype "e4m3" / "e5m2" marks fp8 caches (raw uint8 tensors) holding K / k_scale
+    and V / v_scale; the query dtype sets the compute and output type."""
     num_seqs, num_heads, head_size = query.shape
     num_blocks = key_cache.shape[0]
     return _abi.PaDecodeArgs(
@@ -101,6 +105,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         event_main_end=None if event_end is None else event_end.cuda_event,
         partition_counters=_ptr(partition_counters),
         sliding_window=int(window_left) + 1 if window_left >= 0 else 0,
+        kv_dtype=_KV[kv_dtype], k_scale=float(k_scale), v_scale=float(v_scale),
     )
 
 

@@ -22,6 +22,7 @@ PA_ERR_DEVICE_TIMEOUT = 6
 PA_DTYPE_F32, PA_DTYPE_F16, PA_DTYPE_BF16 = 0, 1, 2
 PA_LAYOUT_SPLIT, PA_LAYOUT_NHD = 0, 1
 PA_MODE_AUTO, PA_MODE_V1, PA_MODE_V2 = 0, 1, 2
+PA_KV_SAME, PA_KV_FP8_E4M3, PA_KV_FP8_E5M2 = 0, 3, 4
 
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SEQ_LEN = 2
@@ -68,6 +69,9 @@ class PaDecodeArgs(ctypes.Structure):
         ("event_main_end", ctypes.c_void_p),
         ("partition_counters", ctypes.c_void_p),
         ("sliding_window", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 

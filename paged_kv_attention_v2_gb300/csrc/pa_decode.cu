@@ -137,7 +137,13 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     if (a->layout != PA_LAYOUT_SPLIT && a->layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
     if (a->mode != PA_MODE_AUTO && a->mode != PA_MODE_V1 && a->mode != PA_MODE_V2)
         return PA_ERR_INVALID_ARG;
-    if (!std::isfinite(a->scale) || !std::isfinite(a->softcap)) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(a->scale) || !std::isfinite(a->softcap) || !std::isfinite(a->k_scale) ||
+        !std::isfinite(a->v_scale))
+        return PA_ERR_INVALID_ARG;
+    const int kv = a->kv_dtype;
+    if (kv != PA_KV_SAME && kv != PA_KV_FP8_E4M3 && kv != PA_KV_FP8_E5M2) return PA_ERR_INVALID_ARG;
+    if (kv != PA_KV_SAME && (a->dtype == PA_DTYPE_F32 || a->layout != PA_LAYOUT_SPLIT))
+        return PA_ERR_UNSUPPORTED;
     if (a->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
     if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
     const int group = a->num_heads / a->num_kv_heads;
@@ -192,7 +198,9 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.max_blocks_per_seq = a->max_blocks_per_seq;
     p.max_seq_len = a->max_seq_len;
     p.max_parts = max_parts;
-    p.scale = a->scale;
+    const float k_scale = (kv != PA_KV_SAME && a->k_scale > 0.f) ? a->k_scale : 1.f;
+    p.scale = a->scale * k_scale;  // q.(k_scale k8) = k_scale (q.k8): folded into the logit scale
+    p.v_scale = (kv != PA_KV_SAME && a->v_scale > 0.f) ? a->v_scale : 1.f;
     p.softcap = a->softcap > 0.f ? a->softcap : 0.f;
     p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
     p.v1 = v1 ? 1 : 0;
@@ -226,10 +234,11 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     la.grid_override = 0;
 
     cudaError_t e;
+    const int kvk = kv == PA_KV_FP8_E4M3 ? pa::kKvE4M3 : pa::kKvE5M2;
     switch (a->dtype) {
     case PA_DTYPE_F32: e = pa::launch_f32(p, la); break;
-    case PA_DTYPE_F16: e = pa::launch_f16(p, la); break;
-    default: e = pa::launch_bf16(p, la); break;
+    case PA_DTYPE_F16: e = kv == PA_KV_SAME ? pa::launch_f16(p, la) : pa::launch_f16_fp8(p, la, kvk); break;
+    default: e = kv == PA_KV_SAME ? pa::launch_bf16(p, la) : pa::launch_bf16_fp8(p, la, kvk); break;
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }

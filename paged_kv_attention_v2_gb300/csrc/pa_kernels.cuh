@@ -34,9 +34,17 @@ constexpr int kNHD = PA_LAYOUT_NHD;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Cache element kinds (template parameter KV of the partition kernel).
+constexpr int kKvSame = 0;      // same 16-bit / 32-bit type as the query
+constexpr int kKvE4M3 = 1;      // fp8 E4M3
+constexpr int kKvE5M2 = 2;      // fp8 E5M2
+
 // Build-time shape of the partition kernel (overridable with -D for sweeps).
 #ifndef PA_STAGES_16BIT
 #define PA_STAGES_16BIT 8      // ring stages (one 16-token page of K and V each), 16-bit caches
+#endif
+#ifndef PA_STAGES_FP8
+#define PA_STAGES_FP8 16       // ring stages, fp8 caches (pages are half the bytes)
 #endif
 #ifndef PA_STAGES_F32
 #define PA_STAGES_F32 4        // ring stages, fp32 caches
@@ -65,7 +73,8 @@ struct Params {
     int32_t* dev_error;
     int num_seqs, num_heads, num_kv_heads, group;
     int num_blocks, max_blocks_per_seq, max_seq_len, max_parts;
-    float scale, softcap, inv_softcap;
+    float scale, softcap, inv_softcap;  // scale includes k_scale for fp8 caches
+    float v_scale;                       // fp8 caches: applied to the partition outputs
     int v1;
     int32_t* counters;  // [num_seqs][num_kv_heads] finished partitions (fused v2 only)
     int window_left;    // < 0: no window; else keys t >= len - 1 - window_left
@@ -99,19 +108,21 @@ __device__ __forceinline__ int tile_pages(int tb, int te) {
 
 // ------------------------------------------------------------------ config
 
-template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV = kKvSame>
 struct Cfg {
     static constexpr bool kF32 = std::is_same<T, float>::value;
     static constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int kElem = sizeof(T);
-    static constexpr int kPageBytes = kBS * HEAD * kElem;  // one page of K (or of V)
+    static constexpr int kElem = sizeof(T);                // query / output element
+    static constexpr int kKvElem = KV == kKvSame ? (int)sizeof(T) : 1;
+    static constexpr int kPageBytes = kBS * HEAD * kKvElem;  // one page of K (or of V)
     static constexpr int kStageBytes = 2 * kPageBytes;
     static constexpr int kMaxG = kF32 ? 16 : NT * 8;       // heads per kv head handled
     static constexpr int kQBytes = kMaxG * HEAD * kElem;
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
-    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32;
+    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32 && KV == kKvSame;
+    static_assert(KV == kKvSame || (LAYOUT == kSplit && !kF32), "fp8 caches: split layout, 16-bit query");
     static constexpr int kScratchFloats = kF32 ? NC * (kBS * 16 + 16) : 0;
 
     static constexpr int oRing = 0;
@@ -372,7 +383,7 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
             o.z += c * a.z;
             o.w += c * a.w;
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float inv = L > 0.f ? p.v_scale / L : 0.f;
         o.x *= inv;
         o.y *= inv;
         o.z *= inv;
@@ -575,7 +586,37 @@ __device__ __forceinline__ void zero_v_tail16(uint32_t vpage, int valid, int lan
     }
 }
 
-template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+// Two adjacent fp8 cache elements (shared address a, 2-byte aligned) as a
+// packed pair of the MMA input type.  fp8 -> fp16 is exact; fp16 -> bf16 is
+// exact for these values (at most 4 significant bits, exponent within range).
+template <int KV, bool BF>
+__device__ __forceinline__ uint32_t fp8_pair(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    uint32_t h;
+    if constexpr (KV == kKvE4M3)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h) : "h"(v));
+    if constexpr (BF) {
+        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+        __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        return *reinterpret_cast<uint32_t*>(&b);
+    }
+    return h;
+}
+
+// Zero the fp8 V entries of tokens >= valid in a staged split page [d][16 tokens].
+template <int HEAD>
+__device__ __forceinline__ void zero_v_tail8(uint32_t vpage, int valid, int lane) {
+    for (int d = lane; d < HEAD; d += 32)
+        for (int t = valid; t < kBS; ++t)
+            asm volatile("st.shared.u8 [%0], %1;" ::"r"(vpage + (uint32_t)(d * kBS + t)),
+                         "h"((unsigned short)0)
+                         : "memory");
+}
+
+template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV>
 __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane) {
     constexpr bool BF = C::kBF16;
     constexpr int KT = HEAD / 16;  // k-steps of Q.K^T, m-tiles of P.V
@@ -654,7 +695,10 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
             const int skip = d.tok_begin - tok0;          // slots < skip: before the window
             if (valid < kBS) {
-                zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
+                if constexpr (KV == kKvSame)
+                    zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
+                else
+                    zero_v_tail8<HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -669,7 +713,16 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
+                if constexpr (KV == kKvSame) {
+                    ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
+                } else {
+                    // fp8 split key page [d/16][token][16]: (token r, dims 16kk + 2cq ..)
+                    const uint32_t ka = kp + (uint32_t)((kk * kBS + r) * 16 + 2 * cq);
+                    a0 = fp8_pair<KV, BF>(ka);
+                    a1 = fp8_pair<KV, BF>(ka + 8 * 16);
+                    a2 = fp8_pair<KV, BF>(ka + 8);
+                    a3 = fp8_pair<KV, BF>(ka + 8 * 16 + 8);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     if (kk & 1)
@@ -739,7 +792,14 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                if constexpr (LAYOUT == kSplit)
+                if constexpr (KV != kKvSame) {
+                    // fp8 split value page [d][token]: (dim 16mt + r, tokens 2cq ..)
+                    const uint32_t va = vp + (uint32_t)((mt * 16 + r) * kBS + 2 * cq);
+                    a0 = fp8_pair<KV, BF>(va);
+                    a1 = fp8_pair<KV, BF>(va + 8 * kBS);
+                    a2 = fp8_pair<KV, BF>(va + 8);
+                    a3 = fp8_pair<KV, BF>(va + 8 * kBS + 8);
+                } else if constexpr (LAYOUT == kSplit)
                     ldsm_x4(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
                 else
                     ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
@@ -962,11 +1022,11 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 
 // ------------------------------------------------------------------ kernels
 
-template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV>
 __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
-    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1017,7 +1077,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     } else if constexpr (C::kF32) {
         consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
     } else {
-        consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+        consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC, KV>(p, sm, warp, lane);
     }
 }
 

@@ -34,12 +34,13 @@ constexpr int kMaxDevices = 64;
 // (a short merge).  With several rounds the CTA that merges falls behind and
 // becomes the last arriver of the next group too, so merges pile up on a few
 // CTAs; the separate reduce kernel spreads them over the whole GPU instead.
-template <typename T, int HEAD, int NT, int LAYOUT>
+template <typename T, int HEAD, int NT, int LAYOUT, int KV>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
-    constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32 : PA_STAGES_16BIT;
+    constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32
+                           : (KV == kKvSame ? PA_STAGES_16BIT : PA_STAGES_FP8);
     constexpr int NC = PA_CONSUMER_WARPS;
-    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC>;
-    auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC>;
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
+    auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
 
     static std::atomic<int> occ_cache[kMaxDevices];
     int dev = 0;
@@ -108,27 +109,31 @@ cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     return launch_reduce_shape<T, HEAD, 8, 4>(p, la);
 }
 
-template <typename T, int HEAD, int NT>
+template <typename T, int HEAD, int NT, int KV>
 cudaError_t launch_layout(const Params& p, const LaunchArgs& la, bool* fused) {
-    return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD>(p, la, fused)
-                             : launch_main<T, HEAD, NT, kSplit>(p, la, fused);
+    if constexpr (KV != kKvSame) {  // fp8 caches: split layout only (checked by the host)
+        return launch_main<T, HEAD, NT, kSplit, KV>(p, la, fused);
+    } else {
+        return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD, KV>(p, la, fused)
+                                 : launch_main<T, HEAD, NT, kSplit, KV>(p, la, fused);
+    }
 }
 
-// Whole operation for one storage type.
-template <typename T>
+// Whole operation for one (query type, cache type) pair.
+template <typename T, int KV = kKvSame>
 cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
     constexpr bool F32 = std::is_same<T, float>::value;
     cudaError_t e;
     bool fused = false;
     if constexpr (F32) {  // one fp32 consumer handles up to 16 heads
-        e = la.head_size == 128 ? launch_layout<T, 128, 2>(p, la, &fused)
-                                : launch_layout<T, 64, 2>(p, la, &fused);
+        e = la.head_size == 128 ? launch_layout<T, 128, 2, KV>(p, la, &fused)
+                                : launch_layout<T, 64, 2, KV>(p, la, &fused);
     } else if (la.head_size == 128) {
-        e = la.group_tiles == 2 ? launch_layout<T, 128, 2>(p, la, &fused)
-                                : launch_layout<T, 128, 1>(p, la, &fused);
+        e = la.group_tiles == 2 ? launch_layout<T, 128, 2, KV>(p, la, &fused)
+                                : launch_layout<T, 128, 1, KV>(p, la, &fused);
     } else {
-        e = la.group_tiles == 2 ? launch_layout<T, 64, 2>(p, la, &fused)
-                                : launch_layout<T, 64, 1>(p, la, &fused);
+        e = la.group_tiles == 2 ? launch_layout<T, 64, 2, KV>(p, la, &fused)
+                                : launch_layout<T, 64, 1, KV>(p, la, &fused);
     }
     if (e != cudaSuccess || p.v1 || fused) return e;
     return la.head_size == 128 ? launch_reduce<T, 128>(p, la) : launch_reduce<T, 64>(p, la);
@@ -137,5 +142,7 @@ cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
 cudaError_t launch_f32(const Params& p, const LaunchArgs& la);
 cudaError_t launch_f16(const Params& p, const LaunchArgs& la);
 cudaError_t launch_bf16(const Params& p, const LaunchArgs& la);
+cudaError_t launch_f16_fp8(const Params& p, const LaunchArgs& la, int kv);   // kv: kKvE4M3 / kKvE5M2
+cudaError_t launch_bf16_fp8(const Params& p, const LaunchArgs& la, int kv);
 
 }  // namespace pa

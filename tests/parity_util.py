@@ -24,16 +24,19 @@ def torch_dtype(dtype: str):
 
 
 def to_torch(a: np.ndarray, dtype: str) -> torch.Tensor:
+    if dtype in ("e4m3", "e5m2"):
+        return torch.from_numpy(np.ascontiguousarray(a))  # raw fp8 bytes
     if dtype == "bf16":
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(a))
 
 
 def to_device(w, device="cuda:0"):
+    cdt = getattr(w, "kv_dtype", None) or w.dtype  # fp8 caches: raw uint8 tensors
     d = {
         "query": to_torch(w.query, w.dtype).to(device),
-        "key_cache": to_torch(w.key_cache, w.dtype).to(device),
-        "value_cache": to_torch(w.value_cache, w.dtype).to(device),
+        "key_cache": to_torch(w.key_cache, cdt).to(device),
+        "value_cache": to_torch(w.value_cache, cdt).to(device),
         "block_tables": torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
         "seq_lens": torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(device),
         "alibi_slopes": None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(device),
@@ -69,7 +72,9 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                      num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
                      alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
                      mode=mode, dev_error=err, partition_counters=counters,
-                     window_left=getattr(w, "window_left", -1), **ws)
+                     window_left=getattr(w, "window_left", -1),
+                     kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
+                     v_scale=getattr(w, "v_scale", 1.0), **ws)
     torch.cuda.synchronize(device)
     if counters is not None:
         assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"

@@ -30,7 +30,8 @@ def _workload(name, layout):
 
 
 FULL = [("tiny", "split"), ("tiny", "nhd"), ("gqa4k", "split"), ("gqa4k", "nhd"),
-        ("long100k", "split"), ("long100k", "nhd"), ("ragged", "split"), ("ragged", "nhd")]
+        ("long100k", "split"), ("long100k", "nhd"), ("ragged", "split"), ("ragged", "nhd"),
+        ("gqa4k_fp8", "split"), ("long100k_fp8", "split")]
 
 
 @pytest.mark.parametrize("name,layout", FULL, ids=[f"{n}-{l}" for n, l in FULL])
@@ -205,3 +206,31 @@ def test_sliding_window_ragged_full_size():
                 check_stats(w, g, ref)
     finally:
         w.window_left = -1
+
+
+FP8 = [
+    # name, query dtype, kv dtype, H, Hkv, d, lens, alibi, softcap, window_left, k_scale, v_scale
+    ("e4m3_f16", "f16", "e4m3", 8, 2, 128, (1, 15, 17, 513, 1100), False, 0.0, -1, 2 ** -6, 2 ** -6),
+    ("e4m3_bf16_alibi", "bf16", "e4m3", 16, 2, 128, (600, 2049), True, 0.0, -1, 0.05, 0.02),
+    ("e5m2_f16_softcap", "f16", "e5m2", 7, 1, 128, (33, 1500), False, 30.0, -1, 0.5, 0.25),
+    ("e5m2_bf16_head64", "bf16", "e5m2", 6, 3, 64, (5, 1030), False, 0.0, -1, 1.0, 1.0),
+    ("e4m3_group16_window", "bf16", "e4m3", 32, 2, 128, (1, 3000), True, 0.0, 700, 2 ** -5, 2 ** -4),
+    ("e4m3_group9", "f16", "e4m3", 18, 2, 64, (100, 513), False, 0.0, -1, 0.01, 0.03),
+]
+
+
+@pytest.mark.parametrize("case", FP8, ids=[c[0] for c in FP8])
+@pytest.mark.parametrize("mode", ["v1", "v2", "v2f"])
+def test_fp8_cache(case, mode):
+    name, dtype, kv, H, Hkv, d, lens, alibi, cap, wl, ks, vs = case
+    spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
+                        head_size=d, dtype=dtype, seq_lens=lens, alibi=alibi, softcap=cap,
+                        kv_dtype=kv, k_scale=ks, v_scale=vs)
+    w = W.make_workload(spec, "split")
+    w.window_left = wl
+    ref = oracle.oracle_decode(w)
+    g = run_gpu(w, mode=mode, calls=2)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], ref["out"])
+    if mode in ("v2", "v2f"):
+        check_stats(w, g, ref)
