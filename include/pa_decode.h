@@ -100,6 +100,7 @@ typedef enum pa_mode { PA_MODE_AUTO = 0, PA_MODE_V1 = 1, PA_MODE_V2 = 2 } pa_mod
 #define PA_DEVERR_BLOCK_ID   1  /* a block table entry outside [0, num_blocks); page 0 read instead */
 #define PA_DEVERR_SEQ_LEN    2  /* seq_lens[s] < 0 or > max_seq_len; clamped into [0, max_seq_len] */
 #define PA_DEVERR_TIMEOUT    4  /* an internal pipeline wait exceeded its limit; results invalid   */
+#define PA_DEVERR_QUERY_RANGE 8 /* fp8 caches with a bf16 query: |q| > 65504 clamped (fp16 MMAs)  */
 
 typedef struct pa_decode_args {
     /* [num_seqs][num_heads][head_size], dtype; written.  16-byte aligned. */

@@ -84,7 +84,9 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               event_begin=None, event_end=None, partition_counters=None,
               window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
               v_scale: float = 1.0) -> _abi.PaDecodeArgs:
-    """Build the C argument struct (no checks beyond shapes; the library validates).
+    """Build the C argument struct.  The library validates sizes and types it can
+    see; this also checks what only the tensors know: the caches' element size
+    and element count against kv_dtype, head_size and num_kv_heads.
 
     window_left follows AttnDispatchConfig (-1 = no window; the query sees the
     keys t >= seq_len - 1 - window_left) and becomes sliding_window = window_left + 1.
@@ -92,6 +94,15 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
     and V / v_scale; the query dtype sets the compute and output type."""
     num_seqs, num_heads, head_size = query.shape
     num_blocks = key_cache.shape[0]
+    kv_bytes = 1 if kv_dtype in ("e4m3", "e5m2") else query.element_size()
+    page = num_kv_heads * block_size * head_size  # elements of one block of one cache
+    for name, c in (("key_cache", key_cache), ("value_cache", value_cache)):
+        if c.element_size() != kv_bytes:
+            raise ValueError(f"{name} has {c.element_size()}-byte elements, kv_dtype "
+                             f"{kv_dtype or 'same as query'} needs {kv_bytes}")
+        if c.numel() != num_blocks * page:
+            raise ValueError(f"{name} holds {c.numel()} elements, expected "
+                             f"num_blocks {num_blocks} x {page}")
     return _abi.PaDecodeArgs(
         out=_ptr(out), query=_ptr(query), key_cache=_ptr(key_cache),
         value_cache=_ptr(value_cache), block_tables=_ptr(block_tables), seq_lens=_ptr(seq_lens),

@@ -27,6 +27,7 @@ PA_KV_SAME, PA_KV_FP8_E4M3, PA_KV_FP8_E5M2 = 0, 3, 4
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SEQ_LEN = 2
 PA_DEVERR_TIMEOUT = 4
+PA_DEVERR_QUERY_RANGE = 8
 
 PA_PARTITION_SIZE = 512
 PA_BLOCK_SIZE = 16

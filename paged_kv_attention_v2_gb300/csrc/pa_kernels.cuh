@@ -44,7 +44,7 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #define PA_STAGES_16BIT 8      // ring stages (one 16-token page of K and V each), 16-bit caches
 #endif
 #ifndef PA_STAGES_FP8
-#define PA_STAGES_FP8 16       // ring stages, fp8 caches (pages are half the bytes)
+#define PA_STAGES_FP8 12       // ring stages, fp8 caches (three CTAs per SM fit)
 #endif
 #ifndef PA_STAGES_F32
 #define PA_STAGES_F32 4        // ring stages, fp32 caches
@@ -586,26 +586,6 @@ __device__ __forceinline__ void zero_v_tail16(uint32_t vpage, int valid, int lan
     }
 }
 
-// Two adjacent fp8 cache elements (shared address a, 2-byte aligned) as a
-// packed pair of the MMA input type.  fp8 -> fp16 is exact; fp16 -> bf16 is
-// exact for these values (at most 4 significant bits, exponent within range).
-template <int KV, bool BF>
-__device__ __forceinline__ uint32_t fp8_pair(uint32_t a) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    uint32_t h;
-    if constexpr (KV == kKvE4M3)
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
-    else
-        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h) : "h"(v));
-    if constexpr (BF) {
-        const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
-        __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-        return *reinterpret_cast<uint32_t*>(&b);
-    }
-    return h;
-}
-
 // Zero the fp8 V entries of tokens >= valid in a staged split page [d][16 tokens].
 template <int HEAD>
 __device__ __forceinline__ void zero_v_tail8(uint32_t vpage, int valid, int lane) {
@@ -616,7 +596,7 @@ __device__ __forceinline__ void zero_v_tail8(uint32_t vpage, int valid, int lane
                          : "memory");
 }
 
-template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV>
+template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane) {
     constexpr bool BF = C::kBF16;
     constexpr int KT = HEAD / 16;  // k-steps of Q.K^T, m-tiles of P.V
@@ -695,10 +675,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
             const int skip = d.tok_begin - tok0;          // slots < skip: before the window
             if (valid < kBS) {
-                if constexpr (KV == kKvSame)
-                    zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
-                else
-                    zero_v_tail8<HEAD>(vp, valid, lane);
+                zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -713,16 +690,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a0, a1, a2, a3;
-                if constexpr (KV == kKvSame) {
-                    ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
-                } else {
-                    // fp8 split key page [d/16][token][16]: (token r, dims 16kk + 2cq ..)
-                    const uint32_t ka = kp + (uint32_t)((kk * kBS + r) * 16 + 2 * cq);
-                    a0 = fp8_pair<KV, BF>(ka);
-                    a1 = fp8_pair<KV, BF>(ka + 8 * 16);
-                    a2 = fp8_pair<KV, BF>(ka + 8);
-                    a3 = fp8_pair<KV, BF>(ka + 8 * 16 + 8);
-                }
+                ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     if (kk & 1)
@@ -792,14 +760,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                if constexpr (KV != kKvSame) {
-                    // fp8 split value page [d][token]: (dim 16mt + r, tokens 2cq ..)
-                    const uint32_t va = vp + (uint32_t)((mt * 16 + r) * kBS + 2 * cq);
-                    a0 = fp8_pair<KV, BF>(va);
-                    a1 = fp8_pair<KV, BF>(va + 8 * kBS);
-                    a2 = fp8_pair<KV, BF>(va + 8);
-                    a3 = fp8_pair<KV, BF>(va + 8 * kBS + 8);
-                } else if constexpr (LAYOUT == kSplit)
+                if constexpr (LAYOUT == kSplit)
                     ldsm_x4(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
                 else
                     ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
@@ -845,6 +806,253 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             return;
         }
         if (!tile_finish<C, T, HEAD, NC>(p, d, sm, warp, lane, mphase)) {  // merge buffers free again
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        gbase += (uint32_t)npages;
+    }
+}
+
+// Four fp8 cache elements (one 32-bit word, lowest address in the low byte) as
+// two f16x2 pairs: lo = elements 0, 1 and hi = elements 2, 3 (exact).
+template <int KV>
+__device__ __forceinline__ void fp8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (KV == kKvE4M3)
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    else
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "cvt.rn.f16x2.e5m2x2 %0, l;\n\tcvt.rn.f16x2.e5m2x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// Consumer for fp8 caches (split layout).  The tensor-core inputs are fp16 for
+// both query types: fp8 -> fp16 is exact; a bf16 query is converted once per
+// tile (values beyond the fp16 range are clamped and PA_DEVERR_QUERY_RANGE is
+// set); P is packed to fp16 (11 significant bits, no second term needed).
+// Every lane fetches four fp8 values with one 32-bit shared load.  For that
+// the reduction index of each MMA is permuted identically on both operands:
+//   Q.K^T  k-index 2cq+j <-> head dim 4cq+j, 2cq+8+j <-> 4cq+2+j  (per 16-dim step)
+//   P.V    k-index 2cq+j <-> token    4cq+j, 2cq+8+j <-> 4cq+2+j  (per page)
+// so row rr of S^T (the M index of Q.K^T) holds token tau(rr) of the page:
+//   tau(r) = 4*(r/2) + (r&1) and tau(r+8) = tau(r) + 2 for r < 8.
+template <class C, typename T, int HEAD, int NT, int STAGES, int NC, int KV>
+__device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int lane) {
+    constexpr bool QBF = C::kBF16;
+    constexpr int KT = HEAD / 16;
+    const int G = p.group;
+    const int r = lane >> 2, cq = lane & 3;
+    const int tlo = ((r >> 1) << 2) + (r & 1);  // page token of S^T row r
+    const int thi = tlo + 2;                    // page token of S^T row r + 8
+    const bool has_alibi = p.alibi != nullptr;
+    const bool has_cap = p.softcap > 0.f;
+    uint32_t gbase = 0;
+    uint32_t mphase = 0;
+    for (int k = 0;; ++k) {
+        const int slot = k % C::kTD;
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        const TileDesc d = sm.desc[slot];
+        if (d.flags & kTileStop) return;
+
+        // Q as fp16 B fragments in the permuted head-dim order.
+        uint32_t qb[NT][KT][2];
+        bool q_clamped = false;
+        const uint32_t qs = sm.q + slot * C::kQBytes;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + r;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t w0 = 0, w1 = 0;
+                if (h < G) {
+                    const uint32_t a = qs + (uint32_t)((h * HEAD + kk * 16 + 4 * cq) * 2);
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(a));
+                    if constexpr (QBF) {
+                        float2 f0 = unpack2<true>(w0), f1 = unpack2<true>(w1);
+                        const float lim = 65504.f;
+                        q_clamped |= fabsf(f0.x) > lim || fabsf(f0.y) > lim || fabsf(f1.x) > lim ||
+                                     fabsf(f1.y) > lim;
+                        w0 = pack2<false>(fminf(fmaxf(f0.x, -lim), lim), fminf(fmaxf(f0.y, -lim), lim));
+                        w1 = pack2<false>(fminf(fmaxf(f1.x, -lim), lim), fminf(fmaxf(f1.y, -lim), lim));
+                    }
+                }
+                qb[nt][kk][0] = w0;  // head dims 16kk + 4cq, +1  (k-index 2cq, 2cq+1)
+                qb[nt][kk][1] = w1;  // head dims 16kk + 4cq+2, +3 (k-index 2cq+8, 2cq+9)
+            }
+        }
+        if (q_clamped) report(p, PA_DEVERR_QUERY_RANGE);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);
+
+        float sl[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = nt * 8 + 2 * cq + e;
+                sl[nt][e] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+            }
+        const int origin = d.tok_end - 1;
+
+        float m[NT][2], l[NT][2];
+        float acc[KT][NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+        }
+
+        const int npages = tile_pages(d.tok_begin, d.tok_end);
+        const int page0 = d.tok_begin / kBS * kBS;
+        for (int j = warp; j < npages; j += NC) {
+            const uint32_t gg = gbase + (uint32_t)j;
+            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+                report(p, PA_DEVERR_TIMEOUT);
+                *sm.abort = 1;
+                return;
+            }
+            const uint32_t kp = sm.ring + st * C::kStageBytes;
+            const uint32_t vp = kp + C::kPageBytes;
+            const int tok0 = page0 + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);
+            const int skip = d.tok_begin - tok0;
+            if (valid < kBS) {
+                zero_v_tail8<HEAD>(vp, valid, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // S^T[row][head]: key page [d/16][token][16 bytes]
+            float s[NT][4], s2[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
+                fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (kk & 1)
+                        mma_16816<false>(s2[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                    else
+                        mma_16816<false>(s[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
+
+            const bool in_lo = tlo < valid && tlo >= skip;
+            const bool in_hi = thi < valid && thi >= skip;
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float z[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = s[nt][e] * p.scale;
+                    if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                    if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + ((e >> 1) ? thi : tlo) - origin);
+                    z[e] = v;
+                }
+                if (!in_lo) z[0] = z[1] = -INFINITY;
+                if (!in_hi) z[2] = z[3] = -INFINITY;
+                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+                const float al0 = exp2f((m[nt][0] - mn0) * kLog2e);
+                const float al1 = exp2f((m[nt][1] - mn1) * kLog2e);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+                const float p0 = exp2f((z[0] - mn0) * kLog2e);
+                const float p1 = exp2f((z[1] - mn1) * kLog2e);
+                const float p2 = exp2f((z[2] - mn0) * kLog2e);
+                const float p3 = exp2f((z[3] - mn1) * kLog2e);
+                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    acc[mt][nt][0] *= al0;
+                    acc[mt][nt][1] *= al1;
+                    acc[mt][nt][2] *= al0;
+                    acc[mt][nt][3] *= al1;
+                }
+                pb[nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tau
+                pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));
+            }
+
+            // acc^T[head dim][head] += V^T . P^T: value page [d][16 tokens]
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
+                fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_16816<false>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+        }
+
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], o);
+                l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], o);
+            }
+        }
+        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h0 = nt * 8 + 2 * cq;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                const int d0 = mt * 16 + r;
+                mw[h0 * C::kMergeStride + d0] = acc[mt][nt][0];
+                mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][nt][1];
+                mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][nt][2];
+                mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
+            }
+            if (r == 0) {
+                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+            }
+        }
+        if (!consumer_sync(sm, mphase, lane)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        if (!tile_finish<C, T, HEAD, NC>(p, d, sm, warp, lane, mphase)) {
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -1077,7 +1285,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     } else if constexpr (C::kF32) {
         consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
     } else {
-        consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC, KV>(p, sm, warp, lane);
+        if constexpr (KV == kKvSame)
+            consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+        else
+            consumer_mma_fp8<C, T, HEAD, NT, STAGES, NC, KV>(p, sm, warp, lane);
     }
 }
 

@@ -136,3 +136,23 @@ def test_null_args(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(_abi.LibraryMissing):
         _abi.load(tmp_path / "missing.so")
+
+
+def test_binding_rejects_cache_tensors_that_do_not_match_the_declared_type():
+    """fp8 caches passed without kv_dtype (or the reverse) would make the kernels
+    read past the buffers: the binding refuses them before any call."""
+    import torch
+    q = torch.zeros((2, 8, 128), dtype=torch.float16)
+    k8 = torch.zeros((10, 2, 8, 16, 16), dtype=torch.uint8)      # fp8 split key cache
+    k16 = torch.zeros((10, 2, 16, 16, 8), dtype=torch.float16)   # fp16 split key cache
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    sl = torch.zeros(2, dtype=torch.int32)
+    kw = dict(num_kv_heads=2, scale=0.1, max_seq_len=64)
+    with pytest.raises(ValueError):
+        pa.make_args(q, q, k8, k8, bt, sl, **kw)
+    with pytest.raises(ValueError):
+        pa.make_args(q, q, k16, k16, bt, sl, kv_dtype="e4m3", **kw)
+    with pytest.raises(ValueError):
+        pa.make_args(q, q, k16[:5].clone(), k16, bt, sl, **kw)
+    pa.make_args(q, q, k8, k8, bt, sl, kv_dtype="e4m3", **kw)
+    pa.make_args(q, q, k16, k16, bt, sl, **kw)
