@@ -54,9 +54,10 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device code of the kernels (host-side launch heuristics excluded)."""
     h = hashlib.sha256()
-    for f in sorted((ROOT / "paged_kv_attention_v2_gb300" / "csrc").glob("*")) + \
-            sorted((ROOT / "include").glob("*.h")):
+    csrc = ROOT / "paged_kv_attention_v2_gb300" / "csrc"
+    for f in [csrc / "pa_kernels.cuh", csrc / "pa_ptx.cuh"] + sorted((ROOT / "include").glob("*.h")):
         h.update(f.name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]

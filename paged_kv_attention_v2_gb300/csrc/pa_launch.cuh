@@ -105,7 +105,12 @@ cudaError_t launch_reduce_shape(const Params& p, const LaunchArgs& la) {
 
 template <typename T, int HEAD>
 cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
-    if (p.max_parts > 32) return launch_reduce_shape<T, HEAD, 16, 8>(p, la);
+    // the wide shape only when there are few (sequence, head) rows to spread
+    // (e.g. 4 x 28 rows of 196 partitions); many rows fill the GPU anyway and
+    // most of a ragged batch's rows are short
+    const int64_t rows = (int64_t)p.num_seqs * p.num_heads;
+    if (p.max_parts > 32 && rows <= 2 * (int64_t)la.sm_count)
+        return launch_reduce_shape<T, HEAD, 16, 8>(p, la);
     return launch_reduce_shape<T, HEAD, 8, 4>(p, la);
 }
 
