@@ -218,6 +218,18 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         }
         c_total = __shfl_sync(0xffffffffu, c_incl, 31);
     };
+    // Ramp: in a batch whose sequences all have max_parts partitions the first
+    // tile of this CTA is known before seq_lens is read; load its block ids now,
+    // in parallel with the walk, and keep them only if the walk confirms the tile.
+    int spec_seq = -1, spec_tb = 0, spec_ids = 0;
+    if (!p.v1 && p.window_left < 0) {
+        const int u = blockIdx.x / Hkv;
+        spec_seq = u / p.max_parts;
+        spec_tb = (u - spec_seq * p.max_parts) * kPart;
+        const int idx = spec_tb / kBS + lane;
+        if (spec_seq < S && idx < p.max_blocks_per_seq)
+            spec_ids = __ldg(p.block_tables + (int64_t)spec_seq * p.max_blocks_per_seq + idx);
+    }
     load_chunk(0);
 
     // Tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ... (kv head fastest).
@@ -266,7 +278,16 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     int k = 0;       // tiles issued by this CTA
     bool ok = true;
     ProducerTile cur = next_tile();
-    int ids = load_ids(cur, 0);
+    int ids;
+    if (cur.valid && cur.seq == spec_seq && cur.tb == spec_tb) {
+        ids = lane < cur.npages ? spec_ids : 0;
+        if ((unsigned)ids >= (unsigned)p.num_blocks) {
+            report(p, PA_DEVERR_BLOCK_ID);
+            ids = 0;
+        }
+    } else {
+        ids = load_ids(cur, 0);
+    }
     while (ok && cur.valid) {
         const ProducerTile nxt = next_tile();  // walk ahead while this tile's pages stream
 
@@ -1309,6 +1330,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     const int bid = blockIdx.x;
     const int s = bid / p.num_heads, h = bid - s * p.num_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();  // the next launch may start its prologue; it waits for us
     pdl_wait_primary();
 
     const int len = clamp_len(p, p.seq_lens[s]);
