@@ -54,6 +54,8 @@ class OracleArgs(ctypes.Structure):
         ("softcap", ctypes.c_double),
         ("window_left", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32),
+        ("query_start", ctypes.c_void_p),
+        ("num_query_tokens", ctypes.c_int32),
         ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double),
         ("seq_subset", ctypes.c_void_p),
@@ -121,8 +123,10 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
                   lib_path=None):
     """Evaluate the oracle on a workloads.Workload (or any object with the same fields).
 
-    Returns a dict of float64 arrays indexed by absolute sequence number:
-      out        [num_seqs, num_heads, head_size]   dense softmax attention
+    Returns a dict of float64 arrays indexed by absolute query row (= sequence
+    number with one query token per sequence; with w.query_start, rows
+    query_start[s] .. query_start[s+1]-1 belong to sequence s):
+      out        [rows, num_heads, head_size]   dense softmax attention
       out_v2     same, log-sum-exp reduce of the partitions (if partials)
       max_logits [num_seqs, num_heads, P_max]        (if partials)
       exp_sums   [num_seqs, num_heads, P_max]        (if partials)
@@ -131,6 +135,9 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
     """
     lib = _load(lib_path)
     S, H, d = w.num_seqs, w.num_heads, w.head_size
+    qs = getattr(w, "query_start", None)
+    qs = None if qs is None else np.ascontiguousarray(qs, dtype=np.int32)
+    R = S if qs is None else int(qs[-1])  # rows: query tokens
     if max_num_partitions is None:
         max_num_partitions = max(1, -(-int(w.max_seq_len) // partition_size))
     P = max_num_partitions
@@ -141,12 +148,12 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
     sl = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
     al = None if w.alibi_slopes is None else np.ascontiguousarray(w.alibi_slopes, dtype=np.float32)
     sub = None if seq_subset is None else np.ascontiguousarray(seq_subset, dtype=np.int32)
-    res = {"out": np.full((S, H, d), np.nan)}
+    res = {"out": np.full((R, H, d), np.nan)}
     if partials:
-        res["out_v2"] = np.full((S, H, d), np.nan)
-        res["max_logits"] = np.full((S, H, P), np.nan)
-        res["exp_sums"] = np.full((S, H, P), np.nan)
-        res["tmp_out"] = np.full((S, H, P, d), np.nan)
+        res["out_v2"] = np.full((R, H, d), np.nan)
+        res["max_logits"] = np.full((R, H, P), np.nan)
+        res["exp_sums"] = np.full((R, H, P), np.nan)
+        res["tmp_out"] = np.full((R, H, P, d), np.nan)
     a = OracleArgs(
         query=_ptr(q), key_cache=_ptr(k), value_cache=_ptr(v), block_tables=_ptr(bt),
         seq_lens=_ptr(sl), alibi_slopes=_ptr(al),
@@ -157,6 +164,7 @@ def oracle_decode(w, seq_subset=None, partials: bool = True, threads: int | None
         scale=float(w.scale), softcap=float(w.softcap),
         window_left=int(getattr(w, "window_left", -1)),
         kv_dtype=DTYPE_CODE[w.kv_dtype] if getattr(w, "kv_dtype", None) else -1,
+        query_start=_ptr(qs), num_query_tokens=R,
         k_scale=float(getattr(w, "k_scale", 1.0)), v_scale=float(getattr(w, "v_scale", 1.0)),
         seq_subset=_ptr(sub), n_subset=0 if sub is None else len(sub),
         num_threads=threads or default_threads(),

@@ -12,6 +12,7 @@ Plain Python loops over Python floats; numpy only decodes storage types.
 """
 from __future__ import annotations
 
+import copy
 import math
 
 import numpy as np
@@ -55,6 +56,31 @@ def _gather(w, s):
 
 
 def brute_decode(w, partition_size: int = 512):
+    """Several query tokens per sequence (w.query_start): query token i of a
+    sequence with q_len tokens sees the keys up to position seq_len - q_len + i."""
+    qs = getattr(w, "query_start", None)
+    if qs is None:
+        return _brute_single(w, partition_size)
+    rows = int(qs[-1])
+    res = None
+    for s in range(w.num_seqs):
+        qn = int(qs[s + 1] - qs[s])
+        for qi in range(qn):
+            one = copy.copy(w)
+            one.num_seqs = 1
+            one.query_start = None
+            one.seq_lens = np.array([int(w.seq_lens[s]) - qn + 1 + qi], dtype=np.int32)
+            one.block_tables = w.block_tables[s:s + 1]
+            one.query = w.query[int(qs[s]) + qi:int(qs[s]) + qi + 1]
+            r = _brute_single(one, partition_size)
+            if res is None:
+                res = {k: [None] * rows for k in r}
+            for k in r:
+                res[k][int(qs[s]) + qi] = r[k][0]
+    return res
+
+
+def _brute_single(w, partition_size: int = 512):
     """Returns dict(out, max_logits, exp_sums, tmp_out) as nested Python lists.
 
     out[s][h][d] is the Phase 2 reduce of the partitions; max_logits/exp_sums

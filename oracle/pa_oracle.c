@@ -35,6 +35,13 @@
  *    fp8 cache ("fp8_e4m3" / "fp8_e5m2") holds the keys / values divided by
  *    their scale, so K = k_scale * decode(K8), V = v_scale * decode(V8); the
  *    query and the output keep the query's type.
+ *  - Several query tokens per sequence (speculative / multi-token decode, the
+ *    qo_len of "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs
+ *    Schedule #967"): reading: a sequence with q_len query tokens holds their
+ *    keys as its last q_len cache entries; query token i sits at position
+ *    seq_len - q_len + i and attends the keys up to its own position (causal).
+ *    Its result is the single-token decode of the sequence cut after that
+ *    position.
  *  - "ex_engine/factors/attn_dispatch.py", AttnDispatchConfig window_left /
  *    window_right (-1 = no window), passed to the decode call: the single
  *    query token sits at position seq_len - 1 and attends the keys
@@ -161,18 +168,26 @@ typedef struct {
     double* vrow;    /* one value row, length head_size */
 } scratch_t;
 
-static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
+static int query_count(const oracle_args* a, int s) {
+    return a->query_start ? a->query_start[s + 1] - a->query_start[s] : 1;
+}
+
+/* Query token qi of sequence s, head h. */
+static void compute_head(const oracle_args* a, int s, int qi, int h, scratch_t* sc) {
     const int d_sz = a->head_size;
     const int group = a->num_heads / a->num_kv_heads;
     const int kvh = h / group;
-    const int len = a->seq_lens[s];
+    const int qn = query_count(a, s);
+    /* keys visible to this query token: positions 0 .. seq_len - qn + qi */
+    const int len = a->seq_lens[s] - qn + 1 + qi;
+    const int64_t row = (a->query_start ? a->query_start[s] : s) + qi;
     const int P_max = a->max_num_partitions;
     const int PS = a->partition_size;
     const int32_t* table = a->block_tables + (int64_t)s * a->max_blocks_per_seq;
-    const int64_t qoff = ((int64_t)s * a->num_heads + h) * d_sz;
+    const int64_t qoff = (row * a->num_heads + h) * d_sz;
     double* out = a->out + qoff;
     double* out_v2 = a->out_v2 ? a->out_v2 + qoff : NULL;
-    const int64_t stat_off = ((int64_t)s * a->num_heads + h) * P_max;
+    const int64_t stat_off = (row * a->num_heads + h) * P_max;
     const int num_parts = (len + PS - 1) / PS;
     /* first key inside the sliding window (0 without a window) */
     int t_lo = 0;
@@ -266,6 +281,8 @@ static void compute_head(const oracle_args* a, int s, int h, scratch_t* sc) {
 
 typedef struct {
     const oracle_args* a;
+    const int32_t* pair_seq;  /* per (sequence, query token) pair: sequence */
+    const int32_t* pair_q;    /* ... and query token within the sequence */
     int64_t n_items;
     int64_t next;
     pthread_mutex_t lock;
@@ -291,10 +308,9 @@ static void* worker(void* arg) {
         int64_t i = pool->next++;
         pthread_mutex_unlock(&pool->lock);
         if (i >= pool->n_items) break;
-        int si = (int)(i / a->num_heads);
+        int64_t pi = i / a->num_heads;
         int h = (int)(i % a->num_heads);
-        int s = a->seq_subset ? a->seq_subset[si] : si;
-        compute_head(a, s, h, &sc);
+        compute_head(a, pool->pair_seq[pi], pool->pair_q[pi], h, &sc);
     }
     free(sc.z);
     free(sc.vrow);
@@ -323,6 +339,9 @@ int oracle_decode(const oracle_args* a) {
         if (s < 0 || s >= a->num_seqs) return ORACLE_ERR_ARG;
         int len = a->seq_lens[s];
         if (len < 0) return ORACLE_ERR_ARG;
+        if (query_count(a, s) < 0 || (len > 0 && query_count(a, s) > len) ||
+            (len == 0 && query_count(a, s) > 1))
+            return ORACLE_ERR_ARG;
         if ((len + a->block_size - 1) / a->block_size > a->max_blocks_per_seq) return ORACLE_ERR_ARG;
         if ((len + a->partition_size - 1) / a->partition_size > a->max_num_partitions &&
             (a->max_logits || a->exp_sums || a->tmp_out))
@@ -333,9 +352,30 @@ int oracle_decode(const oracle_args* a) {
             if (table[b] < 0 || table[b] >= a->num_blocks) return ORACLE_ERR_ARG;
         if (len > max_len) max_len = len;
     }
+    /* (sequence, query token) pairs of the selected sequences */
+    int64_t n_pairs = 0;
+    for (int i = 0; i < n_seq; ++i) n_pairs += query_count(a, a->seq_subset ? a->seq_subset[i] : i);
+    int32_t* pair_seq = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_pairs > 0 ? n_pairs : 1));
+    int32_t* pair_q = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_pairs > 0 ? n_pairs : 1));
+    if (!pair_seq || !pair_q) {
+        free(pair_seq);
+        free(pair_q);
+        return ORACLE_ERR_NOMEM;
+    }
+    n_pairs = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        int s = a->seq_subset ? a->seq_subset[i] : i;
+        for (int qi = 0; qi < query_count(a, s); ++qi) {
+            pair_seq[n_pairs] = s;
+            pair_q[n_pairs] = qi;
+            ++n_pairs;
+        }
+    }
     pool_t pool;
     pool.a = a;
-    pool.n_items = (int64_t)n_seq * a->num_heads;
+    pool.pair_seq = pair_seq;
+    pool.pair_q = pair_q;
+    pool.n_items = n_pairs * a->num_heads;
     pool.next = 0;
     pool.max_len = max_len;
     pool.failed = 0;
@@ -351,6 +391,8 @@ int oracle_decode(const oracle_args* a) {
     if (started == 0) worker(&pool);
     for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
     pthread_mutex_destroy(&pool.lock);
+    free(pair_seq);
+    free(pair_q);
     return pool.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 

@@ -482,12 +482,46 @@ def pin_fp8_cache(run):
     _close(r["exp_sums"], r32["exp_sums"], rtol=1e-12, what="fp8 vs decoded fp32 exp_sums")
 
 
+def pin_multi_token(run):
+    """Several query tokens per sequence: matches the brute force; query token i
+    equals the single-token decode of the sequence cut after its position (bit
+    for bit); one token per sequence through query_start equals the default."""
+    from oracle.brute import brute_decode
+    spec = _spec(name="mq", num_seqs=4, num_heads=4, num_kv_heads=2, head_size=8, dtype="f16",
+                 seq_lens=(3, 514, 1024, 1100), alibi=True, q_len=3)
+    w = W.make_workload(spec, "split")
+    for wl in (-1, 600):
+        ww = _clone(w, window_left=wl)
+        r = run(ww)
+        b = brute_decode(ww)
+        _close(r["out"], b["out"], what=f"multi-token brute (window {wl})")
+        _close(r["max_logits"], b["max_logits"], what="multi-token max_logits")
+        _close(r["exp_sums"], b["exp_sums"], what="multi-token exp_sums")
+        qs = ww.query_start
+        for s in range(ww.num_seqs):
+            qn = int(qs[s + 1] - qs[s])
+            for qi in range(qn):
+                row = int(qs[s]) + qi
+                one = _clone(ww, num_seqs=1, query_start=None, block_tables=ww.block_tables[s:s + 1],
+                             seq_lens=np.array([int(ww.seq_lens[s]) - qn + 1 + qi], dtype=np.int32),
+                             query=ww.query[row:row + 1])
+                r1 = run(one, max_num_partitions=r["max_logits"].shape[2])
+                for key in ("out", "max_logits", "exp_sums"):
+                    assert np.array_equal(r[key][row], r1[key][0], equal_nan=True), (s, qi, key)
+    w1 = W.make_workload(_spec(name="mq1", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=8,
+                               dtype="bf16", seq_lens=(5, 600, 1030), q_len=1), "nhd")
+    a = run(w1)
+    b = run(_clone(w1, query_start=None))
+    for key in ("out", "max_logits", "exp_sums"):
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
 ALL_PINS = [
     pin_brute, pin_sdpa, pin_partitioned_equals_dense, pin_seq_len_one,
     pin_identical_v_rows, pin_pool_permutation, pin_split_equals_nhd, pin_zero_query,
     pin_exp_sum_bounds, pin_softcap, pin_two_token_softmax, pin_alibi_closed_form,
     pin_gqa_mapping, pin_poison_never_read, pin_partitions_at_100k, pin_sliding_window,
-    pin_fp8_cache,
+    pin_fp8_cache, pin_multi_token,
 ]
 
 

@@ -46,8 +46,8 @@ MUTATIONS = [
     ("exp_sum_global_max", "double w = exp(sc->z[t] - m);", "double w = exp(sc->z[t] - M);", 0),
     ("partition_drops_last_token", "t1 = t0 + PS < len ? t0 + PS : len;",
      "t1 = t0 + PS - 1 < len ? t0 + PS - 1 : len;", 0),
-    ("query_rows_transposed", "const int64_t qoff = ((int64_t)s * a->num_heads + h) * d_sz;",
-     "const int64_t qoff = ((int64_t)h * a->num_seqs + s) * d_sz;", 0),
+    ("query_rows_transposed", "const int64_t qoff = (row * a->num_heads + h) * d_sz;",
+     "const int64_t qoff = ((int64_t)h * a->num_query_tokens + row) * d_sz;", 0),
     ("slot_off_by_one", "        int o = t % a->block_size;\n        double dot",
      "        int o = (t + 1) % a->block_size;\n        double dot", 0),
     ("reduce_weight_without_exp_sum", "double r = exp(m - M) * e;", "double r = exp(m - M);", 0),
@@ -59,6 +59,9 @@ MUTATIONS = [
     ("e4m3_bias", "else v = ldexp((double)(8 + f), e - 10);", "else v = ldexp((double)(8 + f), e - 11);", 0),
     ("e5m2_subnormal", "v = ldexp((double)f, -16);", "v = ldexp((double)f, -15);", 0),
     ("fp8_split_packing", "int x = 16 / elem_bytes(cache_dtype(a));", "int x = 16 / elem_bytes(a->dtype);", 0),
+    ("causal_ignored", "const int len = a->seq_lens[s] - qn + 1 + qi;", "const int len = a->seq_lens[s];", 0),
+    ("query_tokens_reversed", "const int len = a->seq_lens[s] - qn + 1 + qi;",
+     "const int len = a->seq_lens[s] - qi;", 0),
     ("unused_partition_sum_one", "if (a->exp_sums) a->exp_sums[stat_off + p] = 0.0;",
      "if (a->exp_sums) a->exp_sums[stat_off + p] = 1.0;", 0),
 ]

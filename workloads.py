@@ -73,6 +73,7 @@ class Spec:
     kv_dtype: Optional[str] = None        # "e4m3" / "e5m2": fp8 cache holding K / k_scale, V / v_scale
     k_scale: float = 1.0
     v_scale: float = 1.0
+    q_len: object = None                  # query tokens per sequence (int or list); None = 1
 
 
 SPECS = {
@@ -127,6 +128,17 @@ class Workload:
     kv_dtype: Optional[str] = None  # fp8 cache type, None = same as dtype
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # several query tokens per sequence: query rows of sequence s are
+    # query_start[s] .. query_start[s+1]-1; None = one row per sequence
+    query_start: Optional[np.ndarray] = None
+
+    @property
+    def num_query_tokens(self) -> int:
+        return self.num_seqs if self.query_start is None else int(self.query_start[-1])
+
+    @property
+    def max_query_len(self) -> int:
+        return 1 if self.query_start is None else int(np.diff(self.query_start).max(initial=0))
 
     @property
     def cache_dtype(self) -> str:
@@ -322,7 +334,14 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
     jobs = [(c0, which) for c0 in range(0, pool, _CHUNK_BLOCKS) for which in ("k", "v")]
     with ThreadPoolExecutor(max_workers=_gen_threads()) as ex:
         list(ex.map(fill, jobs))
-    q = _rng(seed, "query").standard_normal((spec.num_seqs, spec.num_heads, d), dtype=np.float32)
+    query_start = None
+    rows = spec.num_seqs
+    if spec.q_len is not None:
+        ql = np.broadcast_to(np.asarray(spec.q_len, dtype=np.int64), (spec.num_seqs,))
+        ql = np.minimum(ql, lens.astype(np.int64))  # a sequence cannot have more queries than keys
+        query_start = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        rows = int(query_start[-1])
+    q = _rng(seed, "query").standard_normal((rows, spec.num_heads, d), dtype=np.float32)
     if spec.value_mult != 1.0:
         q *= np.float32(spec.value_mult)
     query = round_to_storage(q, spec.dtype)
@@ -336,18 +355,18 @@ def make_workload(spec, layout: str = "split", seed: Optional[int] = None,
         alibi_slopes=alibi_slopes(spec.num_heads) if spec.alibi else None,
         meta={"seed": seed, "shuffle_seed": shuffle_seed, "spec": spec},
         kv_dtype=spec.kv_dtype, k_scale=float(np.float32(spec.k_scale)),
-        v_scale=float(np.float32(spec.v_scale)),
+        v_scale=float(np.float32(spec.v_scale)), query_start=query_start,
     )
 
 
 def small_spec(name="small", num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64,
                dtype="f16", seq_lens=(1, 513, 1100), alibi=False, softcap=0.0,
                value_mult=1.0, pool_extra=5, seed_index=7, block_size=BLOCK_SIZE,
-               kv_dtype=None, k_scale=1.0, v_scale=1.0) -> Spec:
+               kv_dtype=None, k_scale=1.0, v_scale=1.0, q_len=None) -> Spec:
     """A Spec for tests: explicit lengths, a pool with NaN-poisoned spare blocks."""
     lens = list(seq_lens)
     used = sum(-(-l // block_size) for l in lens)
     return Spec(name, num_seqs, num_heads, num_kv_heads, head_size, dtype,
                 seq_lens=lens, pool_blocks=used + pool_extra, alibi=alibi, softcap=softcap,
                 value_mult=value_mult, seed_index=seed_index, block_size=block_size,
-                kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
+                kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale, q_len=q_len)
