@@ -103,9 +103,10 @@ typedef enum pa_mode { PA_MODE_AUTO = 0, PA_MODE_V1 = 1, PA_MODE_V2 = 2 } pa_mod
 #define PA_DEVERR_QUERY_RANGE 8 /* fp8 caches with a bf16 query: |q| > 65504 clamped (fp16 MMAs)  */
 
 typedef struct pa_decode_args {
-    /* [num_seqs][num_heads][head_size], dtype; written.  16-byte aligned. */
+    /* [rows][num_heads][head_size], dtype; written.  16-byte aligned.
+     * rows = num_seqs, or num_query_tokens with query_start (below). */
     void* out;
-    /* [num_seqs][num_heads][head_size], dtype.  16-byte aligned. */
+    /* [rows][num_heads][head_size], dtype.  16-byte aligned. */
     const void* query;
     /* layout-dependent, see pa_layout; 16-byte aligned. */
     const void* key_cache;
@@ -131,8 +132,8 @@ typedef struct pa_decode_args {
     int32_t layout;              /* pa_layout */
     int32_t mode;                /* pa_mode */
     /* Workspace (required for v2, ignored by v1); P = pa_max_num_partitions(max_seq_len):
-     *   exp_sums, max_logits [num_seqs][num_heads][P] fp32,
-     *   tmp_out [num_seqs][num_heads][P][head_size] fp32 (16-byte aligned).
+     *   exp_sums, max_logits [rows][num_heads][P] fp32,
+     *   tmp_out [rows][num_heads][P][head_size] fp32 (16-byte aligned).
      * After a v2 call they hold the Phase 1 statistics of every partition
      * p < ceil(seq_lens[s]/512); for p beyond that max_logits = -inf and
      * exp_sums = 0, tmp_out is left unspecified. */
@@ -171,6 +172,23 @@ typedef struct pa_decode_args {
      * fp8(V); values <= 0 mean 1.0 (so a zero-initialised struct has none). */
     float k_scale;
     float v_scale;
+    /* Several query tokens per sequence (speculative / multi-token decode, the
+     * qo_len of "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs
+     * Schedule #967").  NULL = one query token per sequence, rows of query /
+     * out / workspace indexed by sequence (the fields below are ignored).
+     * Otherwise [num_seqs + 1] int32 offsets, query_start[0] = 0,
+     * nondecreasing, query_start[num_seqs] = num_query_tokens: sequence s owns
+     * the rows [query_start[s], query_start[s+1]) of query and out (and of the
+     * workspace's first dimension).  Its qn = query_start[s+1] - query_start[s]
+     * tokens are the last qn cache entries: token i sits at position
+     * seq_lens[s] - qn + i and attends the keys t <= that position (causal),
+     * within its own sliding window, so its result is the single-token decode
+     * of the sequence cut after that position; a token at a negative position
+     * sees no key and gets a zero row.  qn > max_query_len is reported as
+     * PA_DEVERR_SEQ_LEN and clamped. */
+    const int32_t* query_start;
+    int32_t num_query_tokens;  /* rows of query / out / workspace */
+    int32_t max_query_len;     /* >= every qn, >= 1; max_query_len * group <= 16 */
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the
@@ -202,7 +220,8 @@ pa_status pa_decode(const pa_decode_args* args, void* stream);
  * PA_STATIC_WORKSPACE_FLOATS floats instead, which every GPU that loads the
  * library keeps until the process exits.  Allocates nothing.
  *  - Returns PA_ERR_WORKSPACE, before launching anything, when
- *    num_seqs * num_heads * P * (head_size + 2) > PA_STATIC_WORKSPACE_FLOATS,
+ *    rows * num_heads * P * (head_size + 2) > PA_STATIC_WORKSPACE_FLOATS
+ *    (rows = num_seqs, or num_query_tokens with query_start),
  *    P = pa_max_num_partitions(max_seq_len); other errors as pa_decode.
  *  - The first call on a device looks up the array's address on that device
  *    (the device must be current); make that first call before any stream

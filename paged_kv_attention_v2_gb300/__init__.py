@@ -56,19 +56,22 @@ def _dtype_code(t):
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device,
-                    num_kv_heads: int | None = None):
+                    num_kv_heads: int | None = None, num_query_tokens: int | None = None):
     """torch-allocated v2 workspace: dict(exp_sums, max_logits, tmp_out), plus
-    zeroed partition_counters when num_kv_heads is given (fused merge)."""
+    zeroed partition_counters when num_kv_heads is given (fused merge).  With
+    several query tokens per sequence the statistics have one row per query
+    token (num_query_tokens rows)."""
     import torch
     P = max_num_partitions(max_seq_len)
+    rows = num_seqs if num_query_tokens is None else num_query_tokens
     extra = {}
     if num_kv_heads is not None:
         extra["partition_counters"] = torch.zeros((num_seqs, num_kv_heads), dtype=torch.int32,
                                                   device=device)
     return {**extra,
-        "exp_sums": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
-        "max_logits": torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device),
-        "tmp_out": torch.empty((num_seqs, num_heads, P, head_size), dtype=torch.float32,
+        "exp_sums": torch.empty((rows, num_heads, P), dtype=torch.float32, device=device),
+        "max_logits": torch.empty((rows, num_heads, P), dtype=torch.float32, device=device),
+        "tmp_out": torch.empty((rows, num_heads, P, head_size), dtype=torch.float32,
                                device=device),
     }
 
@@ -83,7 +86,8 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               exp_sums=None, max_logits=None, tmp_out=None, dev_error=None,
               event_begin=None, event_end=None, partition_counters=None,
               window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
-              v_scale: float = 1.0) -> _abi.PaDecodeArgs:
+              v_scale: float = 1.0, query_start=None,
+              max_query_len: int | None = None) -> _abi.PaDecodeArgs:
     """Build the C argument struct.  The library validates sizes and types it can
     see; this also checks what only the tensors know: the caches' element size
     and element count against kv_dtype, head_size and num_kv_heads.
@@ -91,8 +95,22 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
     window_left follows AttnDispatchConfig (-1 = no window; the query sees the
     keys t >= seq_len - 1 - window_left) and becomes sliding_window = window_left + 1.
     kv_dtype "e4m3" / "e5m2" marks fp8 caches (raw uint8 tensors) holding K / k_scale
-    and V / v_scale; the query dtype sets the compute and output type."""
-    num_seqs, num_heads, head_size = query.shape
+    and V / v_scale; the query dtype sets the compute and output type.
+    query_start ([num_seqs + 1] int32 offsets) gives several query tokens per
+    sequence: query / out rows are query tokens, and max_query_len (>= every
+    sequence's token count) is required with it."""
+    num_rows, num_heads, head_size = query.shape
+    num_seqs = seq_lens.shape[0]
+    if tuple(out.shape) != tuple(query.shape):
+        raise ValueError(f"out shape {tuple(out.shape)} != query shape {tuple(query.shape)}")
+    if query_start is None:
+        if num_rows != num_seqs:
+            raise ValueError(f"query has {num_rows} rows for {num_seqs} sequences")
+    else:
+        if max_query_len is None:
+            raise ValueError("max_query_len is required with query_start")
+        if query_start.dtype.itemsize != 4 or query_start.numel() != num_seqs + 1:
+            raise ValueError("query_start must be int32 [num_seqs + 1]")
     num_blocks = key_cache.shape[0]
     kv_bytes = 1 if kv_dtype in ("e4m3", "e5m2") else query.element_size()
     page = num_kv_heads * block_size * head_size  # elements of one block of one cache
@@ -117,6 +135,8 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         partition_counters=_ptr(partition_counters),
         sliding_window=int(window_left) + 1 if window_left >= 0 else 0,
         kv_dtype=_KV[kv_dtype], k_scale=float(k_scale), v_scale=float(v_scale),
+        query_start=_ptr(query_start), num_query_tokens=num_rows if query_start is not None else 0,
+        max_query_len=int(max_query_len) if query_start is not None else 0,
     )
 
 
@@ -125,10 +145,11 @@ def pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens, *, str
     """Enqueue paged decode attention on `stream` (default: torch's current stream).
 
     Tensors must be contiguous CUDA tensors: query/out [num_seqs, num_heads,
-    head_size] (fp32, fp16 or bf16), key_cache/value_cache in the split or NHD
-    layout, block_tables [num_seqs, max_blocks_per_seq] int32, seq_lens
-    [num_seqs] int32, optional alibi_slopes [num_heads] fp32, v2 workspace from
-    alloc_workspace().  Raises PaDecodeError with the library's status on failure.
+    head_size] (fp32, fp16 or bf16; [num_query_tokens, ...] with query_start),
+    key_cache/value_cache in the split or NHD layout, block_tables [num_seqs,
+    max_blocks_per_seq] int32, seq_lens [num_seqs] int32, optional alibi_slopes
+    [num_heads] fp32, v2 workspace from alloc_workspace().  Raises PaDecodeError
+    with the library's status on failure.
     """
     import torch
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens):

@@ -73,6 +73,9 @@ class PaDecodeArgs(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("query_start", ctypes.c_void_p),
+        ("num_query_tokens", ctypes.c_int32),
+        ("max_query_len", ctypes.c_int32),
     ]
 
 

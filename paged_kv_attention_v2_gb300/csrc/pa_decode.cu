@@ -148,6 +148,13 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
     const int group = a->num_heads / a->num_kv_heads;
     if (group > 16) return PA_ERR_UNSUPPORTED;
+    // several query tokens per sequence: all tokens of a (sequence, kv head)
+    // share one tile, their group rows side by side (at most 16)
+    const bool multi = a->query_start != nullptr;
+    const int max_q = multi ? a->max_query_len : 1;
+    if (multi && (a->max_query_len < 1 || a->num_query_tokens < 0 || !aligned(a->query_start, 4)))
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_q * group > 16) return PA_ERR_UNSUPPORTED;
     if (a->num_seqs == 0) return PA_OK;
     if (!a->out || !a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
         return PA_ERR_INVALID_ARG;
@@ -176,6 +183,8 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     const int64_t units = (int64_t)a->num_seqs * (v1 ? 1 : max_parts);
     const int64_t tiles = units * a->num_kv_heads;
     if (tiles >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
+    // reduce grid: one CTA per (sequence, query token, head)
+    if ((int64_t)a->num_seqs * max_q * a->num_heads >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
 
     Params p;
     std::memset(&p, 0, sizeof p);
@@ -206,6 +215,9 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.v1 = v1 ? 1 : 0;
     p.counters = a->partition_counters;
     p.window_left = a->sliding_window > 0 ? a->sliding_window - 1 : -1;
+    p.query_start = a->query_start;
+    p.max_q_len = max_q;
+    p.num_q_rows = multi ? a->num_query_tokens : a->num_seqs;
     p.fused = 0;  // decided at launch, once the persistent grid size is known
 
     alignas(64) CUtensorMap tmk, tmv;
@@ -226,7 +238,7 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     la.tmv = &tmv;
     la.sm_count = sm;
     la.tiles_upper = tiles;
-    la.group_tiles = group > 8 ? 2 : 1;
+    la.group_tiles = max_q * group > 8 ? 2 : 1;
     la.layout = a->layout;
     la.head_size = a->head_size;
     la.ev_begin = a->event_main_begin;

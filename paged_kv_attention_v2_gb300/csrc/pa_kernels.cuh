@@ -77,12 +77,15 @@ struct Params {
     float v_scale;                       // fp8 caches: applied to the partition outputs
     int v1;
     int32_t* counters;  // [num_seqs][num_kv_heads] finished partitions (fused v2 only)
-    int window_left;    // < 0: no window; else keys t >= len - 1 - window_left
+    int window_left;    // < 0: no window; else keys t >= pos - window_left (pos: the query's position)
+    const int32_t* query_start;  // [num_seqs + 1] query rows per sequence, or NULL (one row each)
+    int max_q_len;               // upper bound of query tokens per sequence (1 without query_start)
+    int num_q_rows;              // rows of query / out / workspace
     int fused;          // v2 with the log-sum-exp merge done by the last CTA of each (seq, kv head)
 };
 
 struct TileDesc {
-    int seq, kvh, part, tok_begin, tok_end, len, flags, pad;
+    int seq, kvh, part, tok_begin, tok_end, len, flags, q0, qn, pad[3];
 };
 constexpr int kTileStop = 1;
 
@@ -94,11 +97,39 @@ __device__ __forceinline__ int clamp_len(const Params& p, int raw) {
     return raw < 0 ? 0 : (raw > p.max_seq_len ? p.max_seq_len : raw);
 }
 
-// First key inside the sliding window of a sequence of len tokens (0 without one).
-__device__ __forceinline__ int window_lo(const Params& p, int len) {
+// First key inside the sliding window of a query at position pos (0 without one).
+__device__ __forceinline__ int window_lo_at(const Params& p, int pos) {
     if (p.window_left < 0) return 0;
-    const int lo = len - 1 - p.window_left;
+    const int lo = pos - p.window_left;
     return lo > 0 ? lo : 0;
+}
+
+// First key any query token of a sequence sees: the window of its first query
+// token, at position len - qn.
+__device__ __forceinline__ int window_lo(const Params& p, int len, int qn = 1) {
+    return window_lo_at(p, len - qn);
+}
+
+// Query rows of sequence s: first row and count, clamped to max_q_len tokens
+// and to the rows that exist.
+__device__ __forceinline__ void query_rows(const Params& p, int s, int& q0, int& qn) {
+    if (!p.query_start) {
+        q0 = s;
+        qn = 1;
+        return;
+    }
+    q0 = __ldg(p.query_start + s);
+    qn = __ldg(p.query_start + s + 1) - q0;
+    if (qn < 0 || qn > p.max_q_len || q0 < 0 || q0 > p.num_q_rows - min(max(qn, 0), p.max_q_len)) {
+        report(p, PA_DEVERR_SEQ_LEN);
+        qn = qn < 0 ? 0 : min(qn, p.max_q_len);
+        if (q0 < 0 || q0 > p.num_q_rows) {
+            q0 = 0;
+            qn = 0;
+        } else if (q0 + qn > p.num_q_rows) {
+            qn = p.num_q_rows - q0;
+        }
+    }
 }
 
 // Pages covering tokens [tb, te): from page tb/16 to page ceil(te/16) - 1.
@@ -108,8 +139,10 @@ __device__ __forceinline__ int tile_pages(int tb, int te) {
 
 // ------------------------------------------------------------------ config
 
-template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV = kKvSame>
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV = kKvSame,
+          bool MQ = false>
 struct Cfg {
+    static constexpr bool kMQ = MQ;  // several query tokens per sequence (query_start given)
     static constexpr bool kF32 = std::is_same<T, float>::value;
     static constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     static constexpr int kElem = sizeof(T);                // query / output element
@@ -178,7 +211,7 @@ __device__ __forceinline__ bool consumer_sync(const Smem& sm, uint32_t& phase, i
 // ------------------------------------------------------------------ producer
 
 struct ProducerTile {
-    int seq, kvh, part, tb, te, len, npages;
+    int seq, kvh, part, tb, te, len, npages, q0, qn;
     bool valid;
 };
 
@@ -193,20 +226,23 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
 
     // Walk of seq_lens in chunks of 32 sequences: lane i holds sequence cb+i.
     int cb = 0, cu = 0;  // first sequence of the chunk, tile units before the chunk
-    int c_len = 0, c_units = 0, c_p0 = 0, c_incl = 0, c_total = 0;
+    int c_len = 0, c_units = 0, c_p0 = 0, c_q0 = 0, c_qn = 0, c_incl = 0, c_total = 0;
     auto load_chunk = [&](int base) {
         const int s = base + lane;
         c_len = 0;
         c_units = 0;
         c_p0 = 0;
+        c_q0 = 0;
+        c_qn = 0;
         if (s < S) {
             const int raw = __ldg(p.seq_lens + s);
             c_len = clamp_len(p, raw);
             if (c_len != raw) report(p, PA_DEVERR_SEQ_LEN);
+            query_rows(p, s, c_q0, c_qn);  // a token at a negative position sees no key
             // v1: one tile per sequence; v2: one per partition that has keys in
             // the window (fused v2 keeps one empty tile for an empty sequence so
             // that its output row is written)
-            c_p0 = window_lo(p, c_len) / kPart;
+            c_p0 = window_lo(p, c_len, c_qn) / kPart;
             c_units = p.v1 ? 1 : (c_len + kPart - 1) / kPart - c_p0;
             if (p.fused && c_units == 0) c_units = 1;
         }
@@ -237,7 +273,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     auto next_tile = [&]() {
         ProducerTile t;
         t.valid = false;
-        t.seq = t.part = t.tb = t.te = t.len = t.npages = 0;
+        t.seq = t.part = t.tb = t.te = t.len = t.npages = t.q0 = t.qn = 0;
         const int u = tile / Hkv;
         t.kvh = tile - u * Hkv;
         tile += gridDim.x;
@@ -253,7 +289,9 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         t.seq = cb + j;
         const int excl = __shfl_sync(0xffffffffu, c_incl - c_units, j);
         t.len = __shfl_sync(0xffffffffu, c_len, j);
-        const int lo = window_lo(p, t.len);
+        t.q0 = __shfl_sync(0xffffffffu, c_q0, j);
+        t.qn = __shfl_sync(0xffffffffu, c_qn, j);
+        const int lo = window_lo(p, t.len, t.qn);
         t.part = __shfl_sync(0xffffffffu, c_p0, j) + rel - excl;
         t.tb = p.v1 ? lo : max(t.part * kPart, lo);
         t.te = p.v1 ? t.len : min(t.len, t.part * kPart + kPart);
@@ -302,11 +340,17 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                 d.tok_begin = cur.tb;
                 d.tok_end = cur.te;
                 d.len = cur.len;
+                d.q0 = cur.q0;
+                d.qn = cur.qn;
                 d.flags = 0;
-                mbar_arrive_expect_tx(sm.td_full + slot * 8, qbytes);
-                bulk_g2s(sm.q + slot * C::kQBytes,
-                         qbase + ((int64_t)cur.seq * p.num_heads + (int64_t)cur.kvh * p.group) * HEAD * C::kElem,
-                         qbytes, sm.td_full + slot * 8);
+                // the group's rows of every query token of the sequence: slot row
+                // i * group + g holds query token i, head kvh * group + g
+                mbar_arrive_expect_tx(sm.td_full + slot * 8, qbytes * (uint32_t)cur.qn);
+                for (int qi = 0; qi < cur.qn; ++qi)
+                    bulk_g2s(sm.q + slot * C::kQBytes + (uint32_t)qi * qbytes,
+                             qbase + ((int64_t)(cur.q0 + qi) * p.num_heads + (int64_t)cur.kvh * p.group) *
+                                         HEAD * C::kElem,
+                             qbytes, sm.td_full + slot * 8);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -385,7 +429,9 @@ template <class C, typename T, int HEAD, int NC>
 __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm, int tid) {
     constexpr int D4 = HEAD / 4;
     const int G = p.group;
-    for (int idx = tid; idx < G * D4; idx += NC * 32) {
+    // row v of the merge buffers: query token v / G, head kvh * G + v % G
+    const int qn = C::kMQ ? d.qn : 1;
+    for (int idx = tid; idx < qn * G * D4; idx += NC * 32) {
         const int h = idx / D4, d4 = idx - h * D4;
         float M = -INFINITY;
 #pragma unroll
@@ -409,8 +455,9 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
         o.y *= inv;
         o.z *= inv;
         o.w *= inv;
-        const int head = d.kvh * G + h;
-        const int64_t sh = (int64_t)d.seq * p.num_heads + head;
+        const int qi = C::kMQ ? h / G : 0;
+        const int head = d.kvh * G + (h - qi * G);
+        const int64_t sh = (int64_t)(d.q0 + qi) * p.num_heads + head;
         if (p.v1) {
             T* dst = static_cast<T*>(p.out) + sh * HEAD + 4 * d4;
             if constexpr (C::kF32) {
@@ -441,15 +488,18 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
 // Fused v2 merge, run by the NC consumer warps of the CTA that finished the
 // last partition of (d.seq, d.kvh): Phase 2 for the group's heads, reading the
 // partition statistics the other CTAs wrote (L2 loads: never a stale L1 line).
-template <typename T, int HEAD, int NC>
+template <typename T, int HEAD, int NC, bool MQ>
 __device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
     constexpr int D4 = HEAD / 4;
     const int G = p.group;
-    const int P = (d.len + kPart - 1) / kPart;
-    const int p0 = window_lo(p, d.len) / kPart;  // partitions before p0: outside the window
-    for (int idx = tid; idx < G * D4; idx += NC * 32) {
+    const int qn = MQ ? d.qn : 1;
+    for (int idx = tid; idx < qn * G * D4; idx += NC * 32) {
         const int h = idx / D4, d4 = idx - h * D4;
-        const int64_t sh = (int64_t)d.seq * p.num_heads + d.kvh * G + h;
+        const int qi = MQ ? h / G : 0;
+        const int hi = d.len - qn + qi;                       // the query token's position
+        const int P = hi >= 0 ? (hi + kPart) / kPart : 0;      // partitions up to it
+        const int p0 = window_lo_at(p, hi) / kPart;            // partitions before p0: outside the window
+        const int64_t sh = (int64_t)(d.q0 + qi) * p.num_heads + d.kvh * G + (h - qi * G);
         const float* ml = p.max_logits + sh * p.max_parts;
         const float* es = p.exp_sums + sh * p.max_parts;
         const float* tmp = p.tmp_out + sh * p.max_parts * HEAD + 4 * d4;
@@ -507,15 +557,18 @@ __device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
 
 // After the merge: statistics to absolute ALiBi positions, padding of the
 // unused partitions, counter back to zero for the next call.
-template <int NC>
+template <int NC, bool MQ>
 __device__ void fused_finish_stats(const Params& p, const TileDesc& d, int tid) {
     const int G = p.group, Pm = p.max_parts;
-    const int P = (d.len + kPart - 1) / kPart;
-    const int p0 = window_lo(p, d.len) / kPart;
-    for (int idx = tid; idx < G * Pm; idx += NC * 32) {
+    const int qn = MQ ? d.qn : 1;
+    for (int idx = tid; idx < qn * G * Pm; idx += NC * 32) {
         const int h = idx / Pm, q = idx - h * Pm;
-        const int head = d.kvh * G + h;
-        const int64_t o = ((int64_t)d.seq * p.num_heads + head) * Pm + q;
+        const int qi = MQ ? h / G : 0;
+        const int hi = d.len - qn + qi;
+        const int P = hi >= 0 ? (hi + kPart) / kPart : 0;
+        const int p0 = window_lo_at(p, hi) / kPart;
+        const int head = d.kvh * G + (h - qi * G);
+        const int64_t o = ((int64_t)(d.q0 + qi) * p.num_heads + head) * Pm + q;
         if (q < P && q >= p0) {
             if (p.alibi) p.max_logits[o] += __ldg(p.alibi + head) * (float)(d.len - 1);
         } else {
@@ -539,7 +592,7 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     if (!p.fused || p.v1) return true;
     if (tid == 0) {
         __threadfence();  // this CTA's partition results before its arrival
-        const int P = (d.len + kPart - 1) / kPart - window_lo(p, d.len) / kPart;
+        const int P = (d.len + kPart - 1) / kPart - window_lo(p, d.len, d.qn) / kPart;
         const int units = P > 0 ? P : 1;
         const int old = atomicAdd(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
         sm.abort[2] = (old == units - 1) ? 1 : 0;
@@ -547,9 +600,9 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     if (!consumer_sync(sm, mphase, lane)) return false;
     if (sm.abort[2]) {
         __threadfence();  // the other CTAs' partition results, seen through their arrivals
-        fused_merge<T, HEAD, NC>(p, d, tid);
+        fused_merge<T, HEAD, NC, C::kMQ>(p, d, tid);
         if (!consumer_sync(sm, mphase, lane)) return false;  // statistics read before rewritten
-        fused_finish_stats<NC>(p, d, tid);
+        fused_finish_stats<NC, C::kMQ>(p, d, tid);
     }
     return true;
 }
@@ -636,8 +689,10 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         }
         const TileDesc d = sm.desc[slot];
         if (d.flags & kTileStop) return;
+        const int qn = C::kMQ ? d.qn : 1;
+        const int GE = qn * G;  // rows of N: query token v / G, head kvh * G + v % G
 
-        // Q as B fragments: B[k = head dim][n = head], heads >= G are zero.
+        // Q as B fragments: B[k = head dim][n = row], rows >= GE are zero.
         uint32_t qb[NT][KT][2];
         const uint32_t qs = sm.q + slot * C::kQBytes;
 #pragma unroll
@@ -646,7 +701,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t b0 = 0, b1 = 0;
-                if (h < G) {
+                if (h < GE) {
                     const uint32_t a = qs + (uint32_t)((h * HEAD + kk * 16 + 2 * cq) * 2);
                     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b0) : "r"(a));
                     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b1) : "r"(a + 16));
@@ -664,8 +719,29 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = nt * 8 + 2 * cq + e;
-                sl[nt][e] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+                sl[nt][e] = (has_alibi && h < GE) ? __ldg(p.alibi + d.kvh * G + h % G) : 0.f;
             }
+        // key range of each of this lane's rows: its query token's position and
+        // window, within the tile (padded rows get the tile's range)
+        int klo[NT][2], khi[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int v = nt * 8 + 2 * cq + e;
+                int lo = d.tok_begin, hi = d.tok_end - 1;
+                if (C::kMQ && v < GE) {
+                    const int pos = d.len - qn + v / G;
+                    hi = min(hi, pos);
+                    lo = max(lo, window_lo_at(p, pos));
+                }
+                klo[nt][e] = lo;
+                khi[nt][e] = hi;
+            }
+        // keys inside every row's range: a page within [lo_all, hi_all] needs no mask
+        // (one query token: the tile's own range)
+        const int hi_all = C::kMQ ? min(d.tok_end - 1, d.len - qn) : d.tok_end - 1;
+        const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;  // ALiBi positions are taken relative to this token
 
         float m[NT][2], l[NT][2];
@@ -694,7 +770,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             const uint32_t vp = kp + C::kPageBytes;
             const int tok0 = page0 + j * kBS;
             const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
-            const int skip = d.tok_begin - tok0;          // slots < skip: before the window
+            const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;  // some key masked
             if (valid < kBS) {
                 zero_v_tail16<LAYOUT, HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
@@ -738,8 +814,13 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tlo + ((e >> 1) << 3) - origin);
                     z[e] = v;
                 }
-                if (r >= valid || r < skip) z[0] = z[1] = -INFINITY;
-                if (r + 8 >= valid || r + 8 < skip) z[2] = z[3] = -INFINITY;
+                if (edge) {
+                    const int t0 = tok0 + r, t1 = t0 + 8;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                }
                 float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
@@ -747,14 +828,19 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
                 }
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                const float al0 = exp2f((m[nt][0] - mn0) * kLog2e);
-                const float al1 = exp2f((m[nt][1] - mn1) * kLog2e);
+                // several query tokens: a row with no key in its range so far keeps
+                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
+                // appears.  One token: every page holds a key of every row.
+                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
+                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
+                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
-                const float p0 = exp2f((z[0] - mn0) * kLog2e);
-                const float p1 = exp2f((z[1] - mn1) * kLog2e);
-                const float p2 = exp2f((z[2] - mn0) * kLog2e);
-                const float p3 = exp2f((z[3] - mn1) * kLog2e);
+                const float p0 = exp2f((z[0] - mr0) * kLog2e);
+                const float p1 = exp2f((z[1] - mr1) * kLog2e);
+                const float p2 = exp2f((z[2] - mr0) * kLog2e);
+                const float p3 = exp2f((z[3] - mr1) * kLog2e);
                 l[nt][0] = l[nt][0] * al0 + (p0 + p2);
                 l[nt][1] = l[nt][1] * al1 + (p1 + p3);
 #pragma unroll
@@ -888,6 +974,8 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
         }
         const TileDesc d = sm.desc[slot];
         if (d.flags & kTileStop) return;
+        const int qn = C::kMQ ? d.qn : 1;
+        const int GE = qn * G;  // rows of N: query token v / G, head kvh * G + v % G
 
         // Q as fp16 B fragments in the permuted head-dim order.
         uint32_t qb[NT][KT][2];
@@ -899,7 +987,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t w0 = 0, w1 = 0;
-                if (h < G) {
+                if (h < GE) {
                     const uint32_t a = qs + (uint32_t)((h * HEAD + kk * 16 + 4 * cq) * 2);
                     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(a));
                     if constexpr (QBF) {
@@ -925,8 +1013,29 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = nt * 8 + 2 * cq + e;
-                sl[nt][e] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+                sl[nt][e] = (has_alibi && h < GE) ? __ldg(p.alibi + d.kvh * G + h % G) : 0.f;
             }
+        // key range of each of this lane's rows: its query token's position and
+        // window, within the tile (padded rows get the tile's range)
+        int klo[NT][2], khi[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int v = nt * 8 + 2 * cq + e;
+                int lo = d.tok_begin, hi = d.tok_end - 1;
+                if (C::kMQ && v < GE) {
+                    const int pos = d.len - qn + v / G;
+                    hi = min(hi, pos);
+                    lo = max(lo, window_lo_at(p, pos));
+                }
+                klo[nt][e] = lo;
+                khi[nt][e] = hi;
+            }
+        // keys inside every row's range: a page within [lo_all, hi_all] needs no mask
+        // (one query token: the tile's own range)
+        const int hi_all = C::kMQ ? min(d.tok_end - 1, d.len - qn) : d.tok_end - 1;
+        const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;
 
         float m[NT][2], l[NT][2];
@@ -955,7 +1064,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             const uint32_t vp = kp + C::kPageBytes;
             const int tok0 = page0 + j * kBS;
             const int valid = min(kBS, d.tok_end - tok0);
-            const int skip = d.tok_begin - tok0;
+            const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;  // some key masked
             if (valid < kBS) {
                 zero_v_tail8<HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
@@ -986,8 +1095,6 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
 
-            const bool in_lo = tlo < valid && tlo >= skip;
-            const bool in_hi = thi < valid && thi >= skip;
             uint32_t pb[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -999,8 +1106,13 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + ((e >> 1) ? thi : tlo) - origin);
                     z[e] = v;
                 }
-                if (!in_lo) z[0] = z[1] = -INFINITY;
-                if (!in_hi) z[2] = z[3] = -INFINITY;
+                if (edge) {
+                    const int t0 = tok0 + tlo, t1 = tok0 + thi;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                }
                 float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
@@ -1008,14 +1120,19 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
                 }
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                const float al0 = exp2f((m[nt][0] - mn0) * kLog2e);
-                const float al1 = exp2f((m[nt][1] - mn1) * kLog2e);
+                // several query tokens: a row with no key in its range so far keeps
+                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
+                // appears.  One token: every page holds a key of every row.
+                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
+                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
+                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
-                const float p0 = exp2f((z[0] - mn0) * kLog2e);
-                const float p1 = exp2f((z[1] - mn1) * kLog2e);
-                const float p2 = exp2f((z[2] - mn0) * kLog2e);
-                const float p3 = exp2f((z[3] - mn1) * kLog2e);
+                const float p0 = exp2f((z[0] - mr0) * kLog2e);
+                const float p1 = exp2f((z[1] - mr1) * kLog2e);
+                const float p2 = exp2f((z[2] - mr0) * kLog2e);
+                const float p3 = exp2f((z[3] - mr1) * kLog2e);
                 l[nt][0] = l[nt][0] * al0 + (p0 + p2);
                 l[nt][1] = l[nt][1] * al1 + (p1 + p3);
 #pragma unroll
@@ -1104,11 +1221,22 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
         if (d.flags & kTileStop) return;
         const float* q = reinterpret_cast<const float*>(
             __cvta_shared_to_generic(sm.q + slot * C::kQBytes));
+        const int qn = C::kMQ ? d.qn : 1;
+        const int GE = qn * G;  // rows: query token h / G, head kvh * G + h % G
         float sl[HPL];
+        int klo[HPL], khi[HPL];  // key range of each row within the tile
 #pragma unroll
         for (int i = 0; i < HPL; ++i) {
             const int h = hs + 2 * i;
-            sl[i] = (has_alibi && h < G) ? __ldg(p.alibi + d.kvh * G + h) : 0.f;
+            sl[i] = (has_alibi && h < GE) ? __ldg(p.alibi + d.kvh * G + h % G) : 0.f;
+            int lo = d.tok_begin, hi = d.tok_end - 1;
+            if (C::kMQ && h < GE) {
+                const int pos = d.len - qn + h / G;
+                hi = min(hi, pos);
+                lo = max(lo, window_lo_at(p, pos));
+            }
+            klo[i] = lo;
+            khi[i] = hi;
         }
         const int origin = d.tok_end - 1;
         float m[HPL], l[HPL], acc[MAXG][DPL];
@@ -1153,7 +1281,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
             for (int i = 0; i < HPL; ++i) {
                 const int h = hs + 2 * i;
                 float dot = 0.f;
-                if (h < G) {
+                if (h < GE) {
 #pragma unroll 8
                     for (int d4 = 0; d4 < HEAD / 4; ++d4) {
                         const float4 qv = *reinterpret_cast<const float4*>(q + h * HEAD + 4 * d4);
@@ -1169,7 +1297,8 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                 float v = dot * p.scale;
                 if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
                 if (has_alibi) v += sl[i] * (float)(tok0 + t - origin);
-                z[i] = (t < valid && t >= skip) ? v : -INFINITY;
+                const int tk = tok0 + t;
+                z[i] = (tk >= klo[i] && tk <= khi[i]) ? v : -INFINITY;
             }
 #pragma unroll
             for (int i = 0; i < HPL; ++i) {
@@ -1178,8 +1307,9 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 const float mn = fmaxf(m[i], mx);
-                const float al = exp2f((m[i] - mn) * kLog2e);
-                const float pv = exp2f((z[i] - mn) * kLog2e);
+                const float mr = (C::kMQ && mn == -INFINITY) ? 0.f : mn;  // no -inf - -inf for an empty row
+                const float al = exp2f((m[i] - mr) * kLog2e);
+                const float pv = exp2f((z[i] - mr) * kLog2e);
                 m[i] = mn;
                 l[i] = l[i] * al + pv;
                 if (h < MAXG) {
@@ -1190,7 +1320,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
             __syncwarp();
 #pragma unroll
             for (int h = 0; h < MAXG; ++h) {
-                if (h < G) {
+                if (h < GE) {
                     const float al = pw[kBS * MAXG + h];
 #pragma unroll
                     for (int c = 0; c < DPL; ++c) acc[h][c] *= al;
@@ -1205,7 +1335,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                 }
 #pragma unroll
                 for (int h = 0; h < MAXG; ++h) {
-                    if (h < G) {
+                    if (h < GE) {
                         const float pr = pw[tt * MAXG + h];
 #pragma unroll
                         for (int c = 0; c < DPL; ++c) acc[h][c] = fmaf(pr, vv[c], acc[h][c]);
@@ -1223,7 +1353,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
         float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
 #pragma unroll
         for (int h = 0; h < MAXG; ++h)
-            if (h < G)
+            if (h < GE)
 #pragma unroll
                 for (int c = 0; c < DPL; ++c) mw[h * C::kMergeStride + lane + 32 * c] = acc[h][c];
         if (t == 0) {
@@ -1251,11 +1381,11 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 
 // ------------------------------------------------------------------ kernels
 
-template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV>
+template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, bool MQ>
 __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
-    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1318,7 +1448,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
 // partition rows in flight; it carries its own running max, so no separate
 // pass over max_logits is needed.  The rows are then combined with the usual
 // max rescale in shared memory.
-template <typename T, int HEAD, int WARPS, int U>
+template <typename T, int HEAD, int WARPS, int U, bool MQ>
 __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     constexpr int D4 = HEAD / 4;          // float4 columns of a partition row
     constexpr int RPW = 32 / D4;          // partition rows per warp (1 or 2)
@@ -1327,31 +1457,41 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     __shared__ float4 part[RSTEP][D4];
     __shared__ float rowm[RSTEP], roww[RSTEP];
 
+    // one CTA per (sequence, query token, head); query tokens beyond the
+    // sequence's count return at once
     const int bid = blockIdx.x;
-    const int s = bid / p.num_heads, h = bid - s * p.num_heads;
+    const int sq = bid / p.num_heads, h = bid - sq * p.num_heads;
+    const int s = MQ ? sq / p.max_q_len : sq, qi = MQ ? sq - s * p.max_q_len : 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_launch_dependents();  // the next launch may start its prologue; it waits for us
     pdl_wait_primary();
 
+    int q0 = s, qn = 1;
+    if constexpr (MQ) {
+        query_rows(p, s, q0, qn);
+        if (qi >= qn) return;
+    }
     const int len = clamp_len(p, p.seq_lens[s]);
-    const int P = (len + kPart - 1) / kPart;
-    const int p0 = window_lo(p, len) / kPart;  // partitions before p0: outside the window
-    const int64_t sb = ((int64_t)s * p.num_heads + h) * p.max_parts;
+    const int hi = len - qn + qi;                      // the query token's position
+    const int P = hi >= 0 ? (hi + kPart) / kPart : 0;  // partitions holding its keys
+    const int p0 = window_lo_at(p, hi) / kPart;        // partitions before p0: outside the window
+    const int64_t row = (int64_t)q0 + qi;
+    const int64_t sb = (row * p.num_heads + h) * p.max_parts;
     float* ml = p.max_logits + sb;
     float* es = p.exp_sums + sb;
     const float* tmp = p.tmp_out + sb * HEAD;
-    T* o = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + h) * HEAD;
+    T* o = static_cast<T*>(p.out) + (row * p.num_heads + h) * HEAD;
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (P > 0) {
-        const int row = warp * RPW + lane / D4, d4 = lane % D4;
+        const int prow = warp * RPW + lane / D4, d4 = lane % D4;
         float M = -INFINITY, W = 0.f;
-        for (int q0 = p0 + row; q0 < P; q0 += RSTEP * U) {
+        for (int qb = p0 + prow; qb < P; qb += RSTEP * U) {
             float mq[U], eq[U];
             float4 t[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int q = q0 + u * RSTEP;
+                const int q = qb + u * RSTEP;
                 if (q < P) {
                     mq[u] = ml[q];
                     eq[u] = es[q];
@@ -1382,10 +1522,10 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
                 W += c;
             }
         }
-        part[row][d4] = a;
+        part[prow][d4] = a;
         if (d4 == 0) {
-            rowm[row] = M;
-            roww[row] = W;
+            rowm[prow] = M;
+            roww[prow] = W;
         }
         __syncthreads();
         if (tid < D4) {

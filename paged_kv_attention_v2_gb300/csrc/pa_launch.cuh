@@ -34,13 +34,13 @@ constexpr int kMaxDevices = 64;
 // (a short merge).  With several rounds the CTA that merges falls behind and
 // becomes the last arriver of the next group too, so merges pile up on a few
 // CTAs; the separate reduce kernel spreads them over the whole GPU instead.
-template <typename T, int HEAD, int NT, int LAYOUT, int KV>
+template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32
                            : (KV == kKvSame ? PA_STAGES_16BIT : PA_STAGES_FP8);
     constexpr int NC = PA_CONSUMER_WARPS;
-    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
-    auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV>;
+    using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
+    auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
 
     static std::atomic<int> occ_cache[kMaxDevices];
     int dev = 0;
@@ -88,10 +88,10 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
 // Reduce shape by partition count: few partitions need one round of rows,
 // long sequences (hundreds of partitions, few (sequence, head) CTAs) want as
 // many independent row loads in flight per CTA as possible.
-template <typename T, int HEAD, int WARPS, int U>
+template <typename T, int HEAD, int WARPS, int U, bool MQ>
 cudaError_t launch_reduce_shape(const Params& p, const LaunchArgs& la) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)p.num_seqs * p.num_heads));
+    cfg.gridDim = dim3((unsigned)((int64_t)p.num_seqs * p.max_q_len * p.num_heads));
     cfg.blockDim = dim3(WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = la.stream;
@@ -100,28 +100,36 @@ cudaError_t launch_reduce_shape(const Params& p, const LaunchArgs& la) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD, WARPS, U>, p);
+    return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<T, HEAD, WARPS, U, MQ>, p);
 }
 
-template <typename T, int HEAD>
+template <typename T, int HEAD, bool MQ>
 cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     // the wide shape only when there are few (sequence, head) rows to spread
     // (e.g. 4 x 28 rows of 196 partitions); many rows fill the GPU anyway and
     // most of a ragged batch's rows are short
-    const int64_t rows = (int64_t)p.num_seqs * p.num_heads;
+    const int64_t rows = (int64_t)p.num_seqs * p.max_q_len * p.num_heads;
     if (p.max_parts > 32 && rows <= 2 * (int64_t)la.sm_count)
-        return launch_reduce_shape<T, HEAD, 16, 8>(p, la);
-    return launch_reduce_shape<T, HEAD, 8, 4>(p, la);
+        return launch_reduce_shape<T, HEAD, 16, 8, MQ>(p, la);
+    return launch_reduce_shape<T, HEAD, 8, 4, MQ>(p, la);
 }
 
+template <typename T, int HEAD, int NT, int KV, bool MQ>
+cudaError_t launch_layout_mq(const Params& p, const LaunchArgs& la, bool* fused) {
+    if constexpr (KV != kKvSame) {  // fp8 caches: split layout only (checked by the host)
+        return launch_main<T, HEAD, NT, kSplit, KV, MQ>(p, la, fused);
+    } else {
+        return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD, KV, MQ>(p, la, fused)
+                                 : launch_main<T, HEAD, NT, kSplit, KV, MQ>(p, la, fused);
+    }
+}
+
+// Single-token decode and several query tokens per sequence are separate
+// instantiations, so the common single-token path carries no per-row ranges.
 template <typename T, int HEAD, int NT, int KV>
 cudaError_t launch_layout(const Params& p, const LaunchArgs& la, bool* fused) {
-    if constexpr (KV != kKvSame) {  // fp8 caches: split layout only (checked by the host)
-        return launch_main<T, HEAD, NT, kSplit, KV>(p, la, fused);
-    } else {
-        return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD, KV>(p, la, fused)
-                                 : launch_main<T, HEAD, NT, kSplit, KV>(p, la, fused);
-    }
+    return p.query_start ? launch_layout_mq<T, HEAD, NT, KV, true>(p, la, fused)
+                         : launch_layout_mq<T, HEAD, NT, KV, false>(p, la, fused);
 }
 
 // Whole operation for one (query type, cache type) pair.
@@ -130,7 +138,7 @@ cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
     constexpr bool F32 = std::is_same<T, float>::value;
     cudaError_t e;
     bool fused = false;
-    if constexpr (F32) {  // one fp32 consumer handles up to 16 heads
+    if constexpr (F32) {  // one fp32 consumer handles up to 16 rows (query tokens x heads)
         e = la.head_size == 128 ? launch_layout<T, 128, 2, KV>(p, la, &fused)
                                 : launch_layout<T, 64, 2, KV>(p, la, &fused);
     } else if (la.head_size == 128) {
@@ -141,7 +149,9 @@ cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
                                 : launch_layout<T, 64, 1, KV>(p, la, &fused);
     }
     if (e != cudaSuccess || p.v1 || fused) return e;
-    return la.head_size == 128 ? launch_reduce<T, 128>(p, la) : launch_reduce<T, 64>(p, la);
+    if (p.query_start)
+        return la.head_size == 128 ? launch_reduce<T, 128, true>(p, la) : launch_reduce<T, 64, true>(p, la);
+    return la.head_size == 128 ? launch_reduce<T, 128, false>(p, la) : launch_reduce<T, 64, false>(p, la);
 }
 
 cudaError_t launch_f32(const Params& p, const LaunchArgs& la);

@@ -56,8 +56,10 @@ extern "C" pa_status pa_decode_static_workspace(const pa_decode_args* args, void
     if (!args) return PA_ERR_INVALID_ARG;
     if (args->num_seqs < 0 || args->num_heads <= 0 || args->head_size <= 0 || args->max_seq_len < 0)
         return PA_ERR_INVALID_ARG;
-    const int64_t stats = (int64_t)args->num_seqs * args->num_heads *
-                          pa_max_num_partitions(args->max_seq_len);
+    // workspace rows: one per query token (one per sequence without query_start)
+    const int64_t rows = args->query_start ? args->num_query_tokens : args->num_seqs;
+    if (rows < 0) return PA_ERR_INVALID_ARG;
+    const int64_t stats = rows * args->num_heads * pa_max_num_partitions(args->max_seq_len);
     // tmp_out first (16-byte alignment for its float4 accesses), then the two statistics arrays
     const int64_t tmp = stats * args->head_size;
     if (tmp + 2 * stats > (int64_t)PA_STATIC_WORKSPACE_FLOATS) return PA_ERR_WORKSPACE;

@@ -40,6 +40,8 @@ def to_device(w, device="cuda:0"):
         "block_tables": torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(device),
         "seq_lens": torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(device),
         "alibi_slopes": None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(device),
+        "query_start": (None if getattr(w, "query_start", None) is None
+                        else torch.from_numpy(np.ascontiguousarray(w.query_start)).to(device)),
     }
     return d
 
@@ -59,8 +61,11 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
             counters = torch.zeros((w.num_seqs, w.num_kv_heads), dtype=torch.int32, device=device)
     msl = w.max_seq_len if max_seq_len is None else max_seq_len
     S, H, d = w.num_seqs, w.num_heads, w.head_size
-    out = torch.full((S, H, d), float("nan"), dtype=torch_dtype(w.dtype), device=device)
-    ws = pa.alloc_workspace(S, H, d, msl, device)
+    multi = dev["query_start"] is not None
+    R = w.num_query_tokens if multi else S  # rows of query / out / workspace
+    out = torch.full((R, H, d), float("nan"), dtype=torch_dtype(w.dtype), device=device)
+    ws = pa.alloc_workspace(S, H, d, msl, device, num_query_tokens=R if multi else None)
+    mq = {"query_start": dev["query_start"], "max_query_len": w.max_query_len} if multi else {}
     if poison_workspace:
         for t in ws.values():
             t.fill_(float("nan"))
@@ -74,7 +79,7 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                      mode=mode, dev_error=err, partition_counters=counters,
                      window_left=getattr(w, "window_left", -1),
                      kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
-                     v_scale=getattr(w, "v_scale", 1.0), **ws)
+                     v_scale=getattr(w, "v_scale", 1.0), **mq, **ws)
     torch.cuda.synchronize(device)
     if counters is not None:
         assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"
@@ -107,12 +112,23 @@ def check_out(w, gpu_out, ref_out, seqs=None, what="out"):
                              f"ref {r[idx]!r}; worst excess {err:.3e}")
 
 
+def stat_rows(w, s):
+    """(row, keys visible) for each query token of sequence s: the single token
+    sees the whole sequence; with query_start token i of qn sees seq_len - qn + 1 + i."""
+    L = int(min(max(int(w.seq_lens[s]), 0), w.max_seq_len))
+    qs = getattr(w, "query_start", None)
+    if qs is None:
+        return [(s, L)]
+    q0, qn = int(qs[s]), int(qs[s + 1] - qs[s])
+    return [(q0 + i, max(L - qn + 1 + i, 0)) for i in range(qn)]
+
+
 def check_stats(w, gpu, ref, seqs=None):
     """max_logits / exp_sums / tmp_out of every used partition; padding exactly -inf / 0."""
     atol, rtol = OUT_TOL[w.dtype]
     seqs = range(w.num_seqs) if seqs is None else seqs
-    for s in seqs:
-        P = -(-int(min(max(int(w.seq_lens[s]), 0), w.max_seq_len)) // 512)
+    for s, L in ((r, L) for q in seqs for r, L in stat_rows(w, q)):
+        P = -(-L // 512)
         # partitions the oracle marks unused (before a sliding window): exactly -inf / 0
         unused = np.isneginf(ref["max_logits"][s, :, :P])
         assert np.all(np.isneginf(gpu["max_logits"][s, :, :P][unused])), f"{w.name} seq {s}"

@@ -122,6 +122,13 @@ def _args(**over):
     ({"kv_dtype": _abi.PA_KV_FP8_E5M2, "dtype": _abi.PA_DTYPE_F32}, _abi.PA_ERR_UNSUPPORTED),
     ({"kv_dtype": 9}, _abi.PA_ERR_INVALID_ARG),
     ({"k_scale": float("inf")}, _abi.PA_ERR_INVALID_ARG),
+    ({"query_start": 16, "num_query_tokens": 4, "max_query_len": 0}, _abi.PA_ERR_INVALID_ARG),
+    ({"query_start": 18, "num_query_tokens": 4, "max_query_len": 2}, _abi.PA_ERR_INVALID_ARG),
+    ({"query_start": 16, "num_query_tokens": -1, "max_query_len": 2}, _abi.PA_ERR_INVALID_ARG),
+    # 3 query tokens x group 4 > 16 rows of one tile (group 8 x 2 = 16 fits)
+    ({"query_start": 16, "num_query_tokens": 6, "max_query_len": 5}, _abi.PA_ERR_UNSUPPORTED),
+    ({"query_start": 16, "num_query_tokens": 6, "max_query_len": 3, "num_heads": 16},
+     _abi.PA_ERR_UNSUPPORTED),
     ({"num_seqs": 0}, _abi.PA_OK),                         # empty batch: no-op
 ])
 def test_host_argument_checks(lib, over, expect):
@@ -156,3 +163,25 @@ def test_binding_rejects_cache_tensors_that_do_not_match_the_declared_type():
         pa.make_args(q, q, k16[:5].clone(), k16, bt, sl, **kw)
     pa.make_args(q, q, k8, k8, bt, sl, kv_dtype="e4m3", **kw)
     pa.make_args(q, q, k16, k16, bt, sl, **kw)
+
+
+def test_binding_multi_token_rows():
+    """With query_start the query / out rows are query tokens (any count), the
+    sequence count comes from seq_lens, and max_query_len is required."""
+    import torch
+    k16 = torch.zeros((10, 2, 16, 16, 8), dtype=torch.float16)
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    sl = torch.zeros(2, dtype=torch.int32)
+    q5 = torch.zeros((5, 8, 128), dtype=torch.float16)
+    qs = torch.tensor([0, 2, 5], dtype=torch.int32)
+    kw = dict(num_kv_heads=2, scale=0.1, max_seq_len=64)
+    with pytest.raises(ValueError):
+        pa.make_args(q5, q5, k16, k16, bt, sl, **kw)                 # 5 rows, 2 sequences
+    with pytest.raises(ValueError):
+        pa.make_args(q5, q5, k16, k16, bt, sl, query_start=qs, **kw)  # no max_query_len
+    with pytest.raises(ValueError):
+        pa.make_args(q5, q5, k16, k16, bt, sl, query_start=qs[:2], max_query_len=3, **kw)
+    a = pa.make_args(q5, q5, k16, k16, bt, sl, query_start=qs, max_query_len=3, **kw)
+    assert (a.num_seqs, a.num_query_tokens, a.max_query_len) == (2, 5, 3)
+    b = pa.make_args(q5[:2], q5[:2], k16, k16, bt, sl, **kw)
+    assert (b.num_seqs, b.query_start, b.num_query_tokens) == (2, None, 0)

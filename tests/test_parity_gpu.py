@@ -6,7 +6,9 @@ at full size on sampled sequences the oracle computes one by one), both cache
 layouts, v1 / v2 / auto, and the edge cases: empty and one-token sequences,
 page and partition boundaries, GQA groups from 1 to 16 (two n-tiles),
 head size 64, fp32 / fp16 / bf16, ALiBi, softcap, out-of-range block ids and
-sequence lengths (device error bits, no fault), NaN in unused cache slots.
+sequence lengths (device error bits, no fault), NaN in unused cache slots;
+sliding windows, fp8 (E4M3 / E5M2) caches with scales, and several query
+tokens per sequence (1 to 16 tokens, ragged counts, bad offsets flagged).
 """
 from __future__ import annotations
 
@@ -234,3 +236,72 @@ def test_fp8_cache(case, mode):
     check_out(w, g["out"], ref["out"])
     if mode in ("v2", "v2f"):
         check_stats(w, g, ref)
+
+
+MULTI = [
+    # name, query dtype, kv dtype, layout, H, Hkv, d, lens, q_len, alibi, softcap, window_left
+    ("q2_f16_short", "f16", None, "split", 8, 2, 128, (1, 2, 16, 513, 514, 1100), 2,
+     False, 0.0, -1),
+    ("q4_bf16_nhd_alibi", "bf16", None, "nhd", 8, 2, 128, (3, 17, 512, 513, 3000), 4,
+     True, 0.0, -1),
+    ("q_mixed_window", "f16", None, "split", 12, 3, 128, (5, 600, 1025, 2000), [1, 3, 0, 4],
+     False, 0.0, 511),
+    ("q8_group2_head64", "f16", None, "nhd", 4, 2, 64, (9, 1030, 520), 8, False, 30.0, 100),
+    ("q16_mha", "bf16", None, "split", 3, 3, 128, (20, 531), 16, True, 0.0, -1),
+    ("q3_f32_alibi_window", "f32", None, "nhd", 8, 2, 128, (100, 700), 3, True, 0.0, 200),
+    ("q5_f32_head64", "f32", None, "split", 6, 2, 64, (4, 515), 5, False, 0.0, -1),
+    ("q2_e4m3_group8", "bf16", "e4m3", "split", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
+    ("q3_e5m2_window", "f16", "e5m2", "split", 6, 2, 64, (33, 1500), 3, False, 30.0, 100),
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[c[0] for c in MULTI])
+@pytest.mark.parametrize("mode", ["auto", "v1", "v2", "v2f"])
+def test_multi_token(case, mode):
+    """Several query tokens per sequence (each the single-token decode of the
+    sequence cut after its position): outputs and every row's statistics."""
+    name, dtype, kv, layout, H, Hkv, d, lens, ql, alibi, cap, wl = case
+    spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
+                        head_size=d, dtype=dtype, seq_lens=lens, alibi=alibi, softcap=cap,
+                        kv_dtype=kv, k_scale=2 ** -5 if kv else 1.0,
+                        v_scale=2 ** -4 if kv else 1.0, q_len=ql)
+    w = W.make_workload(spec, layout)
+    w.window_left = wl
+    ref = oracle.oracle_decode(w)
+    g = run_gpu(w, mode=mode, calls=2)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], ref["out"])
+    if mode in ("v2", "v2f") or (mode == "auto" and w.max_seq_len > 512):
+        check_stats(w, g, ref)
+
+
+def test_multi_token_full_size():
+    """The 32 x 4096 GQA workload (28 heads over 4 kv heads) with two query
+    tokens per sequence, both cache layouts."""
+    import dataclasses
+    spec = dataclasses.replace(W.SPECS["gqa4k"], name="gqa4k_q2", q_len=2)
+    for layout in ("split", "nhd"):
+        w = W.make_workload(spec, layout)
+        ref = oracle.oracle_decode(w)
+        for mode in ("v1", "v2", "v2f"):
+            g = run_gpu(w, mode=mode)
+            assert g["dev_error"] == 0
+            check_out(w, g["out"], ref["out"], what=f"out[{mode}]")
+            if mode != "v1":
+                check_stats(w, g, ref)
+
+
+def test_multi_token_bad_query_start_is_flagged_not_faulted():
+    """Offsets beyond the query rows or a count above max_query_len: the kernels
+    clamp them to existing rows, set PA_DEVERR_SEQ_LEN and never fault."""
+    spec = W.small_spec(name="badqs", num_seqs=3, num_heads=8, num_kv_heads=2, head_size=128,
+                        dtype="f16", seq_lens=(40, 600, 1200), q_len=2)
+    w = W.make_workload(spec, "split")
+    dev = to_device(w)
+    # sequence 1 claims rows [2, 9): more than max_query_len (2) and past the 6 rows
+    dev["query_start"] = torch.tensor([0, 2, 9, 6], dtype=torch.int32, device="cuda:0")
+    for mode in ("v1", "v2", "v2f"):
+        g = run_gpu(w, mode=mode, dev=dev)
+        assert g["dev_error"] & 2, mode  # PA_DEVERR_SEQ_LEN
+    ref = oracle.oracle_decode(w)
+    check_out(w, g["out"][:2], ref["out"][:2])  # sequence 0 is untouched

@@ -35,10 +35,16 @@ def test_batch_beyond_static_capacity_is_rejected():
     # 256 * 32 * 64 partitions * (128 + 2) floats > PA_STATIC_WORKSPACE_FLOATS: refused, no launch
     assert lib.pa_decode_static_workspace(ctypes.byref(_args()), None) == _abi.PA_ERR_WORKSPACE
     assert lib.pa_decode_static_workspace(None, None) == _abi.PA_ERR_INVALID_ARG
+    # with several query tokens per sequence the workspace has one row per token:
+    # 8 sequences fit, 8 sequences of 64 tokens do not
+    small = dict(num_seqs=8, max_seq_len=4096, max_blocks_per_seq=256)
+    assert lib.pa_decode_static_workspace(
+        ctypes.byref(_args(**small, query_start=256, num_query_tokens=512, max_query_len=64)),
+        None) == _abi.PA_ERR_WORKSPACE
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", ["gqa4k-split", "alibi-bf16-nhd"])
+@pytest.mark.parametrize("case", ["gqa4k-split", "alibi-bf16-nhd", "multi-token-f16"])
 def test_static_workspace_matches_pa_decode_on_two_calls(case):
     import torch
 
@@ -46,17 +52,23 @@ def test_static_workspace_matches_pa_decode_on_two_calls(case):
 
     if case == "gqa4k-split":
         w = W.make_workload("gqa4k", "split")
-    else:
+    elif case == "alibi-bf16-nhd":
         w = W.make_workload(W.small_spec(name="static_ws", num_seqs=5, num_heads=16,
                                          num_kv_heads=4, head_size=128, dtype="bf16",
                                          seq_lens=(1, 511, 513, 3000, 1800), alibi=True,
                                          softcap=30.0, value_mult=2.0), "nhd")
+    else:
+        w = W.make_workload(W.small_spec(name="static_ws_mt", num_seqs=4, num_heads=8,
+                                         num_kv_heads=2, head_size=128, dtype="f16",
+                                         seq_lens=(3, 513, 1030, 2600), q_len=[1, 4, 2, 3]),
+                            "split")
     dev = to_device(w)
     ref = run_gpu(w, mode="v2", dev=dev)
     assert ref["dev_error"] == 0
 
     lib = _abi.load()
-    out = torch.empty((w.num_seqs, w.num_heads, w.head_size), dtype=torch_dtype(w.dtype),
+    multi = dev["query_start"] is not None
+    out = torch.empty((w.num_query_tokens, w.num_heads, w.head_size), dtype=torch_dtype(w.dtype),
                       device="cuda:0")
     err = torch.zeros(1, dtype=torch.int32, device="cuda:0")
     args = _abi.PaDecodeArgs(
@@ -68,7 +80,10 @@ def test_static_workspace_matches_pa_decode_on_two_calls(case):
         max_blocks_per_seq=w.block_tables.shape[1], scale=w.scale, softcap=w.softcap,
         alibi_slopes=None if dev["alibi_slopes"] is None else dev["alibi_slopes"].data_ptr(),
         dtype={"f32": 0, "f16": 1, "bf16": 2}[w.dtype],
-        layout={"split": 0, "nhd": 1}[w.layout], mode=_abi.PA_MODE_AUTO, dev_error=err.data_ptr())
+        layout={"split": 0, "nhd": 1}[w.layout], mode=_abi.PA_MODE_AUTO, dev_error=err.data_ptr(),
+        query_start=dev["query_start"].data_ptr() if multi else None,
+        num_query_tokens=w.num_query_tokens if multi else 0,
+        max_query_len=w.max_query_len if multi else 0)
     stream = torch.cuda.current_stream().cuda_stream
     atol, rtol = OUT_TOL[w.dtype]
     for call in range(2):
