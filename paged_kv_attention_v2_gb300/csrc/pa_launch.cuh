@@ -57,9 +57,18 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     }
     if (PA_MAX_CTAS_PER_SM > 0 && occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
     int64_t grid = (int64_t)la.sm_count * occ;
-    if (la.grid_override > 0) grid = la.grid_override;
     if (grid > la.tiles_upper) grid = la.tiles_upper;
     if (grid < 1) grid = 1;
+    // Equal rounds: the fewest CTAs that keep the number of rounds of the
+    // static tile schedule, so that in a uniform batch every CTA gets the same
+    // number of tiles instead of a last round that leaves most CTAs idle
+    // (1024 tiles: 256 CTAs x 4 instead of 304 CTAs with 112 doing a 4th).
+    // tiles_upper is exact for equal lengths and only an upper bound otherwise.
+    {
+        const int64_t rounds = (la.tiles_upper + grid - 1) / grid;
+        grid = (la.tiles_upper + rounds - 1) / rounds;
+    }
+    if (la.grid_override > 0) grid = la.grid_override < la.tiles_upper ? la.grid_override : la.tiles_upper;
     Params p = p_in;
     p.fused = (!p.v1 && p.counters && p.max_parts <= PA_FUSED_MAX_PARTITIONS &&
                la.tiles_upper <= grid) ? 1 : 0;
