@@ -55,9 +55,14 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #ifndef PA_MIN_CTAS_PER_SM
 #define PA_MIN_CTAS_PER_SM 1   // __launch_bounds__ minimum resident CTAs
 #endif
+#ifndef PA_REDUCE_WARP_MAX_PARTS
+#define PA_REDUCE_WARP_MAX_PARTS 64  // warp-per-row reduce up to this many partitions per row
+#endif
 #ifndef PA_MAX_CTAS_PER_SM
 #define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
 #endif
+
+constexpr int kReduceWarpsPerCta = 8;  // warp-per-row reduce: rows per CTA
 
 struct Params {
     const void* query;
@@ -1574,6 +1579,154 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     for (int q = tid; q < p0 && q < P; q += NT) {
         ml[q] = -INFINITY;
         es[q] = 0.f;
+    }
+}
+
+// Phase 2 with one warp per (sequence, query token, head) row, for batches of
+// many rows with few partitions each (a CTA per row would need several waves
+// of mostly idle CTAs).  Lane i holds the statistics of partitions i, i + 32,
+// ... and HEAD/32 columns of every partition output; the first eight partition
+// outputs are loaded together with the statistics, so a row of up to eight
+// partitions costs one round trip.  No shared memory, no block barrier.
+template <typename T, int HEAD, bool MQ>
+__global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel(const Params p) {
+    constexpr int VEC = HEAD / 32;  // columns per lane: 4 (HEAD 128) or 2 (HEAD 64)
+    constexpr int PRE = 8;          // partition outputs loaded before the weights are known
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait_primary();
+
+    const int64_t rid = (int64_t)blockIdx.x * kReduceWarpsPerCta + warp;
+    const int64_t nrows = (int64_t)p.num_seqs * (MQ ? p.max_q_len : 1) * p.num_heads;
+    if (rid >= nrows) return;
+    const int sq = (int)(rid / p.num_heads), h = (int)(rid - (int64_t)sq * p.num_heads);
+    const int s = MQ ? sq / p.max_q_len : sq, qi = MQ ? sq - s * p.max_q_len : 0;
+    int q0 = s, qn = 1;
+    if constexpr (MQ) {
+        query_rows(p, s, q0, qn);
+        if (qi >= qn) return;
+    }
+    const int len = clamp_len(p, p.seq_lens[s]);
+    const int hi = len - qn + qi;                      // the query token's position
+    const int P = hi >= 0 ? (hi + kPart) / kPart : 0;  // partitions holding its keys
+    const int p0 = window_lo_at(p, hi) / kPart;        // partitions before p0: outside the window
+    const int64_t row = (int64_t)q0 + qi;
+    const int64_t sb = (row * p.num_heads + h) * p.max_parts;
+    float* ml = p.max_logits + sb;
+    float* es = p.exp_sums + sb;
+    const float* tmp = p.tmp_out + sb * HEAD + lane * VEC;
+
+    // partition outputs p0 .. p0 + 7 and this lane's first statistics, all in flight
+    auto load_out = [&](int q, float (&t)[VEC]) {
+        if constexpr (VEC == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD);
+            t[0] = v.x; t[1] = v.y; t[2] = v.z; t[3] = v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(tmp + (int64_t)q * HEAD);
+            t[0] = v.x; t[1] = v.y;
+        }
+    };
+    float pre[PRE][VEC];
+#pragma unroll
+    for (int k = 0; k < PRE; ++k) {
+        if (p0 + k < P) {
+            load_out(p0 + k, pre[k]);
+        } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) pre[k][v] = 0.f;
+        }
+    }
+    const int q1 = p0 + lane;
+    const float m1 = q1 < P ? ml[q1] : -INFINITY;
+    const float e1 = q1 < P ? es[q1] : 0.f;
+
+    // global max and weight sum over the row's partitions (lanes, then the warp)
+    float M = m1, W = m1 == -INFINITY ? 0.f : e1;
+    for (int q = q1 + 32; q < P; q += 32) {
+        const float m = ml[q], e = es[q];
+        if (m == -INFINITY) continue;
+        if (m > M) {
+            W = (M == -INFINITY) ? 0.f : W * expf(M - m);
+            M = m;
+        }
+        W += expf(m - M) * e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Wo = __shfl_xor_sync(0xffffffffu, W, o);
+        const float Mn = fmaxf(M, Mo);
+        W = (M == -INFINITY ? 0.f : W * expf(M - Mn)) + (Mo == -INFINITY ? 0.f : Wo * expf(Mo - Mn));
+        M = Mn;
+    }
+    const float invW = W > 0.f ? 1.f / W : 0.f;
+
+    // weighted sum of the partition outputs; lane i holds the weight of
+    // partition p0 + 32j + i for the current group j of 32
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    float c = m1 == -INFINITY ? 0.f : expf(m1 - M) * e1 * invW;
+#pragma unroll
+    for (int k = 0; k < PRE; ++k) {
+        const float ck = __shfl_sync(0xffffffffu, c, k);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] = fmaf(ck, pre[k][v], acc[v]);
+    }
+    for (int qb = p0 + PRE; qb < P; qb += PRE) {
+        if (((qb - p0) & 31) == 0) {  // next group of 32 partitions
+            const int q = qb + lane;
+            c = 0.f;
+            if (q < P) {
+                const float m = ml[q];
+                c = m == -INFINITY ? 0.f : expf(m - M) * es[q] * invW;
+            }
+        }
+        float t[PRE][VEC];
+#pragma unroll
+        for (int k = 0; k < PRE; ++k) {
+            if (qb + k < P) {
+                load_out(qb + k, t[k]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) t[k][v] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PRE; ++k) {
+            const float ck = __shfl_sync(0xffffffffu, c, (qb - p0 + k) & 31);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] = fmaf(ck, t[k][v], acc[v]);
+        }
+    }
+
+    T* dst = static_cast<T*>(p.out) + (row * p.num_heads + h) * HEAD + lane * VEC;
+    if constexpr (std::is_same<T, float>::value) {
+        if constexpr (VEC == 4)
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        else
+            *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+    } else {
+        constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+        if constexpr (VEC == 4) {
+            uint2 v;
+            v.x = pack2<BF>(acc[0], acc[1]);
+            v.y = pack2<BF>(acc[2], acc[3]);
+            *reinterpret_cast<uint2*>(dst) = v;
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack2<BF>(acc[0], acc[1]);
+        }
+    }
+    // statistics: sequence frame -> absolute ALiBi positions; unused partitions
+    // padded (every read of this row's statistics is above, in this warp)
+    __syncwarp();
+    const float shift = p.alibi ? __ldg(p.alibi + h) * (float)(len - 1) : 0.f;
+    for (int q = lane; q < p.max_parts; q += 32) {
+        if (q >= p0 && q < P) {
+            if (p.alibi) ml[q] += shift;
+        } else {
+            ml[q] = -INFINITY;
+            es[q] = 0.f;
+        }
     }
 }
 

@@ -113,13 +113,30 @@ cudaError_t launch_reduce_shape(const Params& p, const LaunchArgs& la) {
 }
 
 template <typename T, int HEAD, bool MQ>
+cudaError_t launch_reduce_warp(const Params& p, const LaunchArgs& la, int64_t rows) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kReduceWarpsPerCta - 1) / kReduceWarpsPerCta));
+    cfg.blockDim = dim3(kReduceWarpsPerCta * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = la.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pa_reduce_warp_kernel<T, HEAD, MQ>, p);
+}
+
+template <typename T, int HEAD, bool MQ>
 cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
-    // the wide shape only when there are few (sequence, head) rows to spread
-    // (e.g. 4 x 28 rows of 196 partitions); many rows fill the GPU anyway and
-    // most of a ragged batch's rows are short
+    // Few (sequence, head) rows of many partitions (4 x 28 rows of 196): a
+    // wide CTA per row; otherwise one warp per row, so that a batch of
+    // thousands of short rows runs in one wave instead of several waves of
+    // CTAs that each wait on one round trip.
     const int64_t rows = (int64_t)p.num_seqs * p.max_q_len * p.num_heads;
     if (p.max_parts > 32 && rows <= 2 * (int64_t)la.sm_count)
         return launch_reduce_shape<T, HEAD, 16, 8, MQ>(p, la);
+    if (p.max_parts <= PA_REDUCE_WARP_MAX_PARTS) return launch_reduce_warp<T, HEAD, MQ>(p, la, rows);
     return launch_reduce_shape<T, HEAD, 8, 4, MQ>(p, la);
 }
 
