@@ -204,7 +204,9 @@ def run_ours(args, world, rank, local):
     sl = torch.from_numpy(w.seq_lens).to(dev)
     al = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(dev)
     out = torch.empty(q.shape, dtype=tdt, device=dev)
-    ws = pa.alloc_workspace(w.num_seqs, w.num_heads, w.head_size, w.max_seq_len, dev)
+    qs = None if w.query_start is None else torch.from_numpy(w.query_start).to(dev)
+    ws = pa.alloc_workspace(w.num_seqs, w.num_heads, w.head_size, w.max_seq_len, dev,
+                            num_query_tokens=None if qs is None else w.num_query_tokens)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     mode = args.mode if args.mode != "auto" else pa.choose_mode(w.num_seqs, w.num_kv_heads,
@@ -213,7 +215,8 @@ def run_ours(args, world, rank, local):
     common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
                   kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
                   alibi_slopes=al, softcap=w.softcap, layout=w.layout, mode=mode,
-                  dev_error=err, **ws)
+                  dev_error=err, query_start=qs,
+                  max_query_len=None if qs is None else w.max_query_len, **ws)
     cargs = [pa.make_args(out, q, kcs[i], vcs[i], bt, sl, **common) for i in range(copies)]
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -305,7 +308,8 @@ def run_ours(args, world, rank, local):
                    + w.seq_lens.nbytes)
     if mode == "v2":
         P = -(-w.seq_lens.astype(np.int64) // 512)
-        total_bytes += int(P.sum()) * w.num_heads * (w.head_size + 2) * 4 * 2
+        qn = np.ones_like(P) if w.query_start is None else np.diff(w.query_start).astype(np.int64)
+        total_bytes += int((P * qn).sum()) * w.num_heads * (w.head_size + 2) * 4 * 2
 
     # e2e: host buffers, copies inside the timed region
     e2e = None
@@ -316,8 +320,10 @@ def run_ours(args, world, rank, local):
         hbt = torch.from_numpy(w.block_tables).pin_memory()
         hsl = torch.from_numpy(w.seq_lens).pin_memory()
         hal = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).pin_memory()
+        hqs = None if qs is None else torch.from_numpy(w.query_start).pin_memory()
         hout = torch.empty(out.shape, dtype=tdt).pin_memory()
-        h2d = hq.nbytes + hk.nbytes + hv.nbytes + hbt.nbytes + hsl.nbytes + (hal.nbytes if hal is not None else 0)
+        h2d = (hq.nbytes + hk.nbytes + hv.nbytes + hbt.nbytes + hsl.nbytes +
+               (hal.nbytes if hal is not None else 0) + (hqs.nbytes if hqs is not None else 0))
         d2h = hout.nbytes
         Ke = max(3, min(K, 50))
 
@@ -329,6 +335,8 @@ def run_ours(args, world, rank, local):
             sl.copy_(hsl, non_blocking=True)
             if hal is not None:
                 al.copy_(hal, non_blocking=True)
+            if hqs is not None:
+                qs.copy_(hqs, non_blocking=True)
             step(0)
             hout.copy_(out, non_blocking=True)
 

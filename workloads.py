@@ -89,6 +89,9 @@ SPECS = {
                       kv_dtype="e4m3", k_scale=2.0 ** -6, v_scale=2.0 ** -6),
     "long100k_fp8": Spec("long100k_fp8", 4, 28, 4, 128, "bf16", seq_len=100000, seed_index=6,
                          kv_dtype="e4m3", k_scale=2.0 ** -6, v_scale=2.0 ** -6),
+    # several query tokens per sequence (speculative decoding: 4 drafted tokens
+    # verified at once): 32 x 4096, 32/8 heads (group 4, 16 rows per tile)
+    "spec4k": Spec("spec4k", 32, 32, 8, 128, "bf16", seq_len=4096, seed_index=7, q_len=4),
 }
 
 DESCRIPTIONS = {
@@ -99,6 +102,7 @@ DESCRIPTIONS = {
     "large_batch": "large batch: 128 seqs x 16384, 64/8 heads, d=128, bf16 (x2), softcap 30",
     "gqa4k_fp8": "GQA decode, fp8 e4m3 KV cache (scales 2^-6): 32 seqs x 4096, 28/4 heads, d=128, fp16 query",
     "long100k_fp8": "long context, fp8 e4m3 KV cache (scales 2^-6): 4 seqs x 100000, 28/4 heads, d=128, bf16 query",
+    "spec4k": "speculative decode: 32 seqs x 4096 with 4 query tokens each (causal), 32/8 heads, d=128, bf16",
 }
 
 
