@@ -1386,8 +1386,10 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 
 // ------------------------------------------------------------------ kernels
 
+// Two n-tiles hold 16 rows of accumulators (~200 registers uncapped): cap them
+// so that two CTAs share an SM, as they do for one n-tile.
 template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, bool MQ>
-__global__ void __launch_bounds__((NC + 1) * 32, PA_MIN_CTAS_PER_SM)
+__global__ void __launch_bounds__((NC + 1) * 32, NT > 1 ? 2 : PA_MIN_CTAS_PER_SM)
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
