@@ -250,6 +250,20 @@ pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_s
 int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t sm_count);
 
+/*
+ * Test hook for the bounded waits of the kernels (failure detection without a
+ * GPU fault).  While `enable` is non-zero, every later pa_decode call of this
+ * process withholds the copy of the first page of one CTA, so the consumer
+ * warp waiting for it gives up after `wait_limit_ns`; the kernels then set
+ * PA_DEVERR_TIMEOUT in dev_error, stop, and return (results of that call are
+ * invalid; the CUDA context stays usable).  `wait_limit_ns` (0 = 2 s, the
+ * default) is the limit of every barrier wait of later calls, enabled or not.
+ * pa_debug_withhold_page(0, 0) restores normal operation.  Not thread-safe
+ * against concurrent pa_decode calls.  Returns PA_ERR_INVALID_ARG for a
+ * negative limit.  (The pages have no counterpart.)
+ */
+pa_status pa_debug_withhold_page(int32_t enable, int64_t wait_limit_ns);
+
 /* Static string for a pa_status value. */
 const char* pa_status_str(int32_t status);
 

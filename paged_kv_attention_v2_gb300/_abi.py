@@ -34,7 +34,7 @@ PA_BLOCK_SIZE = 16
 
 # every function include/pa_decode.h declares
 EXPORTED = ("pa_decode", "pa_max_num_partitions", "pa_workspace_elems", "pa_choose_mode",
-            "pa_status_str", "pa_version", "pa_decode_static_workspace")
+            "pa_status_str", "pa_version", "pa_decode_static_workspace", "pa_debug_withhold_page")
 
 PA_STATIC_WORKSPACE_FLOATS = 4 * 1024 * 1024
 PA_FUSED_MAX_PARTITIONS = 8
@@ -110,6 +110,8 @@ def load(path: Path | None = None):
     lib.pa_version.restype = ctypes.c_int32
     lib.pa_decode_static_workspace.argtypes = [ctypes.POINTER(PaDecodeArgs), ctypes.c_void_p]
     lib.pa_decode_static_workspace.restype = ctypes.c_int
+    lib.pa_debug_withhold_page.argtypes = [ctypes.c_int32, ctypes.c_int64]
+    lib.pa_debug_withhold_page.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib

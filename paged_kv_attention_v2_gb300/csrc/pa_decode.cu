@@ -73,6 +73,10 @@ bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_siz
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+// Test hook of pa_debug_withhold_page (process-wide).
+std::atomic<int> g_withhold_page{0};
+std::atomic<int64_t> g_wait_limit_ns{0};
+
 }  // namespace
 
 extern "C" {
@@ -124,6 +128,13 @@ const char* pa_status_str(int32_t status) {
     case PA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     default: return "unknown status";
     }
+}
+
+pa_status pa_debug_withhold_page(int32_t enable, int64_t wait_limit_ns) {
+    if (wait_limit_ns < 0) return PA_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(wait_limit_ns);
+    g_withhold_page.store(enable ? 1 : 0);
+    return PA_OK;
 }
 
 pa_status pa_decode(const pa_decode_args* a, void* stream) {
@@ -219,6 +230,8 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.max_q_len = max_q;
     p.num_q_rows = multi ? a->num_query_tokens : a->num_seqs;
     p.fused = 0;  // decided at launch, once the persistent grid size is known
+    p.wait_limit_ns = (uint64_t)g_wait_limit_ns.load();
+    p.withhold_page = g_withhold_page.load();
 
     alignas(64) CUtensorMap tmk, tmv;
     std::memset(&tmk, 0, sizeof tmk);

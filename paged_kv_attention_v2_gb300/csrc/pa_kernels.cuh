@@ -31,7 +31,7 @@ constexpr int kPart = PA_PARTITION_SIZE;  // tokens per partition
 constexpr int kBS = PA_BLOCK_SIZE;        // tokens per page
 constexpr int kSplit = PA_LAYOUT_SPLIT;
 constexpr int kNHD = PA_LAYOUT_NHD;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait (default)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Cache element kinds (template parameter KV of the partition kernel).
@@ -87,6 +87,8 @@ struct Params {
     int max_q_len;               // upper bound of query tokens per sequence (1 without query_start)
     int num_q_rows;              // rows of query / out / workspace
     int fused;          // v2 with the log-sum-exp merge done by the last CTA of each (seq, kv head)
+    uint64_t wait_limit_ns;  // limit of every barrier wait (0: kWaitLimitNs)
+    int withhold_page;       // test hook: CTA 0 withholds its first page copy (a wait runs out)
 };
 
 struct TileDesc {
@@ -195,11 +197,13 @@ struct Smem {
     uint32_t full, empty, td_full, td_empty;  // shared addresses of barrier arrays
     uint32_t merge_bar;  // consumer warps: partial states written / epilogue reads done
     volatile int* abort;     // [0] give-up flag, [1] never set (drain waits), [2] last-arriver flag
+    uint64_t wait_ns;        // limit of every barrier wait
 };
 
 // Bounded wait by every lane of a warp; the result is the same in all lanes.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort, kWaitLimitNs);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -208,7 +212,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ bool consumer_sync(const Smem& sm, uint32_t& phase, int lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.merge_bar);
-    const bool ok = warp_wait(sm.merge_bar, phase & 1, sm.abort);
+    const bool ok = warp_wait(sm.merge_bar, phase & 1, sm.abort, sm.wait_ns);
     ++phase;
     return ok;
 }
@@ -336,7 +340,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
 
         const int slot = k % C::kTD;
         if (lane == 0) {
-            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, kWaitLimitNs);
+            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, sm.wait_ns);
             if (ok) {
                 TileDesc& d = sm.desc[slot];
                 d.seq = cur.seq;
@@ -374,8 +378,11 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                 if (lane < nb) {
                     const uint32_t gg = g + (uint32_t)lane;
                     const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
-                    lok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, kWaitLimitNs);
-                    if (lok) {
+                    lok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, sm.wait_ns);
+                    // test hook: CTA 0 never issues its first page, so the consumer
+                    // waiting for it runs out of time (bounded, no fault)
+                    const bool withhold = p.withhold_page && blockIdx.x == 0 && gg == 0;
+                    if (lok && !withhold) {
                         const uint32_t fb = sm.full + st * 8;
                         const uint32_t dk = sm.ring + st * C::kStageBytes;
                         const uint32_t dv = dk + C::kPageBytes;
@@ -407,7 +414,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     if (lane == 0) {
         if (ok) {
             const int slot = k % C::kTD;
-            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, kWaitLimitNs);
+            ok = mbar_wait(sm.td_empty + slot * 8, ((k / C::kTD) & 1) ^ 1, sm.abort, sm.wait_ns);
             if (ok) {
                 sm.desc[slot].flags = kTileStop;
                 mbar_arrive(sm.td_full + slot * 8);
@@ -421,7 +428,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         // wait (bounded) for the last phase issued on every stage.
         for (uint32_t st = 0; st < STAGES && st < g; ++st) {
             const uint32_t last = g - 1 - ((g - 1 - st) % STAGES);
-            mbar_wait(sm.full + st * 8, (last / STAGES) & 1, sm.abort + 1, kWaitLimitNs);
+            mbar_wait(sm.full + st * 8, (last / STAGES) & 1, sm.abort + 1, sm.wait_ns);
         }
     }
 }
@@ -687,7 +694,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
     uint32_t mphase = 0;
     for (int k = 0;; ++k) {
         const int slot = k % C::kTD;
-        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort, sm.wait_ns)) {
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -766,7 +773,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
-            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
                 return;
@@ -972,7 +979,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
     uint32_t mphase = 0;
     for (int k = 0;; ++k) {
         const int slot = k % C::kTD;
-        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort, sm.wait_ns)) {
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -1060,7 +1067,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
-            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
                 return;
@@ -1217,7 +1224,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
     uint32_t mphase = 0;
     for (int k = 0;; ++k) {
         const int slot = k % C::kTD;
-        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort)) {
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort, sm.wait_ns)) {
             report(p, PA_DEVERR_TIMEOUT);
             *sm.abort = 1;
             return;
@@ -1260,7 +1267,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
-            if (!warp_wait(sm.full + st * 8, ph, sm.abort)) {
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
                 return;
@@ -1411,6 +1418,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, NT > 1 ? 2 : PA_MIN_CTAS_PER_SM
     sm.td_empty = sm.td_full + C::kTD * 8;
     sm.merge_bar = sm.td_empty + C::kTD * 8;
     sm.abort = reinterpret_cast<volatile int*>(gen + C::oAbort);
+    sm.wait_ns = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {

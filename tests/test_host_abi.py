@@ -185,3 +185,8 @@ def test_binding_multi_token_rows():
     assert (a.num_seqs, a.num_query_tokens, a.max_query_len) == (2, 5, 3)
     b = pa.make_args(q5[:2], q5[:2], k16, k16, bt, sl, **kw)
     assert (b.num_seqs, b.query_start, b.num_query_tokens) == (2, None, 0)
+
+
+def test_withhold_page_hook_arguments(lib):
+    assert lib.pa_debug_withhold_page(0, -1) == _abi.PA_ERR_INVALID_ARG
+    assert lib.pa_debug_withhold_page(0, 0) == _abi.PA_OK
