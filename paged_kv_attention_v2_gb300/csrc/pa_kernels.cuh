@@ -436,31 +436,53 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
 // ------------------------------------------------------------------ epilogue
 
 // Merge the NC consumer warps' partial states of one tile and write either the
-// partition statistics (v2) or the final output row (v1).
+// partition statistics (v2) or the final output row (v1).  Each thread owns up
+// to ITEMS (row, 4-column) items; all their shared-memory loads are issued
+// before any arithmetic, so the merge costs one dependency chain, not ITEMS.
 template <class C, typename T, int HEAD, int NC>
 __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm, int tid) {
     constexpr int D4 = HEAD / 4;
+    constexpr int ITEMS = (C::kMaxG * D4 + NC * 32 - 1) / (NC * 32);
     const int G = p.group;
     // row v of the merge buffers: query token v / G, head kvh * G + v % G
     const int qn = C::kMQ ? d.qn : 1;
-    for (int idx = tid; idx < qn * G * D4; idx += NC * 32) {
+    const int n = qn * G * D4;
+    float2 e[ITEMS][NC];
+    float4 a[ITEMS][NC];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int idx = tid + it * NC * 32;
+        const int h = idx / D4, d4 = idx - h * D4;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) {
+            if (idx < n) {
+                e[it][w] = sm.ml[w * C::kMaxG + h];
+                a[it][w] = *reinterpret_cast<const float4*>(
+                    sm.merge + (w * C::kMaxG + h) * C::kMergeStride + 4 * d4);
+            } else {
+                e[it][w] = make_float2(-INFINITY, 0.f);
+                a[it][w] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int idx = tid + it * NC * 32;
+        if (idx >= n) break;
         const int h = idx / D4, d4 = idx - h * D4;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NC; ++w) M = fmaxf(M, sm.ml[w * C::kMaxG + h].x);
+        for (int w = 0; w < NC; ++w) M = fmaxf(M, e[it][w].x);
         float L = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < NC; ++w) {
-            const float2 e = sm.ml[w * C::kMaxG + h];
-            const float c = (e.x == -INFINITY) ? 0.f : expf(e.x - M);
-            L += c * e.y;
-            const float4 a = *reinterpret_cast<const float4*>(
-                sm.merge + (w * C::kMaxG + h) * C::kMergeStride + 4 * d4);
-            o.x += c * a.x;
-            o.y += c * a.y;
-            o.z += c * a.z;
-            o.w += c * a.w;
+            const float c = (e[it][w].x == -INFINITY) ? 0.f : exp2f((e[it][w].x - M) * kLog2e);
+            L += c * e[it][w].y;
+            o.x += c * a[it][w].x;
+            o.y += c * a[it][w].y;
+            o.z += c * a[it][w].z;
+            o.w += c * a[it][w].w;
         }
         const float inv = L > 0.f ? p.v_scale / L : 0.f;
         o.x *= inv;
@@ -482,7 +504,8 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
             }
         } else {
             const int64_t ps = sh * p.max_parts + d.part;
-            *reinterpret_cast<float4*>(p.tmp_out + ps * HEAD + 4 * d4) = o;
+            // kept in L2 for the reduce that follows (the read demotes it)
+            st_global_v4_hint(p.tmp_out + ps * HEAD + 4 * d4, o, l2_policy_evict_last());
             if (d4 == 0) {
                 float m = M;
                 // logits are kept relative to the tile's last token; move the
@@ -1495,6 +1518,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     float* ml = p.max_logits + sb;
     float* es = p.exp_sums + sb;
     const float* tmp = p.tmp_out + sb * HEAD;
+    const uint64_t pol = l2_policy_evict_first();  // partition outputs: last use
     T* o = static_cast<T*>(p.out) + (row * p.num_heads + h) * HEAD;
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1510,7 +1534,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
                 if (q < P) {
                     mq[u] = ml[q];
                     eq[u] = es[q];
-                    t[u] = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD + 4 * d4);
+                    t[u] = ld_global_v4_hint(tmp + (int64_t)q * HEAD + 4 * d4, pol);
                 } else {
                     mq[u] = -INFINITY;
                     eq[u] = 0.f;
@@ -1627,12 +1651,13 @@ __global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel
     const float* tmp = p.tmp_out + sb * HEAD + lane * VEC;
 
     // partition outputs p0 .. p0 + 7 and this lane's first statistics, all in flight
+    const uint64_t pol = l2_policy_evict_first();  // partition outputs: last use
     auto load_out = [&](int q, float (&t)[VEC]) {
         if constexpr (VEC == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD);
+            const float4 v = ld_global_v4_hint(tmp + (int64_t)q * HEAD, pol);
             t[0] = v.x; t[1] = v.y; t[2] = v.z; t[3] = v.w;
         } else {
-            const float2 v = *reinterpret_cast<const float2*>(tmp + (int64_t)q * HEAD);
+            const float2 v = ld_global_v2_hint(tmp + (int64_t)q * HEAD, pol);
             t[0] = v.x; t[1] = v.y;
         }
     };
