@@ -32,6 +32,19 @@ int sm_count_for_current_device(int* out) {
     return 0;
 }
 
+int l2_bytes_for_current_device(int* out) {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return -1;
+        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v);
+    }
+    *out = v;
+    return 0;
+}
+
 // ---------------------------------------------------------------- tensor maps
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -231,6 +244,16 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     p.num_q_rows = multi ? a->num_query_tokens : a->num_seqs;
     p.fused = 0;  // decided at launch, once the persistent grid size is known
     p.wait_limit_ns = (uint64_t)g_wait_limit_ns.load();
+    // KV copies marked evict_first while the partition outputs (at most the
+    // workspace) take no more than half of L2; with larger workspaces it was
+    // measured to slow the partition kernel (128 x 16384: +1.6 %)
+    {
+        int l2 = 0;
+        if (l2_bytes_for_current_device(&l2) != 0) return PA_ERR_LAUNCH;
+        const int64_t rows = multi ? a->num_query_tokens : a->num_seqs;
+        const int64_t tmp_bytes = v1 ? 0 : rows * a->num_heads * (int64_t)max_parts * a->head_size * 4;
+        p.kv_evict_first = tmp_bytes <= (int64_t)l2 / 2 ? 1 : 0;
+    }
     p.withhold_page = g_withhold_page.load();
 
     alignas(64) CUtensorMap tmk, tmv;

@@ -89,6 +89,7 @@ struct Params {
     int fused;          // v2 with the log-sum-exp merge done by the last CTA of each (seq, kv head)
     uint64_t wait_limit_ns;  // limit of every barrier wait (0: kWaitLimitNs)
     int withhold_page;       // test hook: CTA 0 withholds its first page copy (a wait runs out)
+    int kv_evict_first;      // KV page copies marked evict_first (partition outputs small against L2)
 };
 
 struct TileDesc {
@@ -232,6 +233,9 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     const char* vbase = static_cast<const char*>(p.value_cache);
     const char* qbase = static_cast<const char*>(p.query);
     const uint32_t qbytes = (uint32_t)(p.group * HEAD * C::kElem);
+    // KV pages are read once: first to leave L2, ahead of the partition outputs
+    // (measured: a gain while those fit in L2, a loss once they overflow it)
+    const uint64_t kvpol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
 
     // Walk of seq_lens in chunks of 32 sequences: lane i holds sequence cb+i.
     int cb = 0, cu = 0;  // first sequence of the chunk, tile units before the chunk
@@ -392,12 +396,12 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                             const int y = (int)(page * kBS);
 #pragma unroll
                             for (int half = 0; half < HEAD / 64; ++half) {
-                                tensor2d_g2s(dk + half * 2048, tmk, half * 64, y, fb);
-                                tensor2d_g2s(dv + half * 2048, tmv, half * 64, y, fb);
+                                tensor2d_g2s_hint(dk + half * 2048, tmk, half * 64, y, fb, kvpol);
+                                tensor2d_g2s_hint(dv + half * 2048, tmv, half * 64, y, fb, kvpol);
                             }
                         } else {
-                            bulk_g2s(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb);
-                            bulk_g2s(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb);
+                            bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
+                            bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
                         }
                     }
                 }

@@ -82,6 +82,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// The same with an L2 access policy for the source lines (from createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared through a tensor map.  The inner
 // coordinate x times the element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -90,6 +100,15 @@ __device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap* ma
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tensor2d_g2s_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                  uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -115,12 +134,18 @@ __device__ __forceinline__ void pdl_wait_primary() {
 
 // ---------------------------------------------------------------- L2 eviction hints
 
-// Access policies for the partition outputs: written with evict_last so they
-// are still in L2 when the reduce reads them (that read then demotes them with
-// evict_first, so they do not outstay their use).
+// L2 access policies (createpolicy): the partition outputs are written with
+// evict_last when they fit, so they are still in L2 when the reduce reads them
+// (that read demotes them with evict_first, so they do not outstay their use).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
