@@ -70,8 +70,8 @@ typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_F16 = 1, PA_DTYPE_BF16 = 2 } 
  * paged_attention_v2_pytorch.py): the caches hold K / k_scale and V / v_scale. */
 typedef enum pa_kv_dtype {
     PA_KV_SAME = 0,      /* same as dtype */
-    PA_KV_FP8_E4M3 = 3,  /* OCP fp8 E4M3 (bias 7, no infinities); split layout, f16/bf16 query */
-    PA_KV_FP8_E5M2 = 4   /* OCP fp8 E5M2 (bias 15); split layout, f16/bf16 query */
+    PA_KV_FP8_E4M3 = 3,  /* OCP fp8 E4M3 (bias 7, no infinities); f16/bf16 query */
+    PA_KV_FP8_E5M2 = 4   /* OCP fp8 E5M2 (bias 15); f16/bf16 query */
 } pa_kv_dtype;
 
 /*

@@ -84,6 +84,23 @@ bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_siz
     return r == CUDA_SUCCESS;
 }
 
+// fp8 NHD page of one kv head = 16 rows of head_size bytes: one box of the
+// whole page, swizzled by 128 bytes (head_size 128) or 64 bytes (64) so the
+// kernel's four-byte reads of eight token rows fall in distinct banks.
+bool make_nhd_map_fp8(CUtensorMap* map, const void* base, int64_t rows, int head_size) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size};
+    cuuint32_t box[2] = {(cuuint32_t)head_size, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    head_size == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 // Test hook of pa_debug_withhold_page (process-wide).
@@ -166,8 +183,7 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
         return PA_ERR_INVALID_ARG;
     const int kv = a->kv_dtype;
     if (kv != PA_KV_SAME && kv != PA_KV_FP8_E4M3 && kv != PA_KV_FP8_E5M2) return PA_ERR_INVALID_ARG;
-    if (kv != PA_KV_SAME && (a->dtype == PA_DTYPE_F32 || a->layout != PA_LAYOUT_SPLIT))
-        return PA_ERR_UNSUPPORTED;
+    if (kv != PA_KV_SAME && a->dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
     if (a->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
     if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
     const int group = a->num_heads / a->num_kv_heads;
@@ -263,9 +279,12 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
         const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
         if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
         const bool bf = a->dtype == PA_DTYPE_BF16;
-        if (!make_nhd_map(&tmk, a->key_cache, rows, a->head_size, bf) ||
-            !make_nhd_map(&tmv, a->value_cache, rows, a->head_size, bf))
-            return PA_ERR_LAUNCH;
+        const bool ok = kv != PA_KV_SAME
+                            ? make_nhd_map_fp8(&tmk, a->key_cache, rows, a->head_size) &&
+                                  make_nhd_map_fp8(&tmv, a->value_cache, rows, a->head_size)
+                            : make_nhd_map(&tmk, a->key_cache, rows, a->head_size, bf) &&
+                                  make_nhd_map(&tmv, a->value_cache, rows, a->head_size, bf);
+        if (!ok) return PA_ERR_LAUNCH;
     }
 
     pa::LaunchArgs la;

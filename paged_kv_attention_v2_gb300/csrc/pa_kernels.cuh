@@ -162,8 +162,8 @@ struct Cfg {
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
-    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32 && KV == kKvSame;
-    static_assert(KV == kKvSame || (LAYOUT == kSplit && !kF32), "fp8 caches: split layout, 16-bit query");
+    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32;
+    static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
     static constexpr int kScratchFloats = kF32 ? NC * (kBS * 16 + 16) : 0;
 
     static constexpr int oRing = 0;
@@ -392,7 +392,12 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                         const uint32_t dv = dk + C::kPageBytes;
                         const int64_t page = (int64_t)b * Hkv + cur.kvh;
                         mbar_arrive_expect_tx(fb, C::kStageBytes);
-                        if constexpr (C::kTensorMap) {
+                        if constexpr (C::kTensorMap && C::kKvElem == 1) {
+                            // fp8 NHD: one box of 16 token rows x HEAD bytes per page
+                            const int y = (int)(page * kBS);
+                            tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
+                            tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
+                        } else if constexpr (C::kTensorMap) {
                             const int y = (int)(page * kBS);
 #pragma unroll
                             for (int half = 0; half < HEAD / 64; ++half) {
@@ -976,6 +981,25 @@ __device__ __forceinline__ void fp8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t&
             : "r"(w));
 }
 
+// Byte offset of 16-byte chunk c of token row t in an fp8 NHD page as the
+// tensor copy leaves it: rows of HEAD bytes, chunks swizzled (128-byte swizzle:
+// chunk ^ (t mod 8); 64-byte swizzle: chunk ^ ((t / 2) mod 4)), so the eight
+// rows a warp reads at once fall in distinct banks.
+template <int HEAD>
+__device__ __forceinline__ uint32_t nhd8_off(int t, int c) {
+    const int sw = HEAD == 128 ? (t & 7) : ((t >> 1) & 3);
+    return (uint32_t)(t * HEAD + ((c ^ sw) << 4));
+}
+
+// fp8 NHD value page: zero the rows of tokens >= valid (whole rows: the
+// swizzle only permutes chunks inside a row).
+template <int HEAD>
+__device__ __forceinline__ void zero_v_tail8_nhd(uint32_t vpage, int valid, int lane) {
+    for (int i = lane; i < (kBS - valid) * HEAD / 4; i += 32)
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(vpage + (uint32_t)(valid * HEAD + 4 * i)), "r"(0u)
+                     : "memory");
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -992,14 +1016,17 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
 //   P.V    k-index 2cq+j <-> token    4cq+j, 2cq+8+j <-> 4cq+2+j  (per page)
 // so row rr of S^T (the M index of Q.K^T) holds token tau(rr) of the page:
 //   tau(r) = 4*(r/2) + (r&1) and tau(r+8) = tau(r) + 2 for r < 8.
-template <class C, typename T, int HEAD, int NT, int STAGES, int NC, int KV>
+template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV>
 __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int lane) {
     constexpr bool QBF = C::kBF16;
     constexpr int KT = HEAD / 16;
     const int G = p.group;
     const int r = lane >> 2, cq = lane & 3;
-    const int tlo = ((r >> 1) << 2) + (r & 1);  // page token of S^T row r
-    const int thi = tlo + 2;                    // page token of S^T row r + 8
+    // page token of S^T rows r and r + 8: permuted for the split layout (see
+    // above), natural for NHD, where the transposition of V is done by movmatrix
+    const int tau = ((r >> 1) << 2) + (r & 1);
+    const int tlo = LAYOUT == kNHD ? r : tau;
+    const int thi = LAYOUT == kNHD ? r + 8 : tau + 2;
     const bool has_alibi = p.alibi != nullptr;
     const bool has_cap = p.softcap > 0.f;
     uint32_t gbase = 0;
@@ -1105,12 +1132,16 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             const int valid = min(kBS, d.tok_end - tok0);
             const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;  // some key masked
             if (valid < kBS) {
-                zero_v_tail8<HEAD>(vp, valid, lane);
+                if constexpr (LAYOUT == kNHD)
+                    zero_v_tail8_nhd<HEAD>(vp, valid, lane);
+                else
+                    zero_v_tail8<HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
 
-            // S^T[row][head]: key page [d/16][token][16 bytes]
+            // S^T[row][head]: key page [d/16][token][16 bytes] (split) or
+            // [token][d] with swizzled 16-byte chunks (NHD)
             float s[NT][4], s2[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -1119,8 +1150,13 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a0, a1, a2, a3;
-                fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
-                fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
+                if constexpr (LAYOUT == kNHD) {
+                    fp8x4_to_f16<KV>(lds32(kp + nhd8_off<HEAD>(tlo, kk) + 4 * cq), a0, a2);
+                    fp8x4_to_f16<KV>(lds32(kp + nhd8_off<HEAD>(thi, kk) + 4 * cq), a1, a3);
+                } else {
+                    fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
+                    fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     if (kk & 1)
@@ -1185,12 +1221,27 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));
             }
 
-            // acc^T[head dim][head] += V^T . P^T: value page [d][16 tokens]
+            // acc^T[head dim][head] += V^T . P^T.  Split value page [d][16 tokens]:
+            // one 32-bit load is four permuted tokens of a head dim.  NHD page
+            // [token][d]: one load is four head dims of a token; movmatrix turns
+            // each 8 x 8 block (tokens x head dims 16mt + 4cq + {0,1} or {2,3})
+            // into the A fragment, whose rows are then head dims 16mt + tau(r)
+            // (rows r) and 16mt + tau(r) + 2 (rows r + 8).
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
-                fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
+                if constexpr (LAYOUT == kNHD) {
+                    uint32_t lo0, hi0, lo1, hi1;
+                    fp8x4_to_f16<KV>(lds32(vp + nhd8_off<HEAD>(r, mt) + 4 * cq), lo0, hi0);
+                    fp8x4_to_f16<KV>(lds32(vp + nhd8_off<HEAD>(r + 8, mt) + 4 * cq), lo1, hi1);
+                    a0 = movmatrix_trans(lo0);
+                    a1 = movmatrix_trans(hi0);
+                    a2 = movmatrix_trans(lo1);
+                    a3 = movmatrix_trans(hi1);
+                } else {
+                    fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
+                    fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                     mma_16816<false>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
@@ -1213,11 +1264,13 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             const int h0 = nt * 8 + 2 * cq;
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
-                const int d0 = mt * 16 + r;
+                // head dims of accumulator rows r and r + 8 (see the P.V step)
+                const int d0 = mt * 16 + (LAYOUT == kNHD ? tau : r);
+                const int d1 = d0 + (LAYOUT == kNHD ? 2 : 8);
                 mw[h0 * C::kMergeStride + d0] = acc[mt][nt][0];
                 mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][nt][1];
-                mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][nt][2];
-                mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
+                mw[h0 * C::kMergeStride + d1] = acc[mt][nt][2];
+                mw[(h0 + 1) * C::kMergeStride + d1] = acc[mt][nt][3];
             }
             if (r == 0) {
                 sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
@@ -1481,7 +1534,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, NT > 1 ? 2 : PA_MIN_CTAS_PER_SM
         if constexpr (KV == kKvSame)
             consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
         else
-            consumer_mma_fp8<C, T, HEAD, NT, STAGES, NC, KV>(p, sm, warp, lane);
+            consumer_mma_fp8<C, T, HEAD, NT, LAYOUT, STAGES, NC, KV>(p, sm, warp, lane);
     }
 }
 

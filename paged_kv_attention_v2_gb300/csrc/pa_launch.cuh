@@ -142,12 +142,8 @@ cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
 
 template <typename T, int HEAD, int NT, int KV, bool MQ>
 cudaError_t launch_layout_mq(const Params& p, const LaunchArgs& la, bool* fused) {
-    if constexpr (KV != kKvSame) {  // fp8 caches: split layout only (checked by the host)
-        return launch_main<T, HEAD, NT, kSplit, KV, MQ>(p, la, fused);
-    } else {
-        return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD, KV, MQ>(p, la, fused)
-                                 : launch_main<T, HEAD, NT, kSplit, KV, MQ>(p, la, fused);
-    }
+    return la.layout == kNHD ? launch_main<T, HEAD, NT, kNHD, KV, MQ>(p, la, fused)
+                             : launch_main<T, HEAD, NT, kSplit, KV, MQ>(p, la, fused);
 }
 
 // Single-token decode and several query tokens per sequence are separate

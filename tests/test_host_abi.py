@@ -118,7 +118,6 @@ def _args(**over):
     ({"tmp_out": None}, _abi.PA_ERR_WORKSPACE),
     ({"exp_sums": None}, _abi.PA_ERR_WORKSPACE),
     ({"tmp_out": 24}, _abi.PA_ERR_WORKSPACE),              # misaligned workspace
-    ({"kv_dtype": _abi.PA_KV_FP8_E4M3, "layout": _abi.PA_LAYOUT_NHD}, _abi.PA_ERR_UNSUPPORTED),
     ({"kv_dtype": _abi.PA_KV_FP8_E5M2, "dtype": _abi.PA_DTYPE_F32}, _abi.PA_ERR_UNSUPPORTED),
     ({"kv_dtype": 9}, _abi.PA_ERR_INVALID_ARG),
     ({"k_scale": float("inf")}, _abi.PA_ERR_INVALID_ARG),

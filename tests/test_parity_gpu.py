@@ -33,7 +33,8 @@ def _workload(name, layout):
 
 FULL = [("tiny", "split"), ("tiny", "nhd"), ("gqa4k", "split"), ("gqa4k", "nhd"),
         ("long100k", "split"), ("long100k", "nhd"), ("ragged", "split"), ("ragged", "nhd"),
-        ("gqa4k_fp8", "split"), ("long100k_fp8", "split"), ("spec4k", "split"), ("spec4k", "nhd")]
+        ("gqa4k_fp8", "split"), ("gqa4k_fp8", "nhd"), ("long100k_fp8", "split"),
+        ("long100k_fp8", "nhd"), ("spec4k", "split"), ("spec4k", "nhd")]
 
 
 @pytest.mark.parametrize("name,layout", FULL, ids=[f"{n}-{l}" for n, l in FULL])
@@ -223,12 +224,13 @@ FP8 = [
 
 @pytest.mark.parametrize("case", FP8, ids=[c[0] for c in FP8])
 @pytest.mark.parametrize("mode", ["v1", "v2", "v2f"])
-def test_fp8_cache(case, mode):
+@pytest.mark.parametrize("layout", ["split", "nhd"])
+def test_fp8_cache(case, mode, layout):
     name, dtype, kv, H, Hkv, d, lens, alibi, cap, wl, ks, vs = case
     spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv,
                         head_size=d, dtype=dtype, seq_lens=lens, alibi=alibi, softcap=cap,
                         kv_dtype=kv, k_scale=ks, v_scale=vs)
-    w = W.make_workload(spec, "split")
+    w = W.make_workload(spec, layout)
     w.window_left = wl
     ref = oracle.oracle_decode(w)
     g = run_gpu(w, mode=mode, calls=2)
@@ -252,6 +254,8 @@ MULTI = [
     ("q5_f32_head64", "f32", None, "split", 6, 2, 64, (4, 515), 5, False, 0.0, -1),
     ("q2_e4m3_group8", "bf16", "e4m3", "split", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
     ("q3_e5m2_window", "f16", "e5m2", "split", 6, 2, 64, (33, 1500), 3, False, 30.0, 100),
+    ("q2_e4m3_nhd_group8", "bf16", "e4m3", "nhd", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
+    ("q3_e5m2_nhd_head64", "f16", "e5m2", "nhd", 6, 2, 64, (33, 1500), 3, False, 30.0, 100),
 ]
 
 
