@@ -151,7 +151,9 @@ def dist_setup():
 # ------------------------------------------------------------------ oracle timing
 
 def time_oracle(w, budget_s: float, threads=None):
-    """Time the fp64 oracle on the first n sequences of w, n sized to the budget."""
+    """Time the fp64 oracle on the first n sequences of w, n sized to the
+    budget; when the whole batch takes less than the budget, repeat it (up to
+    20 passes) so the figure rests on about budget_s of CPU work."""
     import oracle
     threads = threads or oracle.default_threads()
     t = time.perf_counter()
@@ -163,8 +165,17 @@ def time_oracle(w, budget_s: float, threads=None):
     t = time.perf_counter()
     oracle.oracle_decode(w, seq_subset=subset, threads=threads)
     dt = time.perf_counter() - t
+    passes = 1
+    if n == w.num_seqs and dt < budget_s / 2:
+        extra = int(min(19, budget_s / max(dt, 1e-4) - 1))
+        t = time.perf_counter()
+        for _ in range(extra):
+            oracle.oracle_decode(w, seq_subset=subset, threads=threads)
+        if extra > 0:
+            dt = (dt + time.perf_counter() - t) / (extra + 1)
+            passes += extra
     kv = int(lens[:n].sum()) * w.num_kv_heads * w.head_size * 2 * w.elem_bytes
-    return {"seconds": dt, "kv_bytes": kv, "seqs": n, "threads": threads}
+    return {"seconds": dt, "kv_bytes": kv, "seqs": n, "threads": threads, "passes": passes}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -367,7 +378,8 @@ def run_ours(args, world, rank, local):
                "cores": r["threads"], "kind": "oracle",
                "seconds": round(r["seconds"], 3),
                "sample": f"first {r['seqs']} of {w.num_seqs} sequences (all heads, dense + "
-                         f"partition statistics in fp64), {r['kv_bytes']} KV bytes"}
+                         f"partition statistics in fp64), {r['kv_bytes']} KV bytes, "
+                         f"mean of {r['passes']} pass(es)"}
 
     if world > 1:
         import torch.distributed as dist
