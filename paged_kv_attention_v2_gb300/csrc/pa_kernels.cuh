@@ -44,7 +44,10 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #define PA_STAGES_16BIT 8      // ring stages (one 16-token page of K and V each), 16-bit caches
 #endif
 #ifndef PA_STAGES_FP8
-#define PA_STAGES_FP8 12       // ring stages, fp8 caches (three CTAs per SM fit)
+#define PA_STAGES_FP8 12       // ring stages, fp8 caches, one page each (three CTAs per SM fit)
+#endif
+#ifndef PA_STAGES_FP8_PAIRS
+#define PA_STAGES_FP8_PAIRS 8  // ring stages, fp8 NHD caches with one n-tile: two pages each
 #endif
 #ifndef PA_STAGES_F32
 #define PA_STAGES_F32 4        // ring stages, fp32 caches
@@ -156,7 +159,13 @@ struct Cfg {
     static constexpr int kElem = sizeof(T);                // query / output element
     static constexpr int kKvElem = KV == kKvSame ? (int)sizeof(T) : 1;
     static constexpr int kPageBytes = kBS * HEAD * kKvElem;  // one page of K (or of V)
-    static constexpr int kStageBytes = 2 * kPageBytes;
+    // Pages per stage.  fp8 NHD with one n-tile takes two: one barrier round,
+    // max reduction and rescale per two pages pays for its value transposes
+    // (measured: long100k_fp8 95.4 -> 86.7 µs); for the split layout the third
+    // CTA per SM that one-page stages leave room for is worth more (76.2 against
+    // 86.6 µs), and 16-row tiles would spill.
+    static constexpr int kPPS = (KV != kKvSame && NT == 1 && LAYOUT == kNHD) ? 2 : 1;
+    static constexpr int kStageBytes = 2 * kPPS * kPageBytes;  // K pages, then V pages
     static constexpr int kMaxG = kF32 ? 16 : NT * 8;       // heads per kv head handled
     static constexpr int kQBytes = kMaxG * HEAD * kElem;
     static constexpr int kTD = 2;                          // tile descriptor ring depth
@@ -372,41 +381,51 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
             const int n = min(32, cur.npages - pc);
             // block ids of the next 32 pages (this tile or the next one), loaded early
             const int ids_next = (pc + 32 < cur.npages) ? load_ids(cur, pc + 32) : load_ids(nxt, 0);
-            // Issue in batches of up to STAGES pages, one page per lane: the
-            // pages of a batch sit in distinct stages, so each lane waits for
-            // exactly the previous use of its own stage.
-            for (int b0 = 0; b0 < n && ok; b0 += STAGES) {
-                const int nb = min(STAGES, n - b0);
-                const int b = __shfl_sync(0xffffffffu, ids, (b0 + lane) & 31);
+            // Issue in batches of up to STAGES stages (kPPS consecutive pages
+            // each), one stage per lane: the stages of a batch are distinct, so
+            // each lane waits for exactly the previous use of its own stage.
+            constexpr int PPS = C::kPPS;
+            const int nst = (n + PPS - 1) / PPS;
+            for (int b0 = 0; b0 < nst && ok; b0 += STAGES) {
+                const int nb = min(STAGES, nst - b0);
+                int bq[PPS];
+#pragma unroll
+                for (int q = 0; q < PPS; ++q) bq[q] = __shfl_sync(0xffffffffu, ids, ((b0 + lane) * PPS + q) & 31);
                 bool lok = true;
                 if (lane < nb) {
                     const uint32_t gg = g + (uint32_t)lane;
                     const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
                     lok = mbar_wait(sm.empty + st * 8, ph ^ 1, sm.abort, sm.wait_ns);
-                    // test hook: CTA 0 never issues its first page, so the consumer
+                    // test hook: CTA 0 never issues its first stage, so the consumer
                     // waiting for it runs out of time (bounded, no fault)
                     const bool withhold = p.withhold_page && blockIdx.x == 0 && gg == 0;
                     if (lok && !withhold) {
+                        const int npg = min(PPS, n - (b0 + lane) * PPS);  // pages of this stage
                         const uint32_t fb = sm.full + st * 8;
-                        const uint32_t dk = sm.ring + st * C::kStageBytes;
-                        const uint32_t dv = dk + C::kPageBytes;
-                        const int64_t page = (int64_t)b * Hkv + cur.kvh;
-                        mbar_arrive_expect_tx(fb, C::kStageBytes);
-                        if constexpr (C::kTensorMap && C::kKvElem == 1) {
-                            // fp8 NHD: one box of 16 token rows x HEAD bytes per page
-                            const int y = (int)(page * kBS);
-                            tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
-                            tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
-                        } else if constexpr (C::kTensorMap) {
-                            const int y = (int)(page * kBS);
+                        const uint32_t dk0 = sm.ring + st * C::kStageBytes;
+                        const uint32_t dv0 = dk0 + PPS * C::kPageBytes;
+                        mbar_arrive_expect_tx(fb, (uint32_t)npg * 2 * C::kPageBytes);
 #pragma unroll
-                            for (int half = 0; half < HEAD / 64; ++half) {
-                                tensor2d_g2s_hint(dk + half * 2048, tmk, half * 64, y, fb, kvpol);
-                                tensor2d_g2s_hint(dv + half * 2048, tmv, half * 64, y, fb, kvpol);
+                        for (int q = 0; q < PPS; ++q) {
+                            if (q >= npg) break;
+                            const uint32_t dk = dk0 + q * C::kPageBytes, dv = dv0 + q * C::kPageBytes;
+                            const int64_t page = (int64_t)bq[q] * Hkv + cur.kvh;
+                            if constexpr (C::kTensorMap && C::kKvElem == 1) {
+                                // fp8 NHD: one box of 16 token rows x HEAD bytes per page
+                                const int y = (int)(page * kBS);
+                                tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
+                                tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
+                            } else if constexpr (C::kTensorMap) {
+                                const int y = (int)(page * kBS);
+#pragma unroll
+                                for (int half = 0; half < HEAD / 64; ++half) {
+                                    tensor2d_g2s_hint(dk + half * 2048, tmk, half * 64, y, fb, kvpol);
+                                    tensor2d_g2s_hint(dv + half * 2048, tmv, half * 64, y, fb, kvpol);
+                                }
+                            } else {
+                                bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
+                                bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
                             }
-                        } else {
-                            bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
-                            bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
                         }
                     }
                 }
@@ -1116,9 +1135,14 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
         }
 
+        // kPPS consecutive pages per ring stage: one barrier round, one max
+        // reduction and one rescale of the accumulators per stage
+        constexpr int PPS = C::kPPS;
+        constexpr int STOK = PPS * kBS;  // tokens per stage
         const int npages = tile_pages(d.tok_begin, d.tok_end);
+        const int nstages = (npages + PPS - 1) / PPS;
         const int page0 = d.tok_begin / kBS * kBS;
-        for (int j = warp; j < npages; j += NC) {
+        for (int j = warp; j < nstages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
             if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
@@ -1126,69 +1150,86 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 *sm.abort = 1;
                 return;
             }
-            const uint32_t kp = sm.ring + st * C::kStageBytes;
-            const uint32_t vp = kp + C::kPageBytes;
-            const int tok0 = page0 + j * kBS;
-            const int valid = min(kBS, d.tok_end - tok0);
-            const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;  // some key masked
-            if (valid < kBS) {
-                if constexpr (LAYOUT == kNHD)
-                    zero_v_tail8_nhd<HEAD>(vp, valid, lane);
-                else
-                    zero_v_tail8<HEAD>(vp, valid, lane);
+            const uint32_t kp = sm.ring + st * C::kStageBytes;  // key page q at kp + q * kPageBytes
+            const uint32_t vp = kp + PPS * C::kPageBytes;       // value page q at vp + q * kPageBytes
+            const int tok0 = page0 + j * STOK;
+            const int valid = min(STOK, d.tok_end - tok0);
+            const bool edge = tok0 < lo_all || tok0 + STOK - 1 > hi_all;  // some key masked
+            if (valid < STOK) {
+#pragma unroll
+                for (int q = 0; q < PPS; ++q) {
+                    const int vq = min(max(valid - q * kBS, 0), kBS);  // valid tokens of page q
+                    if (vq < kBS) {
+                        if constexpr (LAYOUT == kNHD)
+                            zero_v_tail8_nhd<HEAD>(vp + q * C::kPageBytes, vq, lane);
+                        else
+                            zero_v_tail8<HEAD>(vp + q * C::kPageBytes, vq, lane);
+                    }
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
 
-            // S^T[row][head]: key page [d/16][token][16 bytes] (split) or
-            // [token][d] with swizzled 16-byte chunks (NHD)
-            float s[NT][4], s2[NT][4];
+            // S^T[row][head] per page: key page [d/16][token][16 bytes] (split)
+            // or [token][d] with swizzled 16-byte chunks (NHD)
+            float s[PPS][NT][4], s2[PPS][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int q = 0; q < PPS; ++q)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[q][nt][e] = s2[q][nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                if constexpr (LAYOUT == kNHD) {
-                    fp8x4_to_f16<KV>(lds32(kp + nhd8_off<HEAD>(tlo, kk) + 4 * cq), a0, a2);
-                    fp8x4_to_f16<KV>(lds32(kp + nhd8_off<HEAD>(thi, kk) + 4 * cq), a1, a3);
-                } else {
-                    fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
-                    fp8x4_to_f16<KV>(lds32(kp + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
-                }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (kk & 1)
-                        mma_16816<false>(s2[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
-                    else
-                        mma_16816<false>(s[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                for (int q = 0; q < PPS; ++q) {
+                    const uint32_t kq = kp + q * C::kPageBytes;
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (LAYOUT == kNHD) {
+                        fp8x4_to_f16<KV>(lds32(kq + nhd8_off<HEAD>(tlo, kk) + 4 * cq), a0, a2);
+                        fp8x4_to_f16<KV>(lds32(kq + nhd8_off<HEAD>(thi, kk) + 4 * cq), a1, a3);
+                    } else {
+                        fp8x4_to_f16<KV>(lds32(kq + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
+                        fp8x4_to_f16<KV>(lds32(kq + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kk & 1)
+                            mma_16816<false>(s2[q][nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                        else
+                            mma_16816<false>(s[q][nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                    }
                 }
             }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
 
-            uint32_t pb[NT][2];
+            uint32_t pb[PPS][NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float z[4];
+                float z[PPS][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = s[nt][e] * p.scale;
-                    if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
-                    if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + ((e >> 1) ? thi : tlo) - origin);
-                    z[e] = v;
+                for (int q = 0; q < PPS; ++q) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float v = (s[q][nt][e] + s2[q][nt][e]) * p.scale;
+                        if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                        if (has_alibi)
+                            v += sl[nt][e & 1] * (float)(tok0 + q * kBS + ((e >> 1) ? thi : tlo) - origin);
+                        z[q][e] = v;
+                    }
+                    if (edge) {
+                        const int t0 = tok0 + q * kBS + tlo, t1 = tok0 + q * kBS + thi;
+                        if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[q][0] = -INFINITY;
+                        if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[q][1] = -INFINITY;
+                        if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[q][2] = -INFINITY;
+                        if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[q][3] = -INFINITY;
+                    }
                 }
-                if (edge) {
-                    const int t0 = tok0 + tlo, t1 = tok0 + thi;
-                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
-                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
-                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
-                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                float mx0 = fmaxf(z[0][0], z[0][2]), mx1 = fmaxf(z[0][1], z[0][3]);
+#pragma unroll
+                for (int q = 1; q < PPS; ++q) {
+                    mx0 = fmaxf(mx0, fmaxf(z[q][0], z[q][2]));
+                    mx1 = fmaxf(mx1, fmaxf(z[q][1], z[q][3]));
                 }
-                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -1196,20 +1237,28 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 }
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
                 // several query tokens: a row with no key in its range so far keeps
-                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
-                // appears.  One token: every page holds a key of every row.
+                // max -inf (masked stages only); take 0 as reference so no -inf - -inf
+                // appears.  One token: every stage holds a key of every row.
                 const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
                 const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
                 const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
                 const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
-                const float p0 = exp2f((z[0] - mr0) * kLog2e);
-                const float p1 = exp2f((z[1] - mr1) * kLog2e);
-                const float p2 = exp2f((z[2] - mr0) * kLog2e);
-                const float p3 = exp2f((z[3] - mr1) * kLog2e);
-                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
-                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int q = 0; q < PPS; ++q) {
+                    const float p0 = exp2f((z[q][0] - mr0) * kLog2e);
+                    const float p1 = exp2f((z[q][1] - mr1) * kLog2e);
+                    const float p2 = exp2f((z[q][2] - mr0) * kLog2e);
+                    const float p3 = exp2f((z[q][3] - mr1) * kLog2e);
+                    ls0 += p0 + p2;
+                    ls1 += p1 + p3;
+                    pb[q][nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tlo
+                    pb[q][nt][1] = movmatrix_trans(pack2<false>(p2, p3));
+                }
+                l[nt][0] = l[nt][0] * al0 + ls0;
+                l[nt][1] = l[nt][1] * al1 + ls1;
 #pragma unroll
                 for (int mt = 0; mt < KT; ++mt) {
                     acc[mt][nt][0] *= al0;
@@ -1217,34 +1266,36 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                     acc[mt][nt][2] *= al0;
                     acc[mt][nt][3] *= al1;
                 }
-                pb[nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tau
-                pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));
             }
 
-            // acc^T[head dim][head] += V^T . P^T.  Split value page [d][16 tokens]:
-            // one 32-bit load is four permuted tokens of a head dim.  NHD page
-            // [token][d]: one load is four head dims of a token; movmatrix turns
-            // each 8 x 8 block (tokens x head dims 16mt + 4cq + {0,1} or {2,3})
-            // into the A fragment, whose rows are then head dims 16mt + tau(r)
-            // (rows r) and 16mt + tau(r) + 2 (rows r + 8).
+            // acc^T[head dim][head] += V^T . P^T, page by page.  Split value page
+            // [d][16 tokens]: one 32-bit load is four permuted tokens of a head
+            // dim.  NHD page [token][d]: one load is four head dims of a token;
+            // movmatrix turns each 8 x 8 block (tokens x head dims 16mt + 4cq +
+            // {0,1} or {2,3}) into the A fragment, whose rows are then head dims
+            // 16mt + tau(r) (rows r) and 16mt + tau(r) + 2 (rows r + 8).
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                if constexpr (LAYOUT == kNHD) {
-                    uint32_t lo0, hi0, lo1, hi1;
-                    fp8x4_to_f16<KV>(lds32(vp + nhd8_off<HEAD>(r, mt) + 4 * cq), lo0, hi0);
-                    fp8x4_to_f16<KV>(lds32(vp + nhd8_off<HEAD>(r + 8, mt) + 4 * cq), lo1, hi1);
-                    a0 = movmatrix_trans(lo0);
-                    a1 = movmatrix_trans(hi0);
-                    a2 = movmatrix_trans(lo1);
-                    a3 = movmatrix_trans(hi1);
-                } else {
-                    fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
-                    fp8x4_to_f16<KV>(lds32(vp + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
-                }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_16816<false>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                for (int q = 0; q < PPS; ++q) {
+                    const uint32_t vq = vp + q * C::kPageBytes;
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (LAYOUT == kNHD) {
+                        uint32_t lo0, hi0, lo1, hi1;
+                        fp8x4_to_f16<KV>(lds32(vq + nhd8_off<HEAD>(r, mt) + 4 * cq), lo0, hi0);
+                        fp8x4_to_f16<KV>(lds32(vq + nhd8_off<HEAD>(r + 8, mt) + 4 * cq), lo1, hi1);
+                        a0 = movmatrix_trans(lo0);
+                        a1 = movmatrix_trans(hi0);
+                        a2 = movmatrix_trans(lo1);
+                        a3 = movmatrix_trans(hi1);
+                    } else {
+                        fp8x4_to_f16<KV>(lds32(vq + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
+                        fp8x4_to_f16<KV>(lds32(vq + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816<false>(acc[mt][nt], a0, a1, a2, a3, pb[q][nt][0], pb[q][nt][1]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + st * 8);
@@ -1287,7 +1338,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             *sm.abort = 1;
             return;
         }
-        gbase += (uint32_t)npages;
+        gbase += (uint32_t)nstages;
     }
 }
 

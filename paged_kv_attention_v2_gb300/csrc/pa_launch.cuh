@@ -37,7 +37,9 @@ constexpr int kMaxDevices = 64;
 template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32
-                           : (KV == kKvSame ? PA_STAGES_16BIT : PA_STAGES_FP8);
+                           : (KV == kKvSame ? PA_STAGES_16BIT
+                                            : (NT == 1 && LAYOUT == kNHD ? PA_STAGES_FP8_PAIRS
+                                                                         : PA_STAGES_FP8));
     constexpr int NC = PA_CONSUMER_WARPS;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
     auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
