@@ -148,6 +148,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over the ranks of the initialised process group
+    (x itself without one): the whole job takes as long as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Aggregate GB/s of `world` replicas that each move bytes_per_rank per step,
+    timed by the slowest one (weak scaling: per-GPU work fixed)."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ oracle timing
 
 def time_oracle(w, budget_s: float, threads=None):
@@ -303,15 +321,10 @@ def run_ours(args, world, rank, local):
     if derr:
         raise SystemExit(f"device error bits {derr} during the bench")
 
-    ms_step = ms_total / K
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(ms_total / K, dev)
 
     kv = w.kv_bytes
-    value = kv * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(kv, world, ms_step)
     peak, peak_kind = peaks()
     k_ms = statistics.mean(kernel_ms)
     achieved = kv / (k_ms * 1e-3) / 1e9
@@ -361,13 +374,8 @@ def run_ours(args, world, rank, local):
             e2e_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        ms_e2e = f0.elapsed_time(f1) / Ke
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        e2e = {"value": round(kv * world / (ms_e2e * 1e-3) / 1e9, 3), "unit": "GB/s",
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1) / Ke, dev)
+        e2e = {"value": round(whole_job_gbs(kv, world, ms_e2e), 3), "unit": "GB/s",
                "ms_per_step": round(ms_e2e, 4), "steps": Ke,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
