@@ -238,8 +238,11 @@ def run_ours(args, world, rank, local):
                             num_query_tokens=None if qs is None else w.num_query_tokens)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the library's AUTO choice with the host copy of the lengths a serving
+    # loop has at hand (the same rule pa_decode applies to seq_lens_host)
     mode = args.mode if args.mode != "auto" else pa.choose_mode(w.num_seqs, w.num_kv_heads,
-                                                                 w.max_seq_len, sm_count)
+                                                                 w.max_seq_len, sm_count,
+                                                                 w.seq_lens)
     fused = False  # no partition counters: v2 always launches the reduce kernel
     common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
                   kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,

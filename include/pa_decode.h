@@ -189,6 +189,10 @@ typedef struct pa_decode_args {
     const int32_t* query_start;
     int32_t num_query_tokens;  /* rows of query / out / workspace */
     int32_t max_query_len;     /* >= every qn, >= 1; max_query_len * group <= 16 */
+    /* Optional HOST copy of seq_lens ([num_seqs] int32, read during the call,
+     * never by the device), used only by PA_MODE_AUTO to pick v1 or v2 with
+     * pa_choose_mode_for_lengths; NULL = pa_choose_mode (max_seq_len only). */
+    const int32_t* seq_lens_host;
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the
@@ -249,6 +253,18 @@ pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_s
  */
 int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t sm_count);
+
+/*
+ * The same choice when the lengths are known on the host (seq_lens_host,
+ * [num_seqs] int32; NULL behaves as pa_choose_mode).  v1 (one tile per
+ * (sequence, kv head), no partition statistics, no reduce launch) is taken
+ * when max_seq_len <= PA_PARTITION_SIZE, or when those tiles are at least as
+ * many as the SMs and the persistent grid's static assignment of them gives
+ * every CTA nearly the same number of pages (largest load at most 10 % above
+ * the mean); otherwise v2.  Returns PA_MODE_V1 or PA_MODE_V2.
+ */
+int32_t pa_choose_mode_for_lengths(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                   int32_t sm_count, const int32_t* seq_lens_host);
 
 /*
  * Test hook for the bounded waits of the kernels (failure detection without a

@@ -44,8 +44,19 @@ def max_num_partitions(max_seq_len: int) -> int:
     return int(library().pa_max_num_partitions(int(max_seq_len)))
 
 
-def choose_mode(num_seqs: int, num_kv_heads: int, max_seq_len: int, sm_count: int) -> str:
-    m = library().pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count)
+def choose_mode(num_seqs: int, num_kv_heads: int, max_seq_len: int, sm_count: int,
+                seq_lens_host=None) -> str:
+    """The library's AUTO choice; with seq_lens_host (host int32 lengths) the
+    length-aware rule of pa_choose_mode_for_lengths."""
+    if seq_lens_host is None:
+        m = library().pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count)
+    else:
+        import numpy as np
+        lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        if lens.shape != (num_seqs,):
+            raise ValueError("seq_lens_host must hold num_seqs lengths")
+        m = library().pa_choose_mode_for_lengths(num_seqs, num_kv_heads, max_seq_len, sm_count,
+                                                 lens.ctypes.data)
     return "v1" if m == _abi.PA_MODE_V1 else "v2"
 
 
@@ -87,7 +98,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               event_begin=None, event_end=None, partition_counters=None,
               window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
               v_scale: float = 1.0, query_start=None,
-              max_query_len: int | None = None) -> _abi.PaDecodeArgs:
+              max_query_len: int | None = None, seq_lens_host=None) -> _abi.PaDecodeArgs:
     """Build the C argument struct.  The library validates sizes and types it can
     see; this also checks what only the tensors know: the caches' element size
     and element count against kv_dtype, head_size and num_kv_heads.
@@ -98,7 +109,9 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
     and V / v_scale; the query dtype sets the compute and output type.
     query_start ([num_seqs + 1] int32 offsets) gives several query tokens per
     sequence: query / out rows are query tokens, and max_query_len (>= every
-    sequence's token count) is required with it."""
+    sequence's token count) is required with it.  seq_lens_host (a host copy of
+    seq_lens: numpy array or CPU tensor) lets mode "auto" choose by the actual
+    lengths; the struct keeps a reference to it."""
     num_rows, num_heads, head_size = query.shape
     num_seqs = seq_lens.shape[0]
     if tuple(out.shape) != tuple(query.shape):
@@ -121,7 +134,14 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         if c.numel() != num_blocks * page:
             raise ValueError(f"{name} holds {c.numel()} elements, expected "
                              f"num_blocks {num_blocks} x {page}")
-    return _abi.PaDecodeArgs(
+    host_lens = None
+    if seq_lens_host is not None:
+        import numpy as np
+        src = seq_lens_host.numpy() if hasattr(seq_lens_host, "numpy") else seq_lens_host
+        host_lens = np.ascontiguousarray(np.asarray(src, dtype=np.int32))
+        if host_lens.shape != (num_seqs,):
+            raise ValueError("seq_lens_host must hold num_seqs lengths")
+    a = _abi.PaDecodeArgs(
         out=_ptr(out), query=_ptr(query), key_cache=_ptr(key_cache),
         value_cache=_ptr(value_cache), block_tables=_ptr(block_tables), seq_lens=_ptr(seq_lens),
         num_seqs=num_seqs, num_heads=num_heads, num_kv_heads=num_kv_heads, head_size=head_size,
@@ -137,7 +157,10 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         kv_dtype=_KV[kv_dtype], k_scale=float(k_scale), v_scale=float(v_scale),
         query_start=_ptr(query_start), num_query_tokens=num_rows if query_start is not None else 0,
         max_query_len=int(max_query_len) if query_start is not None else 0,
+        seq_lens_host=None if host_lens is None else host_lens.ctypes.data,
     )
+    a._keep_host_lens = host_lens  # the pointer above stays valid as long as the struct lives
+    return a
 
 
 def pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens, *, stream=None,

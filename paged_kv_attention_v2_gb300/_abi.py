@@ -34,6 +34,7 @@ PA_BLOCK_SIZE = 16
 
 # every function include/pa_decode.h declares
 EXPORTED = ("pa_decode", "pa_max_num_partitions", "pa_workspace_elems", "pa_choose_mode",
+            "pa_choose_mode_for_lengths",
             "pa_status_str", "pa_version", "pa_decode_static_workspace", "pa_debug_withhold_page")
 
 PA_STATIC_WORKSPACE_FLOATS = 4 * 1024 * 1024
@@ -76,6 +77,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("query_start", ctypes.c_void_p),
         ("num_query_tokens", ctypes.c_int32),
         ("max_query_len", ctypes.c_int32),
+        ("seq_lens_host", ctypes.c_void_p),
     ]
 
 
@@ -105,6 +107,8 @@ def load(path: Path | None = None):
     lib.pa_workspace_elems.restype = ctypes.c_int
     lib.pa_choose_mode.argtypes = [ctypes.c_int32] * 4
     lib.pa_choose_mode.restype = ctypes.c_int32
+    lib.pa_choose_mode_for_lengths.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_void_p]
+    lib.pa_choose_mode_for_lengths.restype = ctypes.c_int32
     lib.pa_status_str.argtypes = [ctypes.c_int32]
     lib.pa_status_str.restype = ctypes.c_char_p
     lib.pa_version.restype = ctypes.c_int32

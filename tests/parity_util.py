@@ -46,6 +46,12 @@ def to_device(w, device="cuda:0"):
     return d
 
 
+def auto_mode(w, device="cuda:0"):
+    """What mode "auto" picks for w (with its host lengths, as run_gpu passes them)."""
+    sm = torch.cuda.get_device_properties(device).multi_processor_count
+    return pa.choose_mode(w.num_seqs, w.num_kv_heads, w.max_seq_len, sm, w.seq_lens)
+
+
 def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_lens=None,
             block_tables=None, poison_workspace=True, counters=None, calls=1):
     """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error.
@@ -77,6 +83,7 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                      num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
                      alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
                      mode=mode, dev_error=err, partition_counters=counters,
+                     seq_lens_host=w.seq_lens if mode == "auto" else None,
                      window_left=getattr(w, "window_left", -1),
                      kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
                      v_scale=getattr(w, "v_scale", 1.0), **mq, **ws)

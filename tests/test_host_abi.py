@@ -189,3 +189,24 @@ def test_binding_multi_token_rows():
 def test_withhold_page_hook_arguments(lib):
     assert lib.pa_debug_withhold_page(0, -1) == _abi.PA_ERR_INVALID_ARG
     assert lib.pa_debug_withhold_page(0, 0) == _abi.PA_OK
+
+
+def test_length_aware_dispatch():
+    """v1 for batches whose (sequence, kv head) tiles fill the GPU evenly; v2 for
+    few tiles or a ragged mix; max_seq_len <= 512 is always v1."""
+    import numpy as np
+    sm = 152
+    assert pa.choose_mode(128, 8, 16384, sm, np.full(128, 16384)) == "v1"      # 1024 equal tiles
+    assert pa.choose_mode(64, 4, 4096, sm, np.full(64, 4096)) == "v1"         # 256 equal tiles
+    assert pa.choose_mode(32, 4, 4096, sm, np.full(32, 4096)) == "v2"         # 128 tiles < SMs
+    assert pa.choose_mode(4, 4, 100000, sm, np.full(4, 100000)) == "v2"       # 16 tiles
+    rng = np.random.default_rng(0)
+    ragged = np.clip(np.round(2.0 ** (15 * rng.random(256))), 1, 32768).astype(np.int32)
+    assert pa.choose_mode(256, 8, 32768, sm, ragged) == "v2"                  # imbalanced
+    lens = np.full(128, 16384)
+    lens[7] = 100                                                            # one short sequence
+    assert pa.choose_mode(128, 8, 16384, sm, lens) == "v1"
+    assert pa.choose_mode(8, 2, 512, sm, np.full(8, 512)) == "v1"
+    assert pa.choose_mode(128, 8, 16384, sm) == "v2"                          # no host lengths
+    with pytest.raises(ValueError):
+        pa.choose_mode(4, 2, 4096, sm, np.full(3, 4096))

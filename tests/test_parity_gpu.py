@@ -23,7 +23,7 @@ import workloads as W
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from parity_util import check_out, check_stats, run_gpu, to_device  # noqa: E402
+from parity_util import auto_mode, check_out, check_stats, run_gpu, to_device  # noqa: E402
 
 
 @functools.lru_cache(maxsize=2)
@@ -47,7 +47,7 @@ def test_workload_parity(name, layout):
         g = run_gpu(w, mode=mode, dev=dev, calls=2 if mode == "v2f" else 1)
         assert g["dev_error"] == 0, (mode, g["dev_error"])
         check_out(w, g["out"], ref["out"], what=f"out[{mode}]")
-        if mode in ("v2", "v2f") or (mode == "auto" and w.max_seq_len > 512):
+        if mode in ("v2", "v2f") or (mode == "auto" and auto_mode(w) == "v2"):
             check_stats(w, g, ref)
     del dev
     torch.cuda.empty_cache()
@@ -69,6 +69,11 @@ def test_large_batch_sampled():
         ml = g["max_logits"]
         assert np.nanmax(ml) <= 30.0 + 1e-3  # softcap bounds every logit
         assert np.abs(g["out"]).max() <= 4 * vmax
+        # v1, which the length-aware dispatch picks for this even batch
+        g1 = run_gpu(w, mode="v1")
+        assert g1["dev_error"] == 0
+        check_out(w, g1["out"], ref["out"], seqs=sample)
+        assert np.all(np.isfinite(g1["out"]))
         del w
 
 
@@ -275,7 +280,7 @@ def test_multi_token(case, mode):
     g = run_gpu(w, mode=mode, calls=2)
     assert g["dev_error"] == 0
     check_out(w, g["out"], ref["out"])
-    if mode in ("v2", "v2f") or (mode == "auto" and w.max_seq_len > 512):
+    if mode in ("v2", "v2f") or (mode == "auto" and auto_mode(w) == "v2"):
         check_stats(w, g, ref)
 
 
@@ -309,3 +314,41 @@ def test_multi_token_bad_query_start_is_flagged_not_faulted():
         assert g["dev_error"] & 2, mode  # PA_DEVERR_SEQ_LEN
     ref = oracle.oracle_decode(w)
     check_out(w, g["out"][:2], ref["out"][:2])  # sequence 0 is untouched
+
+
+@pytest.mark.parametrize("mode", ["v1", "v2"])
+def test_cuda_graph_capture_replays_the_same_result(mode):
+    """pa_decode allocates nothing and never synchronises, so a CUDA graph can
+    capture it (both kernels of v2, with their programmatic dependency) and
+    replay it with the same result as an eager call."""
+    import paged_kv_attention_v2_gb300 as pa
+    from parity_util import torch_dtype
+    spec = W.small_spec(name="graph", num_seqs=5, num_heads=16, num_kv_heads=4, head_size=128,
+                        dtype="bf16", seq_lens=(1, 511, 513, 3000, 1800), alibi=True)
+    w = W.make_workload(spec, "split")
+    dev = to_device(w)
+    H, d = w.num_heads, w.head_size
+    out = torch.empty((w.num_seqs, H, d), dtype=torch_dtype(w.dtype), device="cuda:0")
+    ws = pa.alloc_workspace(w.num_seqs, H, d, w.max_seq_len, "cuda:0")
+    kw = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
+              alibi_slopes=dev["alibi_slopes"], mode=mode, **ws)
+    pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                 dev["seq_lens"], **kw)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                     dev["seq_lens"], stream=s, **kw)
+        g.capture_end()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    check_out(w, out.double().cpu().numpy(), oracle.oracle_decode(w)["out"])
