@@ -166,14 +166,14 @@ struct Cfg {
     // 86.6 µs), and 16-row tiles would spill.
     static constexpr int kPPS = (KV != kKvSame && NT == 1 && LAYOUT == kNHD) ? 2 : 1;
     static constexpr int kStageBytes = 2 * kPPS * kPageBytes;  // K pages, then V pages
-    static constexpr int kMaxG = kF32 ? 16 : NT * 8;       // heads per kv head handled
+    static constexpr int kMaxG = NT * 8;                   // rows (heads x query tokens) handled
     static constexpr int kQBytes = kMaxG * HEAD * kElem;
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
     static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32;
     static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
-    static constexpr int kScratchFloats = kF32 ? NC * (kBS * 16 + 16) : 0;
+    static constexpr int kScratchFloats = kF32 ? NC * (kBS * kMaxG + kMaxG) : 0;
 
     static constexpr int oRing = 0;
     static constexpr int oQ = oRing + STAGES * kStageBytes;
@@ -1345,7 +1345,8 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 // fp32 inputs: CUDA-core arithmetic (tensor cores would round to tf32).
 template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane) {
-    constexpr int MAXG = 16, HPL = MAXG / 2, DPL = HEAD / 32;
+    // C::kMaxG rows (8 or 16): a row set of 8 keeps two CTAs per SM
+    constexpr int MAXG = C::kMaxG, HPL = MAXG / 2, DPL = HEAD / 32;
     const int G = p.group;
     const int t = lane & 15, hs = lane >> 4;  // Q.K^T: lane = (token t, heads hs, hs+2, ...)
     const bool has_alibi = p.alibi != nullptr;

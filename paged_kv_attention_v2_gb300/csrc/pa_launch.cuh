@@ -159,13 +159,9 @@ cudaError_t launch_layout(const Params& p, const LaunchArgs& la, bool* fused) {
 // Whole operation for one (query type, cache type) pair.
 template <typename T, int KV = kKvSame>
 cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
-    constexpr bool F32 = std::is_same<T, float>::value;
     cudaError_t e;
     bool fused = false;
-    if constexpr (F32) {  // one fp32 consumer handles up to 16 rows (query tokens x heads)
-        e = la.head_size == 128 ? launch_layout<T, 128, 2, KV>(p, la, &fused)
-                                : launch_layout<T, 64, 2, KV>(p, la, &fused);
-    } else if (la.head_size == 128) {
+    if (la.head_size == 128) {
         e = la.group_tiles == 2 ? launch_layout<T, 128, 2, KV>(p, la, &fused)
                                 : launch_layout<T, 128, 1, KV>(p, la, &fused);
     } else {
