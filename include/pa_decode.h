@@ -1,9 +1,9 @@
 /*
  * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-KV decode attention library.
  *
- * One query token per sequence attends over that sequence's keys and values,
- * which live in fixed-size pages ("blocks") of a shared cache and are found
- * through a per-sequence block table.  The operation is the one of
+ * One query token per sequence (or several, see query_start) attends over
+ * that sequence's keys and values, which live in fixed-size pages ("blocks")
+ * of a shared cache and are found through a per-sequence block table.  The operation is the one of
  * "paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2 implementation"
  * (function paged_attention_v2_pytorch, Phase 1 per-partition attention and
  * Phase 2 log-sum-exp reduce), with the NHD cache layout and the `softcap`
@@ -27,8 +27,10 @@
  *
  * Conventions for every entry point below:
  *  - All tensor pointers are DEVICE pointers (global memory of the current
- *    device), caller-owned and caller-allocated; the library allocates no
- *    device memory and keeps no state except per-device cached attributes.
+ *    device), caller-owned and caller-allocated, except seq_lens_host (host
+ *    memory, read during the call); the library allocates no device memory
+ *    and keeps no state except per-device cached attributes (and the array of
+ *    pa_decode_static_workspace).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Calls are asynchronous on that stream and never synchronise the host.
  *  - Errors the host can see are returned before anything is launched.
@@ -240,7 +242,9 @@ pa_status pa_decode_static_workspace(const pa_decode_args* args, void* stream);
 int32_t pa_max_num_partitions(int32_t max_seq_len);
 
 /* Element counts of the v2 workspace: *stats_elems for each of exp_sums and
- * max_logits, *tmp_elems for tmp_out.  Returns PA_ERR_INVALID_ARG on bad sizes. */
+ * max_logits, *tmp_elems for tmp_out.  num_seqs is the row count: pass
+ * num_query_tokens when query_start gives several tokens per sequence.
+ * Returns PA_ERR_INVALID_ARG on bad sizes. */
 pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                              int32_t max_seq_len, int64_t* stats_elems, int64_t* tmp_elems);
 
