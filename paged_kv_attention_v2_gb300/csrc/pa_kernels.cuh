@@ -1010,6 +1010,36 @@ __device__ __forceinline__ uint32_t nhd8_off(int t, int c) {
     return (uint32_t)(t * HEAD + ((c ^ sw) << 4));
 }
 
+// ldmatrix.x4 row address of this lane in an fp8 key page for k-steps kk and
+// kk + 1.  Matrix j = lane / 8 holds the 16-byte rows of the eight tokens of
+// S^T rows 0-7 (j even) or 8-15 (j odd) in k-step kk + j / 2, so register j of
+// lane (r, cq) is the word (token of row r or r + 8, head dims 16k + 4cq..+3).
+template <int LAYOUT, int HEAD>
+__device__ __forceinline__ uint32_t k8_frag_off(int lane, int kk) {
+    const int j = lane >> 3, i = lane & 7;
+    const int c = kk + (j >> 1);
+    if constexpr (LAYOUT == kNHD) {
+        return nhd8_off<HEAD>(i + ((j & 1) << 3), c);  // natural token order
+    } else {
+        const int tok = ((i >> 1) << 2) + (i & 1) + ((j & 1) << 1);  // tau(i), tau(i) + 2
+        return (uint32_t)((c * kBS + tok) * 16);
+    }
+}
+
+// ldmatrix.x4 row address of this lane in an fp8 value page for m-tiles mt and
+// mt + 1: split [d][16 tokens] rows are head dims 16(mt + j/2) + i (+ 8 for odd
+// j); NHD rows are tokens i (+ 8 for odd j), chunk mt + j/2.
+template <int LAYOUT, int HEAD>
+__device__ __forceinline__ uint32_t v8_frag_off(int lane, int mt) {
+    const int j = lane >> 3, i = lane & 7;
+    const int m = mt + (j >> 1);
+    if constexpr (LAYOUT == kNHD) {
+        return nhd8_off<HEAD>(i + ((j & 1) << 3), m);
+    } else {
+        return (uint32_t)((m * 16 + i + ((j & 1) << 3)) * kBS);
+    }
+}
+
 // fp8 NHD value page: zero the rows of tokens >= valid (whole rows: the
 // swizzle only permutes chunks inside a row).
 template <int HEAD>
@@ -1179,25 +1209,26 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[q][nt][e] = s2[q][nt][e] = 0.f;
+            // one ldmatrix.x4 fetches the four 32-bit words (tokens tlo / thi,
+            // k-steps kk / kk + 1) that four separate loads would
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
+            for (int kk = 0; kk < KT; kk += 2) {
 #pragma unroll
                 for (int q = 0; q < PPS; ++q) {
-                    const uint32_t kq = kp + q * C::kPageBytes;
-                    uint32_t a0, a1, a2, a3;
-                    if constexpr (LAYOUT == kNHD) {
-                        fp8x4_to_f16<KV>(lds32(kq + nhd8_off<HEAD>(tlo, kk) + 4 * cq), a0, a2);
-                        fp8x4_to_f16<KV>(lds32(kq + nhd8_off<HEAD>(thi, kk) + 4 * cq), a1, a3);
-                    } else {
-                        fp8x4_to_f16<KV>(lds32(kq + (uint32_t)((kk * kBS + tlo) * 16 + 4 * cq)), a0, a2);
-                        fp8x4_to_f16<KV>(lds32(kq + (uint32_t)((kk * kBS + thi) * 16 + 4 * cq)), a1, a3);
-                    }
+                    uint32_t w[4];
+                    ldsm_x4(kp + q * C::kPageBytes + k8_frag_off<LAYOUT, HEAD>(lane, kk), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (kk & 1)
-                            mma_16816<false>(s2[q][nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
-                        else
-                            mma_16816<false>(s[q][nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+                    for (int u = 0; u < 2; ++u) {
+                        uint32_t a0, a1, a2, a3;
+                        fp8x4_to_f16<KV>(w[2 * u], a0, a2);
+                        fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (u)
+                                mma_16816<false>(s2[q][nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
+                            else
+                                mma_16816<false>(s[q][nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
+                        }
                     }
                 }
             }
@@ -1275,26 +1306,32 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             // {0,1} or {2,3}) into the A fragment, whose rows are then head dims
             // 16mt + tau(r) (rows r) and 16mt + tau(r) + 2 (rows r + 8).
 #pragma unroll
-            for (int mt = 0; mt < KT; ++mt) {
+            for (int mt = 0; mt < KT; mt += 2) {
 #pragma unroll
                 for (int q = 0; q < PPS; ++q) {
-                    const uint32_t vq = vp + q * C::kPageBytes;
-                    uint32_t a0, a1, a2, a3;
-                    if constexpr (LAYOUT == kNHD) {
-                        uint32_t lo0, hi0, lo1, hi1;
-                        fp8x4_to_f16<KV>(lds32(vq + nhd8_off<HEAD>(r, mt) + 4 * cq), lo0, hi0);
-                        fp8x4_to_f16<KV>(lds32(vq + nhd8_off<HEAD>(r + 8, mt) + 4 * cq), lo1, hi1);
-                        a0 = movmatrix_trans(lo0);
-                        a1 = movmatrix_trans(hi0);
-                        a2 = movmatrix_trans(lo1);
-                        a3 = movmatrix_trans(hi1);
-                    } else {
-                        fp8x4_to_f16<KV>(lds32(vq + (uint32_t)((mt * 16 + r) * kBS + 4 * cq)), a0, a2);
-                        fp8x4_to_f16<KV>(lds32(vq + (uint32_t)((mt * 16 + r + 8) * kBS + 4 * cq)), a1, a3);
-                    }
+                    // words of rows r and r + 8 (head dims, or tokens for NHD) of
+                    // m-tiles mt and mt + 1 in one ldmatrix.x4
+                    uint32_t w[4];
+                    ldsm_x4(vp + q * C::kPageBytes + v8_frag_off<LAYOUT, HEAD>(lane, mt), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_16816<false>(acc[mt][nt], a0, a1, a2, a3, pb[q][nt][0], pb[q][nt][1]);
+                    for (int u = 0; u < 2; ++u) {
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (LAYOUT == kNHD) {
+                            uint32_t lo0, hi0, lo1, hi1;
+                            fp8x4_to_f16<KV>(w[2 * u], lo0, hi0);
+                            fp8x4_to_f16<KV>(w[2 * u + 1], lo1, hi1);
+                            a0 = movmatrix_trans(lo0);
+                            a1 = movmatrix_trans(hi0);
+                            a2 = movmatrix_trans(lo1);
+                            a3 = movmatrix_trans(hi1);
+                        } else {
+                            fp8x4_to_f16<KV>(w[2 * u], a0, a2);
+                            fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_16816<false>(acc[mt + u][nt], a0, a1, a2, a3, pb[q][nt][0], pb[q][nt][1]);
+                    }
                 }
             }
             __syncwarp();
