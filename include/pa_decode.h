@@ -248,6 +248,13 @@ int32_t pa_max_num_partitions(int32_t max_seq_len);
 pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                              int32_t max_seq_len, int64_t* stats_elems, int64_t* tmp_elems);
 
+/* Bytes of the whole v2 workspace (exp_sums + max_logits + tmp_out, fp32) for
+ * `rows` query rows; 0 on bad sizes. */
+size_t pa_workspace_bytes(int32_t rows, int32_t num_heads, int32_t head_size, int32_t max_seq_len);
+
+/* Tokens per partition of the v2 workspace (PA_PARTITION_SIZE). */
+int32_t pa_partition_size(void);
+
 /*
  * v1 / v2 choice used by PA_MODE_AUTO, as a pure host function (sm_count is
  * the device's multiprocessor count).  The pages decide by tiles against SMs

@@ -34,7 +34,7 @@ PA_BLOCK_SIZE = 16
 
 # every function include/pa_decode.h declares
 EXPORTED = ("pa_decode", "pa_max_num_partitions", "pa_workspace_elems", "pa_choose_mode",
-            "pa_choose_mode_for_lengths",
+            "pa_choose_mode_for_lengths", "pa_workspace_bytes", "pa_partition_size",
             "pa_status_str", "pa_version", "pa_decode_static_workspace", "pa_debug_withhold_page")
 
 PA_STATIC_WORKSPACE_FLOATS = 4 * 1024 * 1024
@@ -107,6 +107,10 @@ def load(path: Path | None = None):
     lib.pa_workspace_elems.restype = ctypes.c_int
     lib.pa_choose_mode.argtypes = [ctypes.c_int32] * 4
     lib.pa_choose_mode.restype = ctypes.c_int32
+    lib.pa_workspace_bytes.argtypes = [ctypes.c_int32] * 4
+    lib.pa_workspace_bytes.restype = ctypes.c_size_t
+    lib.pa_partition_size.argtypes = []
+    lib.pa_partition_size.restype = ctypes.c_int32
     lib.pa_choose_mode_for_lengths.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_void_p]
     lib.pa_choose_mode_for_lengths.restype = ctypes.c_int32
     lib.pa_status_str.argtypes = [ctypes.c_int32]

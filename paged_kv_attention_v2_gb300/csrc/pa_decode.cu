@@ -128,6 +128,14 @@ pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_s
     return PA_OK;
 }
 
+size_t pa_workspace_bytes(int32_t rows, int32_t num_heads, int32_t head_size, int32_t max_seq_len) {
+    int64_t stats = 0, tmp = 0;
+    if (pa_workspace_elems(rows, num_heads, head_size, max_seq_len, &stats, &tmp) != PA_OK) return 0;
+    return (size_t)(2 * stats + tmp) * sizeof(float);
+}
+
+int32_t pa_partition_size(void) { return PA_PARTITION_SIZE; }
+
 /*
  * v1 / v2 choice.  The pages pick v2 when the v2 tiles of one sequence
  * (kv heads x partitions) exceed twice the SM count.  Here the choice is

@@ -210,3 +210,10 @@ def test_length_aware_dispatch():
     assert pa.choose_mode(128, 8, 16384, sm) == "v2"                          # no host lengths
     with pytest.raises(ValueError):
         pa.choose_mode(4, 2, 4096, sm, np.full(3, 4096))
+
+
+def test_workspace_bytes_and_partition_size(lib):
+    assert lib.pa_partition_size() == 512
+    # 4 x 100000 tokens, 28 heads, d 128: 196 partitions per row
+    assert lib.pa_workspace_bytes(4, 28, 128, 100000) == 4 * 28 * 196 * (128 + 2) * 4
+    assert lib.pa_workspace_bytes(-1, 28, 128, 100000) == 0
