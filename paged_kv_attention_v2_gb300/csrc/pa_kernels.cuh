@@ -1464,7 +1464,11 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                 float dot = 0.f;
                 if (h < GE) {
 #pragma unroll 8
-                    for (int d4 = 0; d4 < HEAD / 4; ++d4) {
+                    for (int d = 0; d < HEAD / 4; ++d) {
+                        // NHD rows of 16 tokens are HEAD floats apart: each token's
+                        // lane walks the head dims from its own offset, so the 16
+                        // rows are read in different banks
+                        const int d4 = LAYOUT == kSplit ? d : ((d + t) & (HEAD / 4 - 1));
                         const float4 qv = *reinterpret_cast<const float4*>(q + h * HEAD + 4 * d4);
                         const float4 kv = (LAYOUT == kSplit)
                             ? *reinterpret_cast<const float4*>(kp + (d4 * kBS + t) * 4)  // [d/4][token][4]
