@@ -1388,7 +1388,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
     const int t = lane & 15, hs = lane >> 4;  // Q.K^T: lane = (token t, heads hs, hs+2, ...)
     const bool has_alibi = p.alibi != nullptr;
     const bool has_cap = p.softcap > 0.f;
-    float* pw = sm.scratch + warp * (kBS * MAXG + MAXG);  // p[token][head], alpha[head]
+    float* pw = sm.scratch + warp * (kBS * MAXG + MAXG);  // p[head][token], alpha[head]
     uint32_t gbase = 0;
     uint32_t mphase = 0;
     for (int k = 0;; ++k) {
@@ -1446,7 +1446,6 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
             float* vp = const_cast<float*>(kp) + kBS * HEAD;
             const int tok0 = page0 + j * kBS;
             const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
-            const int skip = d.tok_begin - tok0;          // slots < skip: before the window
             if (valid < kBS) {
                 if constexpr (LAYOUT == kSplit) {
                     for (int dd = lane; dd < HEAD; dd += 32)
@@ -1498,7 +1497,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                 m[i] = mn;
                 l[i] = l[i] * al + pv;
                 if (h < MAXG) {
-                    pw[t * MAXG + h] = pv;
+                    pw[h * kBS + t] = pv;
                     if (t == 0) pw[kBS * MAXG + h] = al;
                 }
             }
@@ -1511,7 +1510,12 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
                     for (int c = 0; c < DPL; ++c) acc[h][c] *= al;
                 }
             }
-            for (int tt = skip > 0 ? skip : 0; tt < valid; ++tt) {
+            // all 16 tokens: masked ones have p = 0 and a finite (or zeroed) V.
+            // Split V rows are 16 tokens (64 B) per head dim, so the lanes walk
+            // the tokens from different offsets to spread the banks.
+#pragma unroll 4
+            for (int ti = 0; ti < kBS; ++ti) {
+                const int tt = LAYOUT == kSplit ? ((ti + (lane >> 1)) & (kBS - 1)) : ti;
                 float vv[DPL];
 #pragma unroll
                 for (int c = 0; c < DPL; ++c) {
@@ -1521,7 +1525,7 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
                 for (int h = 0; h < MAXG; ++h) {
                     if (h < GE) {
-                        const float pr = pw[tt * MAXG + h];
+                        const float pr = pw[h * kBS + tt];
 #pragma unroll
                         for (int c = 0; c < DPL; ++c) acc[h][c] = fmaf(pr, vv[c], acc[h][c]);
                     }
