@@ -69,16 +69,20 @@ EncodeTiledFn encode_fn() {
 
 // NHD page of one kv head = 16 rows of head_size elements.  The map views a
 // cache as [num_blocks * num_kv_heads * 16 rows][head_size] and moves boxes of
-// 16 rows x 64 elements (128 bytes) with the 128-byte swizzle, so that the
-// ldmatrix reads of the kernel are free of bank conflicts.
-bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_size, bool bf16) {
+// 16 rows x 128 bytes (64 16-bit or 32 fp32 elements) with the 128-byte
+// swizzle, so that the kernel's shared-memory reads are free of bank conflicts.
+bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_size, pa_dtype dt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int elem = dt == PA_DTYPE_F32 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
-    cuuint32_t box[2] = {64, 16};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size * elem};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elem), 16};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const CUtensorMapDataType t = dt == PA_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dt == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(map, t, 2,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -319,15 +323,17 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     alignas(64) CUtensorMap tmk, tmv;
     std::memset(&tmk, 0, sizeof tmk);
     std::memset(&tmv, 0, sizeof tmv);
-    if (a->layout == PA_LAYOUT_NHD && a->dtype != PA_DTYPE_F32) {
+    const int group_tiles = max_q * group > 8 ? 2 : 1;
+    // NHD pages come through tensor maps, except fp32 on the CUDA-core
+    // consumer (two n-tiles), which takes plain bulk copies
+    if (a->layout == PA_LAYOUT_NHD && (a->dtype != PA_DTYPE_F32 || (PA_F32_TENSOR && group_tiles == 1))) {
         const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
         if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
-        const bool bf = a->dtype == PA_DTYPE_BF16;
         const bool ok = kv != PA_KV_SAME
                             ? make_nhd_map_fp8(&tmk, a->key_cache, rows, a->head_size) &&
                                   make_nhd_map_fp8(&tmv, a->value_cache, rows, a->head_size)
-                            : make_nhd_map(&tmk, a->key_cache, rows, a->head_size, bf) &&
-                                  make_nhd_map(&tmv, a->value_cache, rows, a->head_size, bf);
+                            : make_nhd_map(&tmk, a->key_cache, rows, a->head_size, (pa_dtype)a->dtype) &&
+                                  make_nhd_map(&tmv, a->value_cache, rows, a->head_size, (pa_dtype)a->dtype);
         if (!ok) return PA_ERR_LAUNCH;
     }
 
@@ -337,7 +343,7 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     la.tmv = &tmv;
     la.sm_count = sm;
     la.tiles_upper = tiles;
-    la.group_tiles = max_q * group > 8 ? 2 : 1;
+    la.group_tiles = group_tiles;
     la.layout = a->layout;
     la.head_size = a->head_size;
     la.ev_begin = a->event_main_begin;

@@ -61,6 +61,9 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #ifndef PA_REDUCE_WARP_MAX_PARTS
 #define PA_REDUCE_WARP_MAX_PARTS 64  // warp-per-row reduce up to this many partitions per row
 #endif
+#ifndef PA_F32_TENSOR
+#define PA_F32_TENSOR 1        // fp32, split layout, one n-tile: three-term tf32 tensor-core path
+#endif
 #ifndef PA_MAX_CTAS_PER_SM
 #define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
 #endif
@@ -171,7 +174,11 @@ struct Cfg {
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
-    static constexpr bool kTensorMap = (LAYOUT == kNHD) && !kF32;
+    // fp32 with one n-tile: the tf32 tensor-core consumer
+    static constexpr bool kTf32 = kF32 && NT == 1 && PA_F32_TENSOR;
+    // NHD pages arrive through 2-D tensor maps, swizzled by 128 bytes (except
+    // for fp32 on the CUDA-core consumer, which reads plain rows)
+    static constexpr bool kTensorMap = (LAYOUT == kNHD) && (!kF32 || kTf32);
     static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
     static constexpr int kScratchFloats = kF32 ? NC * (kBS * kMaxG + kMaxG) : 0;
 
@@ -416,11 +423,13 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                                 tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
                                 tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
                             } else if constexpr (C::kTensorMap) {
+                                // 16-bit / fp32 NHD: boxes of 16 token rows x 128 bytes
+                                constexpr int EPB = 128 / C::kKvElem;  // elements per box row
                                 const int y = (int)(page * kBS);
 #pragma unroll
-                                for (int half = 0; half < HEAD / 64; ++half) {
-                                    tensor2d_g2s_hint(dk + half * 2048, tmk, half * 64, y, fb, kvpol);
-                                    tensor2d_g2s_hint(dv + half * 2048, tmv, half * 64, y, fb, kvpol);
+                                for (int bx = 0; bx < HEAD / EPB; ++bx) {
+                                    tensor2d_g2s_hint(dk + bx * 2048, tmk, bx * EPB, y, fb, kvpol);
+                                    tensor2d_g2s_hint(dv + bx * 2048, tmv, bx * EPB, y, fb, kvpol);
                                 }
                             } else {
                                 bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
@@ -718,6 +727,27 @@ __device__ __forceinline__ void zero_v_tail16(uint32_t vpage, int valid, int lan
             const int rowi = i >> 3, chunk = i & 7;
             const int tok = valid + rowi / (HEAD / 64), half = rowi % (HEAD / 64);
             const uint32_t a = vpage + (uint32_t)(half * 2048 + tok * 128 + chunk * 16);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+        }
+    }
+}
+
+// Zero the fp32 V entries of tokens >= valid in a staged page: split [d][16
+// tokens], or NHD as HEAD / 32 swizzled boxes of 16 token rows x 128 bytes
+// (the swizzle permutes 16-byte chunks within a row, so a row stays one token's).
+template <int LAYOUT, int HEAD>
+__device__ __forceinline__ void zero_v_tail32(uint32_t vpage, int valid, int lane) {
+    if constexpr (LAYOUT == kSplit) {
+        for (int d = lane; d < HEAD; d += 32)
+            for (int t = valid; t < kBS; ++t)
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(vpage + (uint32_t)(d * kBS + t) * 4), "r"(0u)
+                             : "memory");
+    } else {
+        const int rows = (kBS - valid) * (HEAD / 32);
+        for (int i = lane; i < rows * 8; i += 32) {
+            const int rowi = i >> 3, chunk = i & 7;
+            const int tok = valid + rowi / (HEAD / 32), bx = rowi % (HEAD / 32);
+            const uint32_t a = vpage + (uint32_t)(bx * 2048 + tok * 128 + chunk * 16);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
         }
     }
@@ -1379,6 +1409,258 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
     }
 }
 
+// fp32 inputs, one n-tile: tensor cores with each fp32 operand carried as two
+// tf32 terms (hi + lo) and three MMAs per product (hi.hi + hi.lo + lo.hi),
+// which keeps each product to ~2^-20 relative, well inside the fp32 result's
+// error budget.  Tokens on M, query rows on N for Q.K^T; head dims on M, rows
+// on N for P.V, as in the 16-bit consumer.  P moves from the S^T fragment to
+// the B fragment with shuffles (there is no 32-bit movmatrix).
+//
+// Shared-memory reads.  Split pages: K [d/4][16 tokens][4] gives each k-step's
+// A fragment as one ldmatrix.x4; V [d][16 tokens] likewise (its 64-byte rows
+// cost 4-way bank conflicts whatever the order).  NHD pages (HEAD / 32 boxes
+// of 16 token rows x 128 bytes, 16-byte chunks swizzled by token % 8): K by
+// ldmatrix.x4 as well; V^T needs a transpose that ldmatrix does not do for
+// 32-bit elements, so its fragments are single-word loads, with the k-step's
+// tokens taken in the order 0, 2, 4, 6 | 1, 3, 5, 7 (k-index t -> token 2t, t + 4
+// -> 2t + 1), which puts the 32 words of each load in 32 distinct banks; the
+// P^T fragment follows the same order.
+template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
+__device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lane) {
+    constexpr int KT = HEAD / 8;   // k-steps of Q.K^T (8 head dims each)
+    constexpr int MT = HEAD / 16;  // m-tiles of P.V (16 head dims each)
+    const int G = p.group;
+    const int r = lane >> 2, cq = lane & 3;
+    const bool has_alibi = p.alibi != nullptr;
+    const bool has_cap = p.softcap > 0.f;
+    uint32_t gbase = 0;
+    uint32_t mphase = 0;
+    for (int k = 0;; ++k) {
+        const int slot = k % C::kTD;
+        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort, sm.wait_ns)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        const TileDesc d = sm.desc[slot];
+        if (d.flags & kTileStop) return;
+        const int qn = C::kMQ ? d.qn : 1;
+        const int GE = qn * G;  // rows of N: query token v / G, head kvh * G + v % G
+
+        // Q as B fragments (k = head dim 8kk + cq / + 4, n = row r), hi and lo
+        uint32_t qh[KT][2], ql[KT][2];
+        {
+            const float* q = reinterpret_cast<const float*>(
+                __cvta_shared_to_generic(sm.q + slot * C::kQBytes));
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t x = r < GE ? __float_as_uint(q[r * HEAD + kk * 8 + cq + 4 * e]) : 0u;
+                    split_tf32(x, qh[kk][e], ql[kk][e]);
+                }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // Q and descriptor are in registers
+
+        float sl[2];
+        int klo[2], khi[2];  // key range of this lane's rows within the tile
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int v = 2 * cq + e;
+            sl[e] = (has_alibi && v < GE) ? __ldg(p.alibi + d.kvh * G + v % G) : 0.f;
+            int lo = d.tok_begin, hi = d.tok_end - 1;
+            if (C::kMQ && v < GE) {
+                const int pos = d.len - qn + v / G;
+                hi = min(hi, pos);
+                lo = max(lo, window_lo_at(p, pos));
+            }
+            klo[e] = lo;
+            khi[e] = hi;
+        }
+        const int hi_all = C::kMQ ? min(d.tok_end - 1, d.len - qn) : d.tok_end - 1;
+        const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
+        const int origin = d.tok_end - 1;
+
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float acc[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+
+        const int npages = tile_pages(d.tok_begin, d.tok_end);
+        const int page0 = d.tok_begin / kBS * kBS;
+        // ldmatrix row of this lane: matrix j = lane / 8, row i = lane % 8
+        const int lj = lane >> 3, li = lane & 7;
+        for (int j = warp; j < npages; j += NC) {
+            const uint32_t gg = gbase + (uint32_t)j;
+            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+            if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
+                report(p, PA_DEVERR_TIMEOUT);
+                *sm.abort = 1;
+                return;
+            }
+            const uint32_t kp = sm.ring + st * C::kStageBytes;
+            const uint32_t vp = kp + C::kPageBytes;
+            const int tok0 = page0 + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);
+            const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;
+            if (valid < kBS) {
+                zero_v_tail32<LAYOUT, HEAD>(vp, valid, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // S^T[token][row] = K . Q^T; the four 8 x 4 blocks (tokens 0-7 /
+            // 8-15, head dims 8kk..+3 / +4..+7) of a k-step are its A fragment,
+            // one ldmatrix.x4 (this lane's row: block lj, row li)
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                uint32_t a[4], ah[4], al[4];
+                const int cg = 2 * kk + (lj >> 1);  // 16-byte chunk of the head dims
+                const uint32_t ka =
+                    LAYOUT == kSplit
+                        ? kp + (uint32_t)((cg * kBS + li + ((lj & 1) << 3)) * 16)
+                        : kp + (uint32_t)((cg >> 3) * 2048 + (li + ((lj & 1) << 3)) * 128 +
+                                          (((cg & 7) ^ li) << 4));
+                ldsm_x4(ka, a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_tf32(a[e], ah[e], al[e]);
+                float (&sa)[4] = (kk & 1) ? s2 : s;
+                mma_1688_tf32(sa, al[0], al[1], al[2], al[3], qh[kk][0], qh[kk][1]);
+                mma_1688_tf32(sa, ah[0], ah[1], ah[2], ah[3], ql[kk][0], ql[kk][1]);
+                mma_1688_tf32(sa, ah[0], ah[1], ah[2], ah[3], qh[kk][0], qh[kk][1]);
+            }
+
+            float z[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v = (s[e] + s2[e]) * p.scale;
+                if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                if (has_alibi) v += sl[e & 1] * (float)(tok0 + r + ((e >> 1) << 3) - origin);
+                z[e] = v;
+            }
+            if (edge) {
+                const int t0 = tok0 + r, t1 = t0 + 8;
+                if (t0 < klo[0] || t0 > khi[0]) z[0] = -INFINITY;
+                if (t0 < klo[1] || t0 > khi[1]) z[1] = -INFINITY;
+                if (t1 < klo[0] || t1 > khi[0]) z[2] = -INFINITY;
+                if (t1 < klo[1] || t1 > khi[1]) z[3] = -INFINITY;
+            }
+            float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
+            const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = exp2f((m[0] - mr0) * kLog2e);
+            const float al1 = exp2f((m[1] - mr1) * kLog2e);
+            m[0] = mn0;
+            m[1] = mn1;
+            float pv[4];
+            pv[0] = exp2f((z[0] - mr0) * kLog2e);  // (token r,     row 2cq)
+            pv[1] = exp2f((z[1] - mr1) * kLog2e);  // (token r,     row 2cq + 1)
+            pv[2] = exp2f((z[2] - mr0) * kLog2e);  // (token r + 8, row 2cq)
+            pv[3] = exp2f((z[3] - mr1) * kLog2e);  // (token r + 8, row 2cq + 1)
+            l[0] = l[0] * al0 + (pv[0] + pv[2]);
+            l[1] = l[1] * al1 + (pv[1] + pv[3]);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] *= al0;
+                acc[mt][1] *= al1;
+                acc[mt][2] *= al0;
+                acc[mt][3] *= al1;
+            }
+            // B fragments of P^T for k-steps ks = 0, 1 (tokens 8ks..8ks+7):
+            // b0 = P[row r][token 8ks + cq], b1 = P[row r][token 8ks + cq + 4],
+            // held by lanes (token % 8, row / 2), element by row parity and ks
+            uint32_t pbh[2][2], pbl[2][2];
+            // k-index cq holds token cq (split) or 2cq (NHD), cq + 4 token cq + 4 or 2cq + 1
+            const int tk0 = LAYOUT == kSplit ? cq : 2 * cq, tk1 = LAYOUT == kSplit ? cq + 4 : 2 * cq + 1;
+            const int src0 = 4 * tk0 + (r >> 1), src1 = 4 * tk1 + (r >> 1);
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const float e0 = __shfl_sync(0xffffffffu, pv[2 * ks], src0);
+                const float o0 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src0);
+                const float e1 = __shfl_sync(0xffffffffu, pv[2 * ks], src1);
+                const float o1 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src1);
+                split_tf32(__float_as_uint((r & 1) ? o0 : e0), pbh[ks][0], pbl[ks][0]);
+                split_tf32(__float_as_uint((r & 1) ? o1 : e1), pbh[ks][1], pbl[ks][1]);
+            }
+
+            // acc^T[head dim][row] += V^T . P^T; A fragment of (m-tile mt,
+            // k-step ks): head dims 16mt + r / + 8 by k-indices cq / cq + 4
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4], ah[4], al[4];
+                    if constexpr (LAYOUT == kSplit) {
+                        // [d][16 tokens]: the four 8 x 4 blocks (head dims
+                        // 16mt..+7 / +8..+15, tokens 8ks..+3 / +4..+7), one ldmatrix.x4
+                        ldsm_x4(vp + (uint32_t)(((mt * 16 + li + ((lj & 1) << 3)) * kBS + 8 * ks +
+                                                 4 * (lj >> 1)) * 4),
+                                a[0], a[1], a[2], a[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int dim = mt * 16 + r + ((e & 1) << 3);
+                            const int tok = 8 * ks + ((e >> 1) ? tk1 : tk0);
+                            const uint32_t va = vp + (uint32_t)((dim >> 5) * 2048 + tok * 128 +
+                                                                ((((dim >> 2) & 7) ^ (tok & 7)) << 4) +
+                                                                (dim & 3) * 4);
+                            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(a[e]) : "r"(va));
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split_tf32(a[e], ah[e], al[e]);
+                    mma_1688_tf32(acc[mt], al[0], al[1], al[2], al[3], pbh[ks][0], pbh[ks][1]);
+                    mma_1688_tf32(acc[mt], ah[0], ah[1], ah[2], ah[3], pbl[ks][0], pbl[ks][1]);
+                    mma_1688_tf32(acc[mt], ah[0], ah[1], ah[2], ah[3], pbh[ks][0], pbh[ks][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+        }
+
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+        }
+        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+        const int h0 = 2 * cq;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int d0 = mt * 16 + r;
+            mw[h0 * C::kMergeStride + d0] = acc[mt][0];
+            mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][1];
+            mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][2];
+            mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][3];
+        }
+        if (r == 0) {
+            sm.ml[warp * C::kMaxG + h0] = make_float2(m[0], l[0]);
+            sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[1], l[1]);
+        }
+        if (!consumer_sync(sm, mphase, lane)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        if (!tile_finish<C, float, HEAD, NC>(p, d, sm, warp, lane, mphase)) {
+            report(p, PA_DEVERR_TIMEOUT);
+            *sm.abort = 1;
+            return;
+        }
+        gbase += (uint32_t)npages;
+    }
+}
+
 // fp32 inputs: CUDA-core arithmetic (tensor cores would round to tf32).
 template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane) {
@@ -1570,10 +1852,12 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 
 // ------------------------------------------------------------------ kernels
 
-// Two n-tiles hold 16 rows of accumulators (~200 registers uncapped): cap them
-// so that two CTAs share an SM, as they do for one n-tile.
+// Two n-tiles hold 16 rows of accumulators (~200 registers uncapped), and the
+// fp32 tensor-core consumer holds Q as two tf32 terms (~213): cap them so that
+// two CTAs share an SM, as they do for one n-tile of 16-bit inputs.
 template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, bool MQ>
-__global__ void __launch_bounds__((NC + 1) * 32, NT > 1 ? 2 : PA_MIN_CTAS_PER_SM)
+__global__ void __launch_bounds__((NC + 1) * 32,
+                                  (NT > 1 || std::is_same<T, float>::value) ? 2 : PA_MIN_CTAS_PER_SM)
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
@@ -1626,7 +1910,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, NT > 1 ? 2 : PA_MIN_CTAS_PER_SM
     if (warp == NC) {
         producer<C, HEAD, STAGES>(p, sm, &tmk, &tmv, lane);
     } else if constexpr (C::kF32) {
-        consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+        if constexpr (C::kTf32)
+            consumer_tf32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+        else
+            consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
     } else {
         if constexpr (KV == kKvSame)
             consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);

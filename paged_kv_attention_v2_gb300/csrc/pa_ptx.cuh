@@ -230,6 +230,26 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
     }
 }
 
+// D = A * B + D, m16n8k8 with tf32 operands (32-bit registers holding fp32
+// bit patterns; the tensor core uses their tf32 part), fp32 accumulators.
+__device__ __forceinline__ void mma_1688_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// x = hi + lo: hi keeps sign, exponent and the top 10 mantissa bits (exactly
+// a tf32 value), lo the exact remainder (|lo| < 2^-10 |x|), of which a tf32
+// operand keeps the leading 11 bits.  hi.hi + hi.lo + lo.hi then leaves out
+// lo.lo and the dropped bits of lo: ~2^-20 of |x y| per product.
+__device__ __forceinline__ void split_tf32(uint32_t x, uint32_t& hi, uint32_t& lo) {
+    hi = x & 0xffffe000u;
+    lo = __float_as_uint(__uint_as_float(x) - __uint_as_float(hi));
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF16) {

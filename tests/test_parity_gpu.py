@@ -53,6 +53,24 @@ def test_workload_parity(name, layout):
     torch.cuda.empty_cache()
 
 
+def test_f32_full_size():
+    """The 32 x 4096 GQA workload (28 heads over 4 kv heads) with fp32 query and
+    cache, both layouts, every output and partition statistic."""
+    import dataclasses
+    spec = dataclasses.replace(W.SPECS["gqa4k"], name="gqa4k_f32", dtype="f32")
+    for layout in ("split", "nhd"):
+        w = W.make_workload(spec, layout)
+        ref = oracle.oracle_decode(w)
+        for mode in ("v1", "v2"):
+            g = run_gpu(w, mode=mode)
+            assert g["dev_error"] == 0
+            check_out(w, g["out"], ref["out"], what=f"out[{mode}]")
+            if mode == "v2":
+                check_stats(w, g, ref)
+        del w
+        torch.cuda.empty_cache()
+
+
 def test_large_batch_sampled():
     """128 x 16384 bf16 with softcap 30 at full size; the oracle checks sampled
     sequences, every output row is checked for finiteness and boundedness."""
@@ -99,6 +117,8 @@ EDGE = [
     ("head64_bf16_nhd", "bf16", "nhd", 6, 3, 64, (5, 1030), False, 10.0, 3.0),
     ("f32_head128", "f32", "split", 6, 2, 128, (40, 555), True, 0.0, 1.0),
     ("f32_nhd_g16", "f32", "nhd", 16, 1, 64, (3, 1100), False, 5.0, 2.0),
+    ("f32_split_g8_softcap", "f32", "split", 16, 2, 128, (1, 16, 513, 1025), False, 30.0, 4.0),
+    ("f32_split_g1_alibi", "f32", "split", 4, 4, 64, (17, 2100), True, 0.0, 1.0),
     ("alibi_softcap", "bf16", "split", 8, 2, 128, (511, 2049), True, 30.0, 2.0),
 ]
 
@@ -180,6 +200,7 @@ WINDOWS = [
     ("w600_alibi", "f16", "split", 32, 8, 128, (1, 600, 601, 5000), True, 0.0, 600),
     ("w_beyond_len", "f16", "split", 4, 2, 64, (40, 900), False, 0.0, 5000),
     ("w_f32", "f32", "nhd", 6, 2, 128, (300, 1100), True, 0.0, 333),
+    ("w_f32_split", "f32", "split", 8, 2, 64, (15, 512, 1300), True, 0.0, 100),
 ]
 
 
@@ -257,6 +278,8 @@ MULTI = [
     ("q16_mha", "bf16", None, "split", 3, 3, 128, (20, 531), 16, True, 0.0, -1),
     ("q3_f32_alibi_window", "f32", None, "nhd", 8, 2, 128, (100, 700), 3, True, 0.0, 200),
     ("q5_f32_head64", "f32", None, "split", 6, 2, 64, (4, 515), 5, False, 0.0, -1),
+    ("q2_f32_split_group4", "f32", None, "split", 8, 2, 128, (1, 16, 600, 1030), 2,
+     True, 20.0, 300),
     ("q2_e4m3_group8", "bf16", "e4m3", "split", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
     ("q3_e5m2_window", "f16", "e5m2", "split", 6, 2, 64, (33, 1500), 3, False, 30.0, 100),
     ("q2_e4m3_nhd_group8", "bf16", "e4m3", "nhd", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
