@@ -68,24 +68,29 @@ EncodeTiledFn encode_fn() {
 }
 
 // NHD page of one kv head = 16 rows of head_size elements.  The map views a
-// cache as [num_blocks * num_kv_heads * 16 rows][head_size] and moves boxes of
-// 16 rows x 128 bytes (64 16-bit or 32 fp32 elements) with the 128-byte
-// swizzle, so that the kernel's shared-memory reads are free of bank conflicts.
+// cache as 3-D: (E = 128 / elem elements of a row: one 128-byte chunk, the
+// rows [num_blocks * num_kv_heads * 16], the head_size / E chunks of a row),
+// strides (row: head_size * elem bytes, chunk: 128 bytes), and moves a whole
+// page as one box (E, 16, head_size / E): in shared memory the page lands as
+// head_size / E blocks of 16 rows x 128 bytes, each with the 128-byte swizzle,
+// so that the kernel's shared-memory reads are free of bank conflicts -- the
+// layout of one 2-D box per chunk, with one copy instead of two (16-bit) or
+// four (fp32).
 bool make_nhd_map(CUtensorMap* map, const void* base, int64_t rows, int head_size, pa_dtype dt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int elem = dt == PA_DTYPE_F32 ? 4 : 2;
-    cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_size * elem};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / elem), 16};
-    cuuint32_t estr[2] = {1, 1};
+    const int e = 128 / elem;  // elements of a 128-byte chunk
+    cuuint64_t dims[3] = {(cuuint64_t)e, (cuuint64_t)rows, (cuuint64_t)(head_size / e)};
+    cuuint64_t strides[2] = {(cuuint64_t)head_size * elem, 128};
+    cuuint32_t box[3] = {(cuuint32_t)e, 16, (cuuint32_t)(head_size / e)};
+    cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType t = dt == PA_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                   : dt == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = fn(map, t, 2,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

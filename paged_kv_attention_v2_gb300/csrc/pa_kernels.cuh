@@ -423,14 +423,12 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                                 tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
                                 tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
                             } else if constexpr (C::kTensorMap) {
-                                // 16-bit / fp32 NHD: boxes of 16 token rows x 128 bytes
-                                constexpr int EPB = 128 / C::kKvElem;  // elements per box row
+                                // 16-bit / fp32 NHD: the whole page in one box of the
+                                // 3-D view (128-byte chunk of a row, row, chunk index),
+                                // staged as HEAD * elem / 128 blocks of 16 rows x 128 bytes
                                 const int y = (int)(page * kBS);
-#pragma unroll
-                                for (int bx = 0; bx < HEAD / EPB; ++bx) {
-                                    tensor2d_g2s_hint(dk + bx * 2048, tmk, bx * EPB, y, fb, kvpol);
-                                    tensor2d_g2s_hint(dv + bx * 2048, tmv, bx * EPB, y, fb, kvpol);
-                                }
+                                tensor3d_g2s_hint(dk, tmk, 0, y, 0, fb, kvpol);
+                                tensor3d_g2s_hint(dv, tmv, 0, y, 0, fb, kvpol);
                             } else {
                                 bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
                                 bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);

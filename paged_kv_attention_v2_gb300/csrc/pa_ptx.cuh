@@ -112,6 +112,17 @@ __device__ __forceinline__ void tensor2d_g2s_hint(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared, completing on an mbarrier, with an
+// L2 cache policy.
+__device__ __forceinline__ void tensor3d_g2s_hint(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                  uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
