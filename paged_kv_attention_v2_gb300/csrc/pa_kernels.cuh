@@ -176,8 +176,9 @@ struct Cfg {
     static constexpr int kThreads = (NC + 1) * 32;
     // fp32 with one n-tile: the tf32 tensor-core consumer
     static constexpr bool kTf32 = kF32 && NT == 1 && PA_F32_TENSOR;
-    // NHD pages arrive through 2-D tensor maps, swizzled by 128 bytes (except
-    // for fp32 on the CUDA-core consumer, which reads plain rows)
+    // NHD pages arrive through tensor maps with the 128-byte swizzle (3-D for
+    // 16-bit and fp32, 2-D for fp8), except for fp32 on the CUDA-core
+    // consumer, which reads plain rows
     static constexpr bool kTensorMap = (LAYOUT == kNHD) && (!kF32 || kTf32);
     static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
     static constexpr int kScratchFloats = kF32 ? NC * (kBS * kMaxG + kMaxG) : 0;
@@ -731,7 +732,7 @@ __device__ __forceinline__ void zero_v_tail16(uint32_t vpage, int valid, int lan
 }
 
 // Zero the fp32 V entries of tokens >= valid in a staged page: split [d][16
-// tokens], or NHD as HEAD / 32 swizzled boxes of 16 token rows x 128 bytes
+// tokens], or NHD as HEAD / 32 swizzled blocks of 16 token rows x 128 bytes
 // (the swizzle permutes 16-byte chunks within a row, so a row stays one token's).
 template <int LAYOUT, int HEAD>
 __device__ __forceinline__ void zero_v_tail32(uint32_t vpage, int valid, int lane) {

@@ -92,17 +92,9 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
         : "memory");
 }
 
-// 2-D tiled tensor copy global -> shared through a tensor map.  The inner
-// coordinate x times the element size must be a multiple of 16 bytes.
-__device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                             uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
+// 2-D tiled tensor copy global -> shared through a tensor map, completing on
+// an mbarrier, with an L2 cache policy.  The inner coordinate x times the
+// element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tensor2d_g2s_hint(uint32_t dst, const CUtensorMap* map, int x, int y,
                                                   uint32_t bar, uint64_t pol) {
     asm volatile(
