@@ -52,7 +52,7 @@ extern "C" {
  * paged_attention_v2_pytorch.py). */
 #define PA_PARTITION_SIZE 512
 
-/* Tokens per cache page supported by this build. */
+/* Tokens per cache page supported by this library. */
 #define PA_BLOCK_SIZE 16
 
 typedef enum pa_status {
@@ -259,7 +259,7 @@ int32_t pa_partition_size(void);
  * v1 / v2 choice used by PA_MODE_AUTO, as a pure host function (sm_count is
  * the device's multiprocessor count).  The pages decide by tiles against SMs
  * (should_use_paged_v2 in attn_dispatch.py: v2 when num_kv_heads *
- * ceil(seq_len/512) > 2 * SM_COUNT on a 16-SM part); this build retunes that
+ * ceil(seq_len/512) > 2 * SM_COUNT on a 16-SM part); this library retunes that
  * rule for GB300, see pa_decode.cu.  Returns PA_MODE_V1 or PA_MODE_V2.
  */
 int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
