@@ -119,6 +119,7 @@ EDGE = [
     ("f32_nhd_g16", "f32", "nhd", 16, 1, 64, (3, 1100), False, 5.0, 2.0),
     ("f32_split_g8_softcap", "f32", "split", 16, 2, 128, (1, 16, 513, 1025), False, 30.0, 4.0),
     ("f32_split_g1_alibi", "f32", "split", 4, 4, 64, (17, 2100), True, 0.0, 1.0),
+    ("f32_nhd_head64", "f32", "nhd", 8, 2, 64, (5, 515, 1300), True, 20.0, 1.0),
     ("alibi_softcap", "bf16", "split", 8, 2, 128, (511, 2049), True, 30.0, 2.0),
 ]
 
@@ -280,6 +281,8 @@ MULTI = [
     ("q5_f32_head64", "f32", None, "split", 6, 2, 64, (4, 515), 5, False, 0.0, -1),
     ("q2_f32_split_group4", "f32", None, "split", 8, 2, 128, (1, 16, 600, 1030), 2,
      True, 20.0, 300),
+    ("q2_f32_nhd_group4_head64", "f32", None, "nhd", 8, 2, 64, (3, 600, 1030), 2,
+     False, 10.0, 200),
     ("q2_e4m3_group8", "bf16", "e4m3", "split", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
     ("q3_e5m2_window", "f16", "e5m2", "split", 6, 2, 64, (33, 1500), 3, False, 30.0, 100),
     ("q2_e4m3_nhd_group8", "bf16", "e4m3", "nhd", 16, 2, 128, (600, 2049), 2, True, 0.0, -1),
