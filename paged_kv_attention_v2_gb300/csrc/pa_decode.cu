@@ -330,8 +330,8 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     std::memset(&tmv, 0, sizeof tmv);
     const int group_tiles = max_q * group > 8 ? 2 : 1;
     // NHD pages come through tensor maps, except fp32 on the CUDA-core
-    // consumer (two n-tiles), which takes plain bulk copies
-    if (a->layout == PA_LAYOUT_NHD && (a->dtype != PA_DTYPE_F32 || (PA_F32_TENSOR && group_tiles == 1))) {
+    // consumer (built without the tf32 one), which takes plain bulk copies
+    if (a->layout == PA_LAYOUT_NHD && (a->dtype != PA_DTYPE_F32 || PA_F32_TENSOR)) {
         const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
         if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
         const bool ok = kv != PA_KV_SAME

@@ -50,7 +50,10 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #define PA_STAGES_FP8_PAIRS 8  // ring stages, fp8 NHD caches with one n-tile: two pages each
 #endif
 #ifndef PA_STAGES_F32
-#define PA_STAGES_F32 4        // ring stages, fp32 caches
+#define PA_STAGES_F32 4        // ring stages, fp32 caches, one n-tile (two CTAs per SM)
+#endif
+#ifndef PA_STAGES_F32_2T
+#define PA_STAGES_F32_2T 8     // ring stages, fp32 caches, two n-tiles (one CTA per SM)
 #endif
 #ifndef PA_CONSUMER_WARPS
 #define PA_CONSUMER_WARPS 4    // consumer warps per CTA
@@ -62,7 +65,7 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 #define PA_REDUCE_WARP_MAX_PARTS 64  // warp-per-row reduce up to this many partitions per row
 #endif
 #ifndef PA_F32_TENSOR
-#define PA_F32_TENSOR 1        // fp32, split layout, one n-tile: three-term tf32 tensor-core path
+#define PA_F32_TENSOR 1        // fp32 inputs: three-term tf32 tensor-core consumer (0: CUDA-core FMAs)
 #endif
 #ifndef PA_MAX_CTAS_PER_SM
 #define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
@@ -174,14 +177,14 @@ struct Cfg {
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
-    // fp32 with one n-tile: the tf32 tensor-core consumer
-    static constexpr bool kTf32 = kF32 && NT == 1 && PA_F32_TENSOR;
+    // fp32: the tf32 tensor-core consumer
+    static constexpr bool kTf32 = kF32 && PA_F32_TENSOR;
     // NHD pages arrive through tensor maps with the 128-byte swizzle (3-D for
     // 16-bit and fp32, 2-D for fp8), except for fp32 on the CUDA-core
     // consumer, which reads plain rows
     static constexpr bool kTensorMap = (LAYOUT == kNHD) && (!kF32 || kTf32);
     static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
-    static constexpr int kScratchFloats = kF32 ? NC * (kBS * kMaxG + kMaxG) : 0;
+    static constexpr int kScratchFloats = (kF32 && !kTf32) ? NC * (kBS * kMaxG + kMaxG) : 0;
 
     static constexpr int oRing = 0;
     static constexpr int oQ = oRing + STAGES * kStageBytes;
@@ -1408,26 +1411,30 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
     }
 }
 
-// fp32 inputs, one n-tile: tensor cores with each fp32 operand carried as two
-// tf32 terms (hi + lo) and three MMAs per product (hi.hi + hi.lo + lo.hi),
-// which keeps each product to ~2^-20 relative, well inside the fp32 result's
-// error budget.  Tokens on M, query rows on N for Q.K^T; head dims on M, rows
-// on N for P.V, as in the 16-bit consumer.  P moves from the S^T fragment to
-// the B fragment with shuffles (there is no 32-bit movmatrix).
+// fp32 inputs: tensor cores with each fp32 operand carried as two tf32 terms
+// (hi + lo) and three MMAs per product (hi.hi + hi.lo + lo.hi), which keeps
+// each product to ~2^-20 relative, well inside the fp32 result's error budget.
+// Tokens on M, query rows on N for Q.K^T (NT n-tiles of 8 rows); head dims on
+// M, rows on N for P.V, as in the 16-bit consumer.  P moves from the S^T
+// fragment to the B fragment with shuffles (there is no 32-bit movmatrix).
+// One n-tile keeps Q split in registers for the whole tile; two keep the raw
+// fp32 words (64 registers at head size 128 instead of 128) and split them at
+// each use.
 //
 // Shared-memory reads.  Split pages: K [d/4][16 tokens][4] gives each k-step's
 // A fragment as one ldmatrix.x4; V [d][16 tokens] likewise (its 64-byte rows
-// cost 4-way bank conflicts whatever the order).  NHD pages (HEAD / 32 boxes
+// cost 4-way bank conflicts whatever the order).  NHD pages (HEAD / 32 blocks
 // of 16 token rows x 128 bytes, 16-byte chunks swizzled by token % 8): K by
 // ldmatrix.x4 as well; V^T needs a transpose that ldmatrix does not do for
 // 32-bit elements, so its fragments are single-word loads, with the k-step's
 // tokens taken in the order 0, 2, 4, 6 | 1, 3, 5, 7 (k-index t -> token 2t, t + 4
 // -> 2t + 1), which puts the 32 words of each load in 32 distinct banks; the
 // P^T fragment follows the same order.
-template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
+template <class C, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lane) {
     constexpr int KT = HEAD / 8;   // k-steps of Q.K^T (8 head dims each)
     constexpr int MT = HEAD / 16;  // m-tiles of P.V (16 head dims each)
+    constexpr bool QSPLIT = NT == 1;  // Q held split for the whole tile
     const int G = p.group;
     const int r = lane >> 2, cq = lane & 3;
     const bool has_alibi = p.alibi != nullptr;
@@ -1446,52 +1453,71 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
         const int qn = C::kMQ ? d.qn : 1;
         const int GE = qn * G;  // rows of N: query token v / G, head kvh * G + v % G
 
-        // Q as B fragments (k = head dim 8kk + cq / + 4, n = row r), hi and lo
-        uint32_t qh[KT][2], ql[KT][2];
+        // Q as B fragments (k = head dim 8kk + cq / + 4, n = row nt * 8 + r):
+        // hi and lo terms (one n-tile) or the raw words (two)
+        uint32_t qa[NT][KT][2];
+        uint32_t qlo[QSPLIT ? KT : 1][2];
         {
             const float* q = reinterpret_cast<const float*>(
                 __cvta_shared_to_generic(sm.q + slot * C::kQBytes));
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint32_t x = r < GE ? __float_as_uint(q[r * HEAD + kk * 8 + cq + 4 * e]) : 0u;
-                    split_tf32(x, qh[kk][e], ql[kk][e]);
-                }
+                for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int row = nt * 8 + r;
+                        const uint32_t x =
+                            row < GE ? __float_as_uint(q[row * HEAD + kk * 8 + cq + 4 * e]) : 0u;
+                        if constexpr (QSPLIT)
+                            split_tf32(x, qa[nt][kk][e], qlo[kk][e]);
+                        else
+                            qa[nt][kk][e] = x;
+                    }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // Q and descriptor are in registers
 
-        float sl[2];
-        int klo[2], khi[2];  // key range of this lane's rows within the tile
+        float sl[NT][2];
+        int klo[NT][2], khi[NT][2];  // key range of this lane's rows within the tile
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int v = 2 * cq + e;
-            sl[e] = (has_alibi && v < GE) ? __ldg(p.alibi + d.kvh * G + v % G) : 0.f;
-            int lo = d.tok_begin, hi = d.tok_end - 1;
-            if (C::kMQ && v < GE) {
-                const int pos = d.len - qn + v / G;
-                hi = min(hi, pos);
-                lo = max(lo, window_lo_at(p, pos));
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int v = nt * 8 + 2 * cq + e;
+                sl[nt][e] = (has_alibi && v < GE) ? __ldg(p.alibi + d.kvh * G + v % G) : 0.f;
+                int lo = d.tok_begin, hi = d.tok_end - 1;
+                if (C::kMQ && v < GE) {
+                    const int pos = d.len - qn + v / G;
+                    hi = min(hi, pos);
+                    lo = max(lo, window_lo_at(p, pos));
+                }
+                klo[nt][e] = lo;
+                khi[nt][e] = hi;
             }
-            klo[e] = lo;
-            khi[e] = hi;
-        }
         const int hi_all = C::kMQ ? min(d.tok_end - 1, d.len - qn) : d.tok_end - 1;
         const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;
 
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-        float acc[MT][4];
+        float m[NT][2], l[NT][2];
+        float acc[MT][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+        }
 
         const int npages = tile_pages(d.tok_begin, d.tok_end);
         const int page0 = d.tok_begin / kBS * kBS;
         // ldmatrix row of this lane: matrix j = lane / 8, row i = lane % 8
         const int lj = lane >> 3, li = lane & 7;
+        // P^T k-index cq holds token cq (split) or 2cq (NHD), cq + 4 token cq + 4 or 2cq + 1
+        const int tk0 = LAYOUT == kSplit ? cq : 2 * cq, tk1 = LAYOUT == kSplit ? cq + 4 : 2 * cq + 1;
+        const int src0 = 4 * tk0 + (r >> 1), src1 = 4 * tk1 + (r >> 1);
         for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
@@ -1513,8 +1539,18 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
 
             // S^T[token][row] = K . Q^T; the four 8 x 4 blocks (tokens 0-7 /
             // 8-15, head dims 8kk..+3 / +4..+7) of a k-step are its A fragment,
-            // one ldmatrix.x4 (this lane's row: block lj, row li)
-            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+            // one ldmatrix.x4 (this lane's row: block lj, row li).  Each
+            // k-step's three products go to a fresh accumulator that is then
+            // added with a rounded fp32 add, so that the tensor core's own
+            // accumulation (which need not round to nearest) never carries a
+            // sum across the k-steps of a page or, for P.V below, the pages of
+            // a tile: without it a 24-head, group-12 fp32 case missed the 1e-5
+            // tolerance even with the rounded split.
+            float s[NT][4], s2[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a[4], ah[4], al[4];
@@ -1527,69 +1563,86 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
                 ldsm_x4(ka, a[0], a[1], a[2], a[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) split_tf32(a[e], ah[e], al[e]);
-                float (&sa)[4] = (kk & 1) ? s2 : s;
-                mma_1688_tf32(sa, al[0], al[1], al[2], al[3], qh[kk][0], qh[kk][1]);
-                mma_1688_tf32(sa, ah[0], ah[1], ah[2], ah[3], ql[kk][0], ql[kk][1]);
-                mma_1688_tf32(sa, ah[0], ah[1], ah[2], ah[3], qh[kk][0], qh[kk][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t bh[2], bl[2];
+                    if constexpr (QSPLIT) {
+                        bh[0] = qa[nt][kk][0];
+                        bh[1] = qa[nt][kk][1];
+                        bl[0] = qlo[kk][0];
+                        bl[1] = qlo[kk][1];
+                    } else {
+                        split_tf32(qa[nt][kk][0], bh[0], bl[0]);
+                        split_tf32(qa[nt][kk][1], bh[1], bl[1]);
+                    }
+                    float t[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_1688_tf32(t, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+                    mma_1688_tf32(t, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+                    mma_1688_tf32(t, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+                    float (&sa)[4] = (kk & 1) ? s2[nt] : s[nt];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sa[e] = __fadd_rn(sa[e], t[e]);
+                }
             }
 
-            float z[4];
+            // logits, online softmax, P^T as B fragments (hi and lo) per n-tile
+            uint32_t pbh[NT][2][2], pbl[NT][2][2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = (s[e] + s2[e]) * p.scale;
-                if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
-                if (has_alibi) v += sl[e & 1] * (float)(tok0 + r + ((e >> 1) << 3) - origin);
-                z[e] = v;
-            }
-            if (edge) {
-                const int t0 = tok0 + r, t1 = t0 + 8;
-                if (t0 < klo[0] || t0 > khi[0]) z[0] = -INFINITY;
-                if (t0 < klo[1] || t0 > khi[1]) z[1] = -INFINITY;
-                if (t1 < klo[0] || t1 > khi[0]) z[2] = -INFINITY;
-                if (t1 < klo[1] || t1 > khi[1]) z[3] = -INFINITY;
-            }
-            float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+            for (int nt = 0; nt < NT; ++nt) {
+                float z[4];
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-            const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
-            const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = exp2f((m[0] - mr0) * kLog2e);
-            const float al1 = exp2f((m[1] - mr1) * kLog2e);
-            m[0] = mn0;
-            m[1] = mn1;
-            float pv[4];
-            pv[0] = exp2f((z[0] - mr0) * kLog2e);  // (token r,     row 2cq)
-            pv[1] = exp2f((z[1] - mr1) * kLog2e);  // (token r,     row 2cq + 1)
-            pv[2] = exp2f((z[2] - mr0) * kLog2e);  // (token r + 8, row 2cq)
-            pv[3] = exp2f((z[3] - mr1) * kLog2e);  // (token r + 8, row 2cq + 1)
-            l[0] = l[0] * al0 + (pv[0] + pv[2]);
-            l[1] = l[1] * al1 + (pv[1] + pv[3]);
+                for (int e = 0; e < 4; ++e) {
+                    float v = (s[nt][e] + s2[nt][e]) * p.scale;
+                    if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                    if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + r + ((e >> 1) << 3) - origin);
+                    z[e] = v;
+                }
+                if (edge) {
+                    const int t0 = tok0 + r, t1 = t0 + 8;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                }
+                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                acc[mt][0] *= al0;
-                acc[mt][1] *= al1;
-                acc[mt][2] *= al0;
-                acc[mt][3] *= al1;
-            }
-            // B fragments of P^T for k-steps ks = 0, 1 (tokens 8ks..8ks+7):
-            // b0 = P[row r][token 8ks + cq], b1 = P[row r][token 8ks + cq + 4],
-            // held by lanes (token % 8, row / 2), element by row parity and ks
-            uint32_t pbh[2][2], pbl[2][2];
-            // k-index cq holds token cq (split) or 2cq (NHD), cq + 4 token cq + 4 or 2cq + 1
-            const int tk0 = LAYOUT == kSplit ? cq : 2 * cq, tk1 = LAYOUT == kSplit ? cq + 4 : 2 * cq + 1;
-            const int src0 = 4 * tk0 + (r >> 1), src1 = 4 * tk1 + (r >> 1);
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
+                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
+                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+                float pv[4];
+                pv[0] = exp2f((z[0] - mr0) * kLog2e);  // (token r,     row 2cq)
+                pv[1] = exp2f((z[1] - mr1) * kLog2e);  // (token r,     row 2cq + 1)
+                pv[2] = exp2f((z[2] - mr0) * kLog2e);  // (token r + 8, row 2cq)
+                pv[3] = exp2f((z[3] - mr1) * kLog2e);  // (token r + 8, row 2cq + 1)
+                l[nt][0] = l[nt][0] * al0 + (pv[0] + pv[2]);
+                l[nt][1] = l[nt][1] * al1 + (pv[1] + pv[3]);
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const float e0 = __shfl_sync(0xffffffffu, pv[2 * ks], src0);
-                const float o0 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src0);
-                const float e1 = __shfl_sync(0xffffffffu, pv[2 * ks], src1);
-                const float o1 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src1);
-                split_tf32(__float_as_uint((r & 1) ? o0 : e0), pbh[ks][0], pbl[ks][0]);
-                split_tf32(__float_as_uint((r & 1) ? o1 : e1), pbh[ks][1], pbl[ks][1]);
+                for (int mt = 0; mt < MT; ++mt) {
+                    acc[mt][nt][0] *= al0;
+                    acc[mt][nt][1] *= al1;
+                    acc[mt][nt][2] *= al0;
+                    acc[mt][nt][3] *= al1;
+                }
+                // B fragments of P^T for k-steps ks = 0, 1 (tokens 8ks..8ks+7):
+                // b0 = P[row r][token 8ks + tk0], b1 = P[row r][token 8ks + tk1],
+                // held by lanes (token % 8, row / 2), element by row parity and ks
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float e0 = __shfl_sync(0xffffffffu, pv[2 * ks], src0);
+                    const float o0 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src0);
+                    const float e1 = __shfl_sync(0xffffffffu, pv[2 * ks], src1);
+                    const float o1 = __shfl_sync(0xffffffffu, pv[2 * ks + 1], src1);
+                    split_tf32(__float_as_uint((r & 1) ? o0 : e0), pbh[nt][ks][0], pbl[nt][ks][0]);
+                    split_tf32(__float_as_uint((r & 1) ? o1 : e1), pbh[nt][ks][1], pbl[nt][ks][1]);
+                }
             }
 
             // acc^T[head dim][row] += V^T . P^T; A fragment of (m-tile mt,
@@ -1618,33 +1671,42 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) split_tf32(a[e], ah[e], al[e]);
-                    mma_1688_tf32(acc[mt], al[0], al[1], al[2], al[3], pbh[ks][0], pbh[ks][1]);
-                    mma_1688_tf32(acc[mt], ah[0], ah[1], ah[2], ah[3], pbl[ks][0], pbl[ks][1]);
-                    mma_1688_tf32(acc[mt], ah[0], ah[1], ah[2], ah[3], pbh[ks][0], pbh[ks][1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_1688_tf32(t, al[0], al[1], al[2], al[3], pbh[nt][ks][0], pbh[nt][ks][1]);
+                        mma_1688_tf32(t, ah[0], ah[1], ah[2], ah[3], pbl[nt][ks][0], pbl[nt][ks][1]);
+                        mma_1688_tf32(t, ah[0], ah[1], ah[2], ah[3], pbh[nt][ks][0], pbh[nt][ks][1]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[mt][nt][e] = __fadd_rn(acc[mt][nt][e], t[e]);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + st * 8);
         }
 
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
-            l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
-        }
         float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
-        const int h0 = 2 * cq;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int d0 = mt * 16 + r;
-            mw[h0 * C::kMergeStride + d0] = acc[mt][0];
-            mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][1];
-            mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][2];
-            mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][3];
-        }
-        if (r == 0) {
-            sm.ml[warp * C::kMaxG + h0] = make_float2(m[0], l[0]);
-            sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[1], l[1]);
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], o);
+                l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], o);
+            }
+            const int h0 = nt * 8 + 2 * cq;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int d0 = mt * 16 + r;
+                mw[h0 * C::kMergeStride + d0] = acc[mt][nt][0];
+                mw[(h0 + 1) * C::kMergeStride + d0] = acc[mt][nt][1];
+                mw[h0 * C::kMergeStride + d0 + 8] = acc[mt][nt][2];
+                mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
+            }
+            if (r == 0) {
+                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+            }
         }
         if (!consumer_sync(sm, mphase, lane)) {
             report(p, PA_DEVERR_TIMEOUT);
@@ -1853,10 +1915,13 @@ __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane
 
 // Two n-tiles hold 16 rows of accumulators (~200 registers uncapped), and the
 // fp32 tensor-core consumer holds Q as two tf32 terms (~213): cap them so that
-// two CTAs share an SM, as they do for one n-tile of 16-bit inputs.
+// two CTAs share an SM, as they do for one n-tile of 16-bit inputs.  fp32 with
+// two n-tiles fills an SM's shared memory with one CTA (16 KB stages): no cap.
 template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, bool MQ>
 __global__ void __launch_bounds__((NC + 1) * 32,
-                                  (NT > 1 || std::is_same<T, float>::value) ? 2 : PA_MIN_CTAS_PER_SM)
+                                  (std::is_same<T, float>::value && NT > 1)
+                                      ? 1
+                                      : ((NT > 1 || std::is_same<T, float>::value) ? 2 : PA_MIN_CTAS_PER_SM))
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
@@ -1910,7 +1975,7 @@ __global__ void __launch_bounds__((NC + 1) * 32,
         producer<C, HEAD, STAGES>(p, sm, &tmk, &tmv, lane);
     } else if constexpr (C::kF32) {
         if constexpr (C::kTf32)
-            consumer_tf32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+            consumer_tf32<C, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
         else
             consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
     } else {

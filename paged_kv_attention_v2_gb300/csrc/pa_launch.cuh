@@ -36,7 +36,7 @@ constexpr int kMaxDevices = 64;
 // CTAs; the separate reduce kernel spreads them over the whole GPU instead.
 template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
-    constexpr int STAGES = std::is_same<T, float>::value ? PA_STAGES_F32
+    constexpr int STAGES = std::is_same<T, float>::value ? (NT == 1 ? PA_STAGES_F32 : PA_STAGES_F32_2T)
                            : (KV == kKvSame ? PA_STAGES_16BIT
                                             : (NT == 1 && LAYOUT == kNHD ? PA_STAGES_FP8_PAIRS
                                                                          : PA_STAGES_FP8));

@@ -120,6 +120,8 @@ EDGE = [
     ("f32_split_g8_softcap", "f32", "split", 16, 2, 128, (1, 16, 513, 1025), False, 30.0, 4.0),
     ("f32_split_g1_alibi", "f32", "split", 4, 4, 64, (17, 2100), True, 0.0, 1.0),
     ("f32_nhd_head64", "f32", "nhd", 8, 2, 64, (5, 515, 1300), True, 20.0, 1.0),
+    ("f32_group16_split", "f32", "split", 32, 2, 128, (1, 700, 2100), True, 10.0, 1.0),
+    ("f32_group12_nhd_head64", "f32", "nhd", 24, 2, 64, (17, 1500), False, 0.0, 3.0),
     ("alibi_softcap", "bf16", "split", 8, 2, 128, (511, 2049), True, 30.0, 2.0),
 ]
 
