@@ -1722,7 +1722,9 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
     }
 }
 
-// fp32 inputs: CUDA-core arithmetic (tensor cores would round to tf32).
+// fp32 inputs on CUDA-core FMAs: the consumer of builds with PA_F32_TENSOR=0
+// (the default build takes consumer_tf32), kept as the plain-arithmetic
+// alternative to the three-term tf32 products.
 template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane) {
     // C::kMaxG rows (8 or 16): a row set of 8 keeps two CTAs per SM
