@@ -212,6 +212,28 @@ def test_length_aware_dispatch():
         pa.choose_mode(4, 2, 4096, sm, np.full(3, 4096))
 
 
+def test_length_aware_dispatch_edges(lib):
+    """Degenerate inputs of the host rule: no usable lengths or SM count fall
+    back to v2; lengths outside [0, max_seq_len] are clamped before the load
+    balance is judged (an all-empty batch is trivially even)."""
+    import numpy as np
+    sm = 152
+    lens = np.full(128, 16384, dtype=np.int32)
+    ptr = lens.ctypes.data
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, 0, ptr) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode_for_lengths(0, 8, 16384, sm, ptr) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, None) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode_for_lengths(128, 8, 300, sm, None) == _abi.PA_MODE_V1
+    zeros = np.zeros(128, dtype=np.int32)
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, zeros.ctypes.data) == _abi.PA_MODE_V1
+    # lengths beyond max_seq_len count as max_seq_len, negative ones as 0
+    over = np.full(128, 1 << 30, dtype=np.int32)
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, over.ctypes.data) == _abi.PA_MODE_V1
+    mixed = lens.copy()
+    mixed[::2] = -5  # every other sequence empty: the round-robin load is uneven
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, mixed.ctypes.data) == _abi.PA_MODE_V2
+
+
 def test_workspace_bytes_and_partition_size(lib):
     assert lib.pa_partition_size() == 512
     # 4 x 100000 tokens, 28 heads, d 128: 196 partitions per row
