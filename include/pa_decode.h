@@ -229,27 +229,43 @@ pa_status pa_decode(const pa_decode_args* args, void* stream);
  *    rows * num_heads * P * (head_size + 2) > PA_STATIC_WORKSPACE_FLOATS
  *    (rows = num_seqs, or num_query_tokens with query_start),
  *    P = pa_max_num_partitions(max_seq_len); other errors as pa_decode.
- *  - The first call on a device looks up the array's address on that device
- *    (the device must be current); make that first call before any stream
- *    capture.
+ *  - The array used is the one of the CURRENT device (cudaGetDevice): make
+ *    the device of `stream` and of the tensors current before the call.  The
+ *    first call on a device looks up the array's address on that device; make
+ *    that first call before any stream capture.  The address is cached for the
+ *    life of the process: after a cudaDeviceReset of that device it is no
+ *    longer valid, so do not call this entry point again on it.
  *  - All calls on a device share the array, which keeps the last call's
  *    contents; nothing in it needs to start at zero.  Calls whose kernels
  *    overlap on the GPU (unordered streams) race on it: order them.
  */
 pa_status pa_decode_static_workspace(const pa_decode_args* args, void* stream);
 
-/* ceil(max_seq_len / PA_PARTITION_SIZE), at least 1 (workspace partition stride). */
+/* ceil(max_seq_len / PA_PARTITION_SIZE), at least 1: the max_num_partitions
+ * of "paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2
+ * implementation" (the third dimension of exp_sums / max_logits / tmp_output
+ * in the signature of paged_attention_v2_pytorch; a sequence of seq_len
+ * tokens uses the first ceil(seq_len / 512) of them).  It is the partition
+ * stride of the workspace rows.  Pure host function; no error case
+ * (max_seq_len <= 0 gives 1). */
 int32_t pa_max_num_partitions(int32_t max_seq_len);
 
-/* Element counts of the v2 workspace: *stats_elems for each of exp_sums and
- * max_logits, *tmp_elems for tmp_out.  num_seqs is the row count: pass
+/* Element counts of the v2 workspace, from the shapes in the signature of
+ * paged_attention_v2_pytorch ("paged_attention_v2_pytorch.py -- BI-V100
+ * PagedAttention V2 implementation"): exp_sums and max_logits
+ * [num_seqs][num_heads][max_num_partitions], tmp_output
+ * [num_seqs][num_heads][max_num_partitions][head_size].  *stats_elems gets
+ * the count of each of exp_sums and max_logits, *tmp_elems that of tmp_out
+ * (either pointer may be NULL).  num_seqs is the row count: pass
  * num_query_tokens when query_start gives several tokens per sequence.
- * Returns PA_ERR_INVALID_ARG on bad sizes. */
+ * Pure host function.  Returns PA_ERR_INVALID_ARG on negative sizes or a
+ * non-positive num_heads / head_size, writing nothing. */
 pa_status pa_workspace_elems(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                              int32_t max_seq_len, int64_t* stats_elems, int64_t* tmp_elems);
 
-/* Bytes of the whole v2 workspace (exp_sums + max_logits + tmp_out, fp32) for
- * `rows` query rows; 0 on bad sizes. */
+/* Bytes of the whole fp32 v2 workspace (the same shapes: exp_sums +
+ * max_logits + tmp_out, as in pa_workspace_elems) for `rows` query rows.
+ * Pure host function; returns 0 on the sizes pa_workspace_elems rejects. */
 size_t pa_workspace_bytes(int32_t rows, int32_t num_heads, int32_t head_size, int32_t max_seq_len);
 
 /* Tokens per partition of the v2 workspace (PA_PARTITION_SIZE). */

@@ -48,8 +48,7 @@
  *    t >= seq_len - 1 - window_left (window_right cannot matter: no key lies
  *    after the query).  Partitions with no key inside the window are unused.
  *
- * Readings where the pages are silent or inconsistent (each is listed in
- * the design doc as well):
+ * Readings where the pages are silent or inconsistent:
  *  - tmp_p is stored normalised by e_p (the reduce on the page is only equal
  *    to a full softmax with that reading).
  *  - softcap (the `softcap` field of AttnDispatchConfig, formula not printed):

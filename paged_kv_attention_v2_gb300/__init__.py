@@ -182,7 +182,9 @@ def pa_decode(out, query, key_cache, value_cache, block_tables, seq_lens, *, str
     if stream is None:
         stream = torch.cuda.current_stream(query.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    st = library().pa_decode(ctypes.byref(args), ctypes.c_void_p(handle))
+    # the library sizes its grid for (and caches attributes of) the current device
+    with torch.cuda.device(query.device):
+        st = library().pa_decode(ctypes.byref(args), ctypes.c_void_p(handle))
     if st != _abi.PA_OK:
         raise PaDecodeError(st)
 
@@ -206,6 +208,8 @@ def pa_decode_static_workspace(out, query, key_cache, value_cache, block_tables,
     if stream is None:
         stream = torch.cuda.current_stream(query.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    st = library().pa_decode_static_workspace(ctypes.byref(args), ctypes.c_void_p(handle))
+    # the array used is the current device's: make the tensors' device current
+    with torch.cuda.device(query.device):
+        st = library().pa_decode_static_workspace(ctypes.byref(args), ctypes.c_void_p(handle))
     if st != _abi.PA_OK:
         raise PaDecodeError(st)

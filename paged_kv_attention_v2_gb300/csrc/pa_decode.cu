@@ -329,9 +329,8 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     std::memset(&tmk, 0, sizeof tmk);
     std::memset(&tmv, 0, sizeof tmv);
     const int group_tiles = max_q * group > 8 ? 2 : 1;
-    // NHD pages come through tensor maps, except fp32 on the CUDA-core
-    // consumer (built without the tf32 one), which takes plain bulk copies
-    if (a->layout == PA_LAYOUT_NHD && (a->dtype != PA_DTYPE_F32 || PA_F32_TENSOR)) {
+    // NHD pages come through tensor maps
+    if (a->layout == PA_LAYOUT_NHD) {
         const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
         if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
         const bool ok = kv != PA_KV_SAME
@@ -353,7 +352,6 @@ pa_status pa_decode(const pa_decode_args* a, void* stream) {
     la.head_size = a->head_size;
     la.ev_begin = a->event_main_begin;
     la.ev_end = a->event_main_end;
-    la.grid_override = 0;
 
     cudaError_t e;
     const int kvk = kv == PA_KV_FP8_E4M3 ? pa::kKvE4M3 : pa::kKvE5M2;

@@ -39,37 +39,17 @@ constexpr int kKvSame = 0;      // same 16-bit / 32-bit type as the query
 constexpr int kKvE4M3 = 1;      // fp8 E4M3
 constexpr int kKvE5M2 = 2;      // fp8 E5M2
 
-// Build-time shape of the partition kernel (overridable with -D for sweeps).
-#ifndef PA_STAGES_16BIT
-#define PA_STAGES_16BIT 8      // ring stages (one 16-token page of K and V each), 16-bit caches
-#endif
-#ifndef PA_STAGES_FP8
-#define PA_STAGES_FP8 12       // ring stages, fp8 caches, one page each (three CTAs per SM fit)
-#endif
-#ifndef PA_STAGES_FP8_PAIRS
-#define PA_STAGES_FP8_PAIRS 8  // ring stages, fp8 NHD caches with one n-tile: two pages each
-#endif
-#ifndef PA_STAGES_F32
-#define PA_STAGES_F32 4        // ring stages, fp32 caches, one n-tile (two CTAs per SM)
-#endif
-#ifndef PA_STAGES_F32_2T
-#define PA_STAGES_F32_2T 8     // ring stages, fp32 caches, two n-tiles (one CTA per SM)
-#endif
-#ifndef PA_CONSUMER_WARPS
-#define PA_CONSUMER_WARPS 4    // consumer warps per CTA
-#endif
-#ifndef PA_MIN_CTAS_PER_SM
-#define PA_MIN_CTAS_PER_SM 1   // __launch_bounds__ minimum resident CTAs
-#endif
-#ifndef PA_REDUCE_WARP_MAX_PARTS
-#define PA_REDUCE_WARP_MAX_PARTS 64  // warp-per-row reduce up to this many partitions per row
-#endif
-#ifndef PA_F32_TENSOR
-#define PA_F32_TENSOR 1        // fp32 inputs: three-term tf32 tensor-core consumer (0: CUDA-core FMAs)
-#endif
-#ifndef PA_MAX_CTAS_PER_SM
-#define PA_MAX_CTAS_PER_SM 0   // persistent grid: CTAs per SM (0 = as many as fit)
-#endif
+// Shape of the partition kernel.  Ring stages per cache type: one 16-token
+// page of K and V each, except fp8 NHD tiles of one n-tile (two pages each);
+// fp8 split pages take 12 stages so that three CTAs share an SM, fp32 pages
+// with two n-tiles 8 stages of 16 KB (one CTA per SM).
+constexpr int kStages16 = 8;       // 16-bit caches
+constexpr int kStagesFp8 = 12;     // fp8 caches, one page per stage
+constexpr int kStagesFp8Pairs = 8; // fp8 NHD caches with one n-tile: two pages per stage
+constexpr int kStagesF32 = 4;      // fp32 caches, one n-tile (two CTAs per SM)
+constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
+constexpr int kConsumerWarps = 4;  // consumer warps per CTA
+constexpr int kReduceWarpMaxParts = 64;  // warp-per-row reduce up to this many partitions per row
 
 constexpr int kReduceWarpsPerCta = 8;  // warp-per-row reduce: rows per CTA
 
@@ -177,21 +157,16 @@ struct Cfg {
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
     static constexpr int kThreads = (NC + 1) * 32;
-    // fp32: the tf32 tensor-core consumer
-    static constexpr bool kTf32 = kF32 && PA_F32_TENSOR;
     // NHD pages arrive through tensor maps with the 128-byte swizzle (3-D for
-    // 16-bit and fp32, 2-D for fp8), except for fp32 on the CUDA-core
-    // consumer, which reads plain rows
-    static constexpr bool kTensorMap = (LAYOUT == kNHD) && (!kF32 || kTf32);
+    // 16-bit and fp32, 2-D for fp8)
+    static constexpr bool kTensorMap = LAYOUT == kNHD;
     static_assert(KV == kKvSame || !kF32, "fp8 caches: 16-bit query");
-    static constexpr int kScratchFloats = (kF32 && !kTf32) ? NC * (kBS * kMaxG + kMaxG) : 0;
 
     static constexpr int oRing = 0;
     static constexpr int oQ = oRing + STAGES * kStageBytes;
     static constexpr int oMerge = oQ + kTD * kQBytes;
     static constexpr int oML = oMerge + NC * kMaxG * kMergeStride * 4;
-    static constexpr int oScratch = oML + NC * kMaxG * 8;
-    static constexpr int oDesc = oScratch + kScratchFloats * 4;
+    static constexpr int oDesc = oML + NC * kMaxG * 8;
     static constexpr int oBar = (oDesc + kTD * (int)sizeof(TileDesc) + 7) & ~7;
     static constexpr int oAbort = oBar + (2 * STAGES + 2 * kTD + 1) * 8;
     static constexpr int kSmemBytes = oAbort + 16 + 1024;  // + slack for 1024-B alignment
@@ -213,7 +188,6 @@ struct Smem {
     uint32_t q;          // shared address of Q slot 0
     float* merge;
     float2* ml;
-    float* scratch;
     TileDesc* desc;
     uint32_t full, empty, td_full, td_empty;  // shared addresses of barrier arrays
     uint32_t merge_bar;  // consumer warps: partial states written / epilogue reads done
@@ -1722,197 +1696,6 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
     }
 }
 
-// fp32 inputs on CUDA-core FMAs: the consumer of builds with PA_F32_TENSOR=0
-// (the default build takes consumer_tf32), kept as the plain-arithmetic
-// alternative to the three-term tf32 products.
-template <class C, int HEAD, int LAYOUT, int STAGES, int NC>
-__device__ void consumer_f32(const Params& p, const Smem& sm, int warp, int lane) {
-    // C::kMaxG rows (8 or 16): a row set of 8 keeps two CTAs per SM
-    constexpr int MAXG = C::kMaxG, HPL = MAXG / 2, DPL = HEAD / 32;
-    const int G = p.group;
-    const int t = lane & 15, hs = lane >> 4;  // Q.K^T: lane = (token t, heads hs, hs+2, ...)
-    const bool has_alibi = p.alibi != nullptr;
-    const bool has_cap = p.softcap > 0.f;
-    float* pw = sm.scratch + warp * (kBS * MAXG + MAXG);  // p[head][token], alpha[head]
-    uint32_t gbase = 0;
-    uint32_t mphase = 0;
-    for (int k = 0;; ++k) {
-        const int slot = k % C::kTD;
-        if (!warp_wait(sm.td_full + slot * 8, (k / C::kTD) & 1, sm.abort, sm.wait_ns)) {
-            report(p, PA_DEVERR_TIMEOUT);
-            *sm.abort = 1;
-            return;
-        }
-        const TileDesc d = sm.desc[slot];
-        if (d.flags & kTileStop) return;
-        const float* q = reinterpret_cast<const float*>(
-            __cvta_shared_to_generic(sm.q + slot * C::kQBytes));
-        const int qn = C::kMQ ? d.qn : 1;
-        const int GE = qn * G;  // rows: query token h / G, head kvh * G + h % G
-        float sl[HPL];
-        int klo[HPL], khi[HPL];  // key range of each row within the tile
-#pragma unroll
-        for (int i = 0; i < HPL; ++i) {
-            const int h = hs + 2 * i;
-            sl[i] = (has_alibi && h < GE) ? __ldg(p.alibi + d.kvh * G + h % G) : 0.f;
-            int lo = d.tok_begin, hi = d.tok_end - 1;
-            if (C::kMQ && h < GE) {
-                const int pos = d.len - qn + h / G;
-                hi = min(hi, pos);
-                lo = max(lo, window_lo_at(p, pos));
-            }
-            klo[i] = lo;
-            khi[i] = hi;
-        }
-        const int origin = d.tok_end - 1;
-        float m[HPL], l[HPL], acc[MAXG][DPL];
-#pragma unroll
-        for (int i = 0; i < HPL; ++i) {
-            m[i] = -INFINITY;
-            l[i] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < MAXG; ++h)
-#pragma unroll
-            for (int c = 0; c < DPL; ++c) acc[h][c] = 0.f;
-
-        const int npages = tile_pages(d.tok_begin, d.tok_end);
-        const int page0 = d.tok_begin / kBS * kBS;  // first token of the tile's first page
-        for (int j = warp; j < npages; j += NC) {
-            const uint32_t gg = gbase + (uint32_t)j;
-            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
-            if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
-                report(p, PA_DEVERR_TIMEOUT);
-                *sm.abort = 1;
-                return;
-            }
-            const float* kp = reinterpret_cast<const float*>(
-                __cvta_shared_to_generic(sm.ring + st * C::kStageBytes));
-            float* vp = const_cast<float*>(kp) + kBS * HEAD;
-            const int tok0 = page0 + j * kBS;
-            const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
-            if (valid < kBS) {
-                if constexpr (LAYOUT == kSplit) {
-                    for (int dd = lane; dd < HEAD; dd += 32)
-                        for (int tt = valid; tt < kBS; ++tt) vp[dd * kBS + tt] = 0.f;
-                } else {
-                    for (int i = lane; i < (kBS - valid) * HEAD; i += 32) vp[valid * HEAD + i] = 0.f;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            float z[HPL];
-#pragma unroll
-            for (int i = 0; i < HPL; ++i) {
-                const int h = hs + 2 * i;
-                float dot = 0.f;
-                if (h < GE) {
-#pragma unroll 8
-                    for (int d = 0; d < HEAD / 4; ++d) {
-                        // NHD rows of 16 tokens are HEAD floats apart: each token's
-                        // lane walks the head dims from its own offset, so the 16
-                        // rows are read in different banks
-                        const int d4 = LAYOUT == kSplit ? d : ((d + t) & (HEAD / 4 - 1));
-                        const float4 qv = *reinterpret_cast<const float4*>(q + h * HEAD + 4 * d4);
-                        const float4 kv = (LAYOUT == kSplit)
-                            ? *reinterpret_cast<const float4*>(kp + (d4 * kBS + t) * 4)  // [d/4][token][4]
-                            : *reinterpret_cast<const float4*>(kp + t * HEAD + 4 * d4);
-                        dot = fmaf(qv.x, kv.x, dot);
-                        dot = fmaf(qv.y, kv.y, dot);
-                        dot = fmaf(qv.z, kv.z, dot);
-                        dot = fmaf(qv.w, kv.w, dot);
-                    }
-                }
-                float v = dot * p.scale;
-                if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
-                if (has_alibi) v += sl[i] * (float)(tok0 + t - origin);
-                const int tk = tok0 + t;
-                z[i] = (tk >= klo[i] && tk <= khi[i]) ? v : -INFINITY;
-            }
-#pragma unroll
-            for (int i = 0; i < HPL; ++i) {
-                const int h = hs + 2 * i;
-                float mx = z[i];
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float mn = fmaxf(m[i], mx);
-                const float mr = (C::kMQ && mn == -INFINITY) ? 0.f : mn;  // no -inf - -inf for an empty row
-                const float al = exp2f((m[i] - mr) * kLog2e);
-                const float pv = exp2f((z[i] - mr) * kLog2e);
-                m[i] = mn;
-                l[i] = l[i] * al + pv;
-                if (h < MAXG) {
-                    pw[h * kBS + t] = pv;
-                    if (t == 0) pw[kBS * MAXG + h] = al;
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int h = 0; h < MAXG; ++h) {
-                if (h < GE) {
-                    const float al = pw[kBS * MAXG + h];
-#pragma unroll
-                    for (int c = 0; c < DPL; ++c) acc[h][c] *= al;
-                }
-            }
-            // all 16 tokens: masked ones have p = 0 and a finite (or zeroed) V.
-            // Split V rows are 16 tokens (64 B) per head dim, so the lanes walk
-            // the tokens from different offsets to spread the banks.
-#pragma unroll 4
-            for (int ti = 0; ti < kBS; ++ti) {
-                const int tt = LAYOUT == kSplit ? ((ti + (lane >> 1)) & (kBS - 1)) : ti;
-                float vv[DPL];
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) {
-                    const int dd = lane + 32 * c;
-                    vv[c] = (LAYOUT == kSplit) ? vp[dd * kBS + tt] : vp[tt * HEAD + dd];
-                }
-#pragma unroll
-                for (int h = 0; h < MAXG; ++h) {
-                    if (h < GE) {
-                        const float pr = pw[h * kBS + tt];
-#pragma unroll
-                        for (int c = 0; c < DPL; ++c) acc[h][c] = fmaf(pr, vv[c], acc[h][c]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty + st * 8);
-        }
-        // sum l over the 16 tokens (lanes with the same hs)
-#pragma unroll
-        for (int i = 0; i < HPL; ++i)
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], o);
-        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
-#pragma unroll
-        for (int h = 0; h < MAXG; ++h)
-            if (h < GE)
-#pragma unroll
-                for (int c = 0; c < DPL; ++c) mw[h * C::kMergeStride + lane + 32 * c] = acc[h][c];
-        if (t == 0) {
-#pragma unroll
-            for (int i = 0; i < HPL; ++i) {
-                const int h = hs + 2 * i;
-                if (h < MAXG) sm.ml[warp * C::kMaxG + h] = make_float2(m[i], l[i]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // done with Q in shared memory
-        if (!consumer_sync(sm, mphase, lane)) {
-            report(p, PA_DEVERR_TIMEOUT);
-            *sm.abort = 1;
-            return;
-        }
-        if (!tile_finish<C, float, HEAD, NC>(p, d, sm, warp, lane, mphase)) {
-            report(p, PA_DEVERR_TIMEOUT);
-            *sm.abort = 1;
-            return;
-        }
-        gbase += (uint32_t)npages;
-    }
-}
-
 // ------------------------------------------------------------------ kernels
 
 // Two n-tiles hold 16 rows of accumulators (~200 registers uncapped), and the
@@ -1923,7 +1706,7 @@ template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, 
 __global__ void __launch_bounds__((NC + 1) * 32,
                                   (std::is_same<T, float>::value && NT > 1)
                                       ? 1
-                                      : ((NT > 1 || std::is_same<T, float>::value) ? 2 : PA_MIN_CTAS_PER_SM))
+                                      : ((NT > 1 || std::is_same<T, float>::value) ? 2 : 1))
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
@@ -1937,7 +1720,6 @@ __global__ void __launch_bounds__((NC + 1) * 32,
     sm.q = base + C::oQ;
     sm.merge = reinterpret_cast<float*>(gen + C::oMerge);
     sm.ml = reinterpret_cast<float2*>(gen + C::oML);
-    sm.scratch = reinterpret_cast<float*>(gen + C::oScratch);
     sm.desc = reinterpret_cast<TileDesc*>(gen + C::oDesc);
     sm.full = base + C::oBar;
     sm.empty = sm.full + STAGES * 8;
@@ -1976,10 +1758,7 @@ __global__ void __launch_bounds__((NC + 1) * 32,
     if (warp == NC) {
         producer<C, HEAD, STAGES>(p, sm, &tmk, &tmv, lane);
     } else if constexpr (C::kF32) {
-        if constexpr (C::kTf32)
-            consumer_tf32<C, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
-        else
-            consumer_f32<C, HEAD, LAYOUT, STAGES, NC>(p, sm, warp, lane);
+        consumer_tf32<C, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);
     } else {
         if constexpr (KV == kKvSame)
             consumer_mma<C, T, HEAD, NT, LAYOUT, STAGES, NC>(p, sm, warp, lane);

@@ -22,7 +22,6 @@ struct LaunchArgs {
     int head_size;
     void* ev_begin;
     void* ev_end;
-    int grid_override;       // > 0: use this many CTAs (tests / sweeps)
 };
 
 constexpr int kMaxDevices = 64;
@@ -36,11 +35,10 @@ constexpr int kMaxDevices = 64;
 // CTAs; the separate reduce kernel spreads them over the whole GPU instead.
 template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
-    constexpr int STAGES = std::is_same<T, float>::value ? (NT == 1 ? PA_STAGES_F32 : PA_STAGES_F32_2T)
-                           : (KV == kKvSame ? PA_STAGES_16BIT
-                                            : (NT == 1 && LAYOUT == kNHD ? PA_STAGES_FP8_PAIRS
-                                                                         : PA_STAGES_FP8));
-    constexpr int NC = PA_CONSUMER_WARPS;
+    constexpr int STAGES = std::is_same<T, float>::value ? (NT == 1 ? kStagesF32 : kStagesF32x2)
+                           : (KV == kKvSame ? kStages16
+                                            : (NT == 1 && LAYOUT == kNHD ? kStagesFp8Pairs : kStagesFp8));
+    constexpr int NC = kConsumerWarps;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
     auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
 
@@ -57,7 +55,6 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
         if (occ < 1) return cudaErrorInvalidConfiguration;
         if (dev >= 0 && dev < kMaxDevices) occ_cache[dev].store(occ);
     }
-    if (PA_MAX_CTAS_PER_SM > 0 && occ > PA_MAX_CTAS_PER_SM) occ = PA_MAX_CTAS_PER_SM;
     int64_t grid = (int64_t)la.sm_count * occ;
     if (grid > la.tiles_upper) grid = la.tiles_upper;
     if (grid < 1) grid = 1;
@@ -70,7 +67,6 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
         const int64_t rounds = (la.tiles_upper + grid - 1) / grid;
         grid = (la.tiles_upper + rounds - 1) / rounds;
     }
-    if (la.grid_override > 0) grid = la.grid_override < la.tiles_upper ? la.grid_override : la.tiles_upper;
     Params p = p_in;
     p.fused = (!p.v1 && p.counters && p.max_parts <= PA_FUSED_MAX_PARTITIONS &&
                la.tiles_upper <= grid) ? 1 : 0;
@@ -138,7 +134,7 @@ cudaError_t launch_reduce(const Params& p, const LaunchArgs& la) {
     const int64_t rows = (int64_t)p.num_seqs * p.max_q_len * p.num_heads;
     if (p.max_parts > 32 && rows <= 2 * (int64_t)la.sm_count)
         return launch_reduce_shape<T, HEAD, 16, 8, MQ>(p, la);
-    if (p.max_parts <= PA_REDUCE_WARP_MAX_PARTS) return launch_reduce_warp<T, HEAD, MQ>(p, la, rows);
+    if (p.max_parts <= kReduceWarpMaxParts) return launch_reduce_warp<T, HEAD, MQ>(p, la, rows);
     return launch_reduce_shape<T, HEAD, 8, 4, MQ>(p, la);
 }
 

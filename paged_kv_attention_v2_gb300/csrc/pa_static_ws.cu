@@ -59,10 +59,19 @@ extern "C" pa_status pa_decode_static_workspace(const pa_decode_args* args, void
     // workspace rows: one per query token (one per sequence without query_start)
     const int64_t rows = args->query_start ? args->num_query_tokens : args->num_seqs;
     if (rows < 0) return PA_ERR_INVALID_ARG;
-    const int64_t stats = rows * args->num_heads * pa_max_num_partitions(args->max_seq_len);
+    // rows * num_heads * P * (head_size + 2) <= capacity, checked factor by
+    // factor so that no product of the (int32) sizes can wrap: each partial
+    // product stays below the capacity (2^22) times an int32.
+    const int64_t cap = PA_STATIC_WORKSPACE_FLOATS;
+    const int64_t per_stat = (int64_t)args->head_size + 2;  // floats per (row, head, partition)
+    const int64_t parts = pa_max_num_partitions(args->max_seq_len);
+    if (rows > cap / args->num_heads) return PA_ERR_WORKSPACE;
+    const int64_t row_heads = rows * args->num_heads;  // <= cap
+    if (parts > cap / per_stat) return PA_ERR_WORKSPACE;
+    if (row_heads > 0 && parts * per_stat > cap / row_heads) return PA_ERR_WORKSPACE;
+    const int64_t stats = row_heads * parts;
     // tmp_out first (16-byte alignment for its float4 accesses), then the two statistics arrays
     const int64_t tmp = stats * args->head_size;
-    if (tmp + 2 * stats > (int64_t)PA_STATIC_WORKSPACE_FLOATS) return PA_ERR_WORKSPACE;
     if (args->num_seqs == 0) return PA_OK;
     float* base = static_workspace_address();
     if (!base) return PA_ERR_LAUNCH;

@@ -6,7 +6,9 @@ the library a freshly allocated workspace.  This entry point keeps the
 partition workspace in a fixed device array inside the library instead.  The
 GPU test calls it through the C ABI twice in a row and checks each result
 against the regular pa_decode entry point, within the tolerance the parity tests
-use.  (This file is named so that pytest collects it last.)
+use, after a call that leaves NaN in the part of the array the checked calls
+use (contents left by an earlier call must not matter).  (This file is named
+so that pytest collects it last.)
 """
 import ctypes
 
@@ -41,6 +43,17 @@ def test_batch_beyond_static_capacity_is_rejected():
     assert lib.pa_decode_static_workspace(
         ctypes.byref(_args(**small, query_start=256, num_query_tokens=512, max_query_len=64)),
         None) == _abi.PA_ERR_WORKSPACE
+    # sizes whose product would wrap a 64-bit integer are refused, not wrapped
+    # into a small footprint (rows ~2^31, 2^24 heads, 1024 partitions)
+    huge = dict(num_seqs=8, num_heads=1 << 24, num_kv_heads=1 << 20, max_seq_len=1 << 19,
+                max_blocks_per_seq=1 << 15, query_start=256, num_query_tokens=(1 << 31) - 1,
+                max_query_len=1)
+    assert lib.pa_decode_static_workspace(ctypes.byref(_args(**huge)), None) == _abi.PA_ERR_WORKSPACE
+    for rows, heads, msl in ((1 << 30, 1 << 20, 1 << 30), (1, 1, (1 << 31) - 1), (1 << 20, 8, 1 << 20)):
+        a = _args(num_seqs=8, num_heads=heads, num_kv_heads=1, max_seq_len=msl,
+                  max_blocks_per_seq=(msl + 15) // 16, query_start=256, num_query_tokens=rows,
+                  max_query_len=1)
+        assert lib.pa_decode_static_workspace(ctypes.byref(a), None) == _abi.PA_ERR_WORKSPACE
 
 
 @pytest.mark.gpu
@@ -85,6 +98,31 @@ def test_static_workspace_matches_pa_decode_on_two_calls(case):
         num_query_tokens=w.num_query_tokens if multi else 0,
         max_query_len=w.max_query_len if multi else 0)
     stream = torch.cuda.current_stream().cuda_stream
+
+    # Leave NaN in every entry of the array the checked calls can touch: a call
+    # of the same rows and heads with twice the partitions, all of them used,
+    # and a NaN value cache writes NaN partition outputs over more than the
+    # whole footprint of the checked calls.  A checked call that read an entry
+    # it did not write itself would then return NaN.
+    R = w.num_query_tokens
+    P2 = 2 * max(1, -(-w.max_seq_len // 512))
+    lens2 = torch.full((R,), P2 * 512, dtype=torch.int32, device="cuda:0")
+    bt2 = torch.zeros((R, P2 * 32), dtype=torch.int32, device="cuda:0")
+    v_nan = torch.full_like(dev["value_cache"], float("nan"))
+    out2 = torch.zeros_like(out)
+    poison = _abi.PaDecodeArgs(
+        out=out2.data_ptr(), query=dev["query"].data_ptr(), key_cache=dev["key_cache"].data_ptr(),
+        value_cache=v_nan.data_ptr(), block_tables=bt2.data_ptr(), seq_lens=lens2.data_ptr(),
+        num_seqs=R, num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_size=w.head_size,
+        num_blocks=w.num_blocks, block_size=w.block_size, max_seq_len=P2 * 512,
+        max_blocks_per_seq=P2 * 32, scale=w.scale, softcap=0.0,
+        dtype={"f32": 0, "f16": 1, "bf16": 2}[w.dtype], layout={"split": 0, "nhd": 1}[w.layout],
+        mode=_abi.PA_MODE_AUTO, dev_error=err.data_ptr())
+    assert lib.pa_decode_static_workspace(ctypes.byref(poison), ctypes.c_void_p(stream)) == _abi.PA_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isnan(out2.float()).all(), "the poisoning call did not leave NaN behind"
+
     atol, rtol = OUT_TOL[w.dtype]
     for call in range(2):
         out.fill_(float("nan"))
