@@ -198,6 +198,205 @@ def time_oracle(w, budget_s: float, threads=None):
 
 # ------------------------------------------------------------------ GPU arm
 
+SECONDARY = "long100k"  # the second target workload, timed in the same default run
+MEDIAN_STEPS = 50       # steps timed one by one for the per-step median
+
+
+def t_(a, dtype):
+    import torch
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))  # fp32 / fp16, or raw fp8 bytes
+
+
+class Setup:
+    """Device buffers and prepared C argument structs of one workload: several
+    KV pools that the steps rotate through, so the bytes touched between two
+    uses of a pool exceed 4x the L2 size."""
+
+    def __init__(self, w, mode_arg, dev, pa, counters=True):
+        import torch
+        self.w, self.dev = w, dev
+        cdt = w.cache_dtype
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.pool_bytes = w.key_cache.nbytes + w.value_cache.nbytes
+        self.copies = max(1, min(8, -(-4 * self.l2 // self.pool_bytes)))
+        self.q = t_(w.query, w.dtype).to(dev)
+        self.kcs = [t_(w.key_cache, cdt).to(dev) for _ in range(self.copies)]
+        self.vcs = [t_(w.value_cache, cdt).to(dev) for _ in range(self.copies)]
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        self.al = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(dev)
+        self.out = torch.empty(self.q.shape, dtype=tdt, device=dev)
+        self.qs = None if w.query_start is None else torch.from_numpy(w.query_start).to(dev)
+        # v2 workspace with partition counters, so the library may merge the
+        # partitions inside the partition kernel where its rule allows
+        self.ws = pa.alloc_workspace(w.num_seqs, w.num_heads, w.head_size, w.max_seq_len, dev,
+                                     num_kv_heads=w.num_kv_heads if counters else None,
+                                     num_query_tokens=None if self.qs is None else w.num_query_tokens)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
+                      kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
+                      alibi_slopes=self.al, softcap=w.softcap, layout=w.layout, mode=mode_arg,
+                      dev_error=self.err, query_start=self.qs,
+                      max_query_len=None if self.qs is None else w.max_query_len,
+                      seq_lens_host=w.seq_lens, **self.ws)
+        self.cargs = [pa.make_args(self.out, self.q, self.kcs[i], self.vcs[i], self.bt, self.sl, **common)
+                      for i in range(self.copies)]
+        # what one call runs (mode, in-kernel merge, kernels per call), as the library plans it
+        with torch.cuda.device(dev):
+            self.plan = pa.plan(self.cargs[0])
+        self.stream = torch.cuda.current_stream(dev)
+        self.sh = self.stream.cuda_stream
+        self.pa = pa
+
+    def step(self, i, ev=None):
+        a = self.cargs[i % self.copies]
+        if ev is not None:
+            a.event_main_begin, a.event_main_end = ev[0].cuda_event, ev[1].cuda_event
+        else:
+            a.event_main_begin = a.event_main_end = None
+        st = self.pa.decode_args_call(a, self.sh)
+        if st != 0:
+            raise self.pa.PaDecodeError(st)
+
+
+def measure(S, K, warmup, world, soak_s, sampler):
+    """Time K back-to-back steps (the headline), then the same steps with
+    events around the main kernel (roofline), MEDIAN_STEPS steps timed one by
+    one (per-step median), and the warm-L2 steps on one pool."""
+    import torch
+    dev, stream = S.dev, S.stream
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    t_soak = time.time()
+    i = 0
+    while time.time() - t_soak < soak_s:  # clock soak (untimed)
+        for _ in range(50):
+            S.step(i)
+            i += 1
+        torch.cuda.synchronize(dev)
+    for j in range(warmup):
+        S.step(j)
+    torch.cuda.synchronize(dev)
+
+    def events(n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:  # torch creates events lazily: record once so the handles exist
+            a.record(stream)
+            b.record(stream)
+        return ev
+
+    kev = events(K)
+    sev = events(max(K, MEDIAN_STEPS))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+
+    # timed region: exactly K steps back to back
+    t0 = time.time()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for j in range(K):
+        S.step(j)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    ms_total = e0.elapsed_time(e1)
+
+    # the same K steps with CUDA events around the main kernel of every step
+    # (roofline.achieved); the events split the programmatic overlap of the
+    # kernels, so this pass is reported separately and not used for `value`
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for j in range(K):
+        S.step(j, kev[j])
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    ms_instrumented = e2.elapsed_time(e3) / K
+
+    # every step between its own pair of events (each step then starts on an
+    # idle stream): the per-step median the timing rule of the pages' context asks for
+    for j, (a, b) in enumerate(sev):
+        a.record(stream)
+        S.step(j)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = [a.elapsed_time(b) for a, b in sev]
+
+    # warm: the same steps on one KV pool only (whatever of it L2 keeps between steps)
+    e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        S.step(0)
+    e4.record(stream)
+    for _ in range(K):
+        S.step(0)
+    e5.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_warm = e4.elapsed_time(e5) / K
+    derr = int(S.err.item())
+    if derr:
+        raise SystemExit(f"device error bits {derr} during the bench ({S.w.name})")
+    return {"ms_step": max_over_ranks(ms_total / K, dev), "kernel_ms": statistics.mean(kernel_ms),
+            "ms_instrumented": ms_instrumented, "step_ms_median": statistics.median(step_ms),
+            "step_ms_min": min(step_ms), "median_steps": len(step_ms), "ms_warm": ms_warm,
+            "window": (t_soak, time.time()), "timed_window": (t0, t1)}
+
+
+def total_bytes(w, S, mode):
+    tb = (w.kv_bytes + w.query.nbytes + S.out.numel() * S.out.element_size() + w.block_tables.nbytes
+          + w.seq_lens.nbytes)
+    if mode == "v2":
+        P = -(-w.seq_lens.astype(np.int64) // 512)
+        qn = np.ones_like(P) if w.query_start is None else np.diff(w.query_start).astype(np.int64)
+        tb += int((P * qn).sum()) * w.num_heads * (w.head_size + 2) * 4 * 2
+    return int(tb)
+
+
+def roofline(w, S, r, peak, peak_kind):
+    kv = w.kv_bytes
+    plan = S.plan
+    return {"bound": "hbm", "achieved": round(kv / (r["kernel_ms"] * 1e-3) / 1e9, 2), "peak": peak,
+            "unit": "GB/s", "frac": round(kv / (r["kernel_ms"] * 1e-3) / 1e9 / peak, 4),
+            "peak_kind": peak_kind,
+            "kernel": "pa_partition_kernel" + (" (v1)" if plan["mode"] == "v1" else ""),
+            "kernel_ms": round(r["kernel_ms"], 6),
+            "traffic": recorded_traffic(w.name, w.layout, plan["mode"]),
+            "note": "achieved = algorithmic KV bytes / mean CUDA-event time of the partition kernel, "
+                    "from a second pass of the same steps with events around that kernel (they split "
+                    "its programmatic overlap with the next launch, so kernel_ms can exceed ms_per_step)"}
+
+
+def config_record(w, S, r, args, world):
+    plan = S.plan
+    return {"workload": W.DESCRIPTIONS[w.name], "name": w.name, "layout": w.layout,
+            "mode": plan["mode"],
+            "merge": ("in the partition kernel" if plan["merge_in_kernel"] else "reduce kernel")
+            if plan["mode"] == "v2" else "none (v1)",
+            "partition_grid": plan["grid"], "ctas_per_sm": plan["ctas_per_sm"],
+            "kv_bytes_per_step": w.kv_bytes, "total_bytes_per_step": total_bytes(w, S, plan["mode"]),
+            "l2": f"rotate {S.copies} KV pools ({S.copies * S.pool_bytes} B >= 4x L2 {S.l2} B)"
+            if S.copies * S.pool_bytes >= 4 * S.l2 else f"{S.copies} KV pools of {S.pool_bytes} B",
+            "parallelism": f"replicas x{world}", "clock_soak_s": 0.0 if args.no_soak else 1.0,
+            "ms_per_step_with_kernel_events": round(r["ms_instrumented"], 6),
+            "per_step": {"median_ms": round(r["step_ms_median"], 6), "min_ms": round(r["step_ms_min"], 6),
+                         "steps": r["median_steps"],
+                         "note": "each step between its own events on an idle stream (no overlap "
+                                 "with the previous step), median; the headline is the mean of K "
+                                 "steps back to back"},
+            "warm_l2": {"ms_per_step": round(r["ms_warm"], 6),
+                        "value": round(whole_job_gbs(w.kv_bytes, 1, r["ms_warm"]), 3),
+                        "note": "one KV pool reused step after step (rank-local)"}}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -212,197 +411,99 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = W.make_workload(args.config, args.layout)
-    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
-
-    def t_(a, dtype=None):
-        dtype = dtype or w.dtype
-        if dtype == "bf16":
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(a))  # fp8 caches: raw bytes
-
-    cdt = w.cache_dtype
-
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool_bytes = w.key_cache.nbytes + w.value_cache.nbytes
-    copies = max(1, min(8, -(-4 * l2 // pool_bytes)))
-    q = t_(w.query).to(dev)
-    kcs = [t_(w.key_cache, cdt).to(dev) for _ in range(copies)]
-    vcs = [t_(w.value_cache, cdt).to(dev) for _ in range(copies)]
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    sl = torch.from_numpy(w.seq_lens).to(dev)
-    al = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).to(dev)
-    out = torch.empty(q.shape, dtype=tdt, device=dev)
-    qs = None if w.query_start is None else torch.from_numpy(w.query_start).to(dev)
-    ws = pa.alloc_workspace(w.num_seqs, w.num_heads, w.head_size, w.max_seq_len, dev,
-                            num_query_tokens=None if qs is None else w.num_query_tokens)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    # the library's AUTO choice with the host copy of the lengths a serving
-    # loop has at hand (the same rule pa_decode applies to seq_lens_host)
-    mode = args.mode if args.mode != "auto" else pa.choose_mode(w.num_seqs, w.num_kv_heads,
-                                                                 w.max_seq_len, sm_count,
-                                                                 w.seq_lens)
-    fused = False  # no partition counters: v2 always launches the reduce kernel
-    common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
-                  kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
-                  alibi_slopes=al, softcap=w.softcap, layout=w.layout, mode=mode,
-                  dev_error=err, query_start=qs,
-                  max_query_len=None if qs is None else w.max_query_len, **ws)
-    cargs = [pa.make_args(out, q, kcs[i], vcs[i], bt, sl, **common) for i in range(copies)]
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-
-    def step(i, ev=None):
-        a = cargs[i % copies]
-        if ev is not None:
-            a.event_main_begin, a.event_main_end = ev[0].cuda_event, ev[1].cuda_event
-        else:
-            a.event_main_begin = a.event_main_end = None
-        st = pa.decode_args_call(a, sh)
-        if st != 0:
-            raise pa.PaDecodeError(st)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    # clock soak (untimed): run steps back to back for ~1 s while nvidia-smi samples start
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    t_soak = time.time()
-    i = 0
-    while not args.no_soak and time.time() - t_soak < 1.0:
-        for _ in range(50):
-            step(i)
-            i += 1
-        torch.cuda.synchronize(dev)
-
-    for j in range(args.warmup):
-        step(j)
-    torch.cuda.synchronize(dev)
-
-    K = args.steps
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
-    for a, b in kev:  # torch creates events lazily: record once so the handles exist
-        a.record(stream)
-        b.record(stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-
-    # timed region: exactly K steps back to back (value, ms_per_step)
-    barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for j in range(K):
-        step(j)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    t_wall1 = time.time()
-    ms_total = e0.elapsed_time(e1)
-
-    # the same K steps with CUDA events around the main kernel of every step
-    # (roofline.achieved); the events split the programmatic overlap of the two
-    # kernels, so this pass is reported separately and not used for `value`.
-    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for j in range(K):
-        step(j, kev[j])
-    e3.record(stream)
-    torch.cuda.synchronize(dev)
-    kernel_ms = [a.elapsed_time(b) for a, b in kev]
-    ms_total_instrumented = e2.elapsed_time(e3)
-
-    # warm: the same steps on one KV pool only (whatever of it L2 keeps between
-    # steps is reused); reported beside the cold headline, not used for `value`
-    e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(3):
-        step(0)
-    e4.record(stream)
-    for _ in range(K):
-        step(0)
-    e5.record(stream)
-    torch.cuda.synchronize(dev)
-    ms_warm = e4.elapsed_time(e5) / K
-    time.sleep(0.15)
-    sampler.stop()
-    clocks = sampler.summary(t_soak, time.time())
-
-    derr = int(err.item())
-    if derr:
-        raise SystemExit(f"device error bits {derr} during the bench")
-
-    ms_step = max_over_ranks(ms_total / K, dev)
-
-    kv = w.kv_bytes
-    value = whole_job_gbs(kv, world, ms_step)
+    soak = 0.0 if args.no_soak else 1.0
     peak, peak_kind = peaks()
-    k_ms = statistics.mean(kernel_ms)
-    achieved = kv / (k_ms * 1e-3) / 1e9
-    total_bytes = (kv + w.query.nbytes + out.numel() * out.element_size() + w.block_tables.nbytes
-                   + w.seq_lens.nbytes)
-    if mode == "v2":
-        P = -(-w.seq_lens.astype(np.int64) // 512)
-        qn = np.ones_like(P) if w.query_start is None else np.diff(w.query_start).astype(np.int64)
-        total_bytes += int((P * qn).sum()) * w.num_heads * (w.head_size + 2) * 4 * 2
 
-    # e2e: host buffers, copies inside the timed region
+    w = W.make_workload(args.config, args.layout)
+    S = Setup(w, args.mode, dev, pa, counters=args.merge == "auto")
+    r = measure(S, args.steps, args.warmup, world, soak, sampler)
+    kv = w.kv_bytes
+    value = whole_job_gbs(kv, world, r["ms_step"])
+
+    # e2e: host buffers, copies inside the timed region, through the C ABI
     e2e = None
     if not args.no_e2e:
-        hq = t_(w.query).pin_memory()
+        cdt = w.cache_dtype
+        hq = t_(w.query, w.dtype).pin_memory()
         hk = t_(w.key_cache, cdt).pin_memory()
         hv = t_(w.value_cache, cdt).pin_memory()
         hbt = torch.from_numpy(w.block_tables).pin_memory()
         hsl = torch.from_numpy(w.seq_lens).pin_memory()
         hal = None if w.alibi_slopes is None else torch.from_numpy(w.alibi_slopes).pin_memory()
-        hqs = None if qs is None else torch.from_numpy(w.query_start).pin_memory()
-        hout = torch.empty(out.shape, dtype=tdt).pin_memory()
+        hqs = None if S.qs is None else torch.from_numpy(w.query_start).pin_memory()
+        hout = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
         h2d = (hq.nbytes + hk.nbytes + hv.nbytes + hbt.nbytes + hsl.nbytes +
                (hal.nbytes if hal is not None else 0) + (hqs.nbytes if hqs is not None else 0))
         d2h = hout.nbytes
-        Ke = max(3, min(K, 50))
+        Ke = max(3, min(args.steps, 50))
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            kcs[0].copy_(hk, non_blocking=True)
-            vcs[0].copy_(hv, non_blocking=True)
-            bt.copy_(hbt, non_blocking=True)
-            sl.copy_(hsl, non_blocking=True)
+            S.q.copy_(hq, non_blocking=True)
+            S.kcs[0].copy_(hk, non_blocking=True)
+            S.vcs[0].copy_(hv, non_blocking=True)
+            S.bt.copy_(hbt, non_blocking=True)
+            S.sl.copy_(hsl, non_blocking=True)
             if hal is not None:
-                al.copy_(hal, non_blocking=True)
+                S.al.copy_(hal, non_blocking=True)
             if hqs is not None:
-                qs.copy_(hqs, non_blocking=True)
-            step(0)
-            hout.copy_(out, non_blocking=True)
+                S.qs.copy_(hqs, non_blocking=True)
+            S.step(0)
+            hout.copy_(S.out, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
-        barrier()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
+        f0.record(S.stream)
         for _ in range(Ke):
             e2e_step()
-        f1.record(stream)
+        f1.record(S.stream)
         torch.cuda.synchronize(dev)
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / Ke, dev)
         e2e = {"value": round(whole_job_gbs(kv, world, ms_e2e), 3), "unit": "GB/s",
                "ms_per_step": round(ms_e2e, 4), "steps": Ke,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    line_cfg = config_record(w, S, r, args, world)
+    rl = roofline(w, S, r, peak, peak_kind)
+    launches = args.steps * S.plan["kernels"]
+    timed = r["timed_window"]
+    del S
+    torch.cuda.empty_cache()
+
+    # the second target workload (100K-token context), same method, same run
+    secondary = None
+    if not args.no_secondary and args.config != SECONDARY:
+        w2 = W.make_workload(SECONDARY, "split")
+        S2 = Setup(w2, "auto", dev, pa, counters=args.merge == "auto")
+        r2 = measure(S2, args.steps, args.warmup, world, soak, sampler)
+        v2 = whole_job_gbs(w2.kv_bytes, world, r2["ms_step"])
+        secondary = {SECONDARY: {
+            "value": round(v2, 3), "unit": "GB/s", "ms_per_step": round(r2["ms_step"], 6),
+            "us_per_step": round(r2["ms_step"] * 1e3, 3), "frac_of_peak": round(v2 / world / peak, 4),
+            "steps": args.steps, "warmup": args.warmup, "dtype": w2.dtype,
+            "config": config_record(w2, S2, r2, args, world), "roofline": roofline(w2, S2, r2, peak, peak_kind),
+            "clocks": sampler.summary(*r2["window"])}}
+        del S2
+        torch.cuda.empty_cache()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(*r["window"])
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        r = time_oracle(w, args.cpu_budget)
-        cpu = {"value": round(r["kv_bytes"] / r["seconds"] / 1e9, 6), "unit": "GB/s",
-               "cores": r["threads"], "kind": "oracle",
-               "seconds": round(r["seconds"], 3),
-               "sample": f"first {r['seqs']} of {w.num_seqs} sequences (all heads, dense + "
-                         f"partition statistics in fp64), {r['kv_bytes']} KV bytes, "
-                         f"mean of {r['passes']} pass(es)"}
+        c = time_oracle(w, args.cpu_budget)
+        cpu = {"value": round(c["kv_bytes"] / c["seconds"] / 1e9, 6), "unit": "GB/s",
+               "cores": c["threads"], "kind": "oracle",
+               "seconds": round(c["seconds"], 3),
+               "sample": f"first {c['seqs']} of {w.num_seqs} sequences (all heads, dense + "
+                         f"partition statistics in fp64), {c['kv_bytes']} KV bytes, "
+                         f"mean of {c['passes']} pass(es)"}
 
     if world > 1:
         import torch.distributed as dist
@@ -410,39 +511,41 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
     if rank != 0:
         return None
-    line = {
+    return {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
-        "us_per_step": round(ms_step * 1e3, 3), "frac_of_peak": round(value / world / peak, 4),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 6),
+        "us_per_step": round(r["ms_step"] * 1e3, 3), "frac_of_peak": round(value / world / peak, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic: seeded N(0,1) inputs rounded to the storage dtype, shuffled block tables",
-        "config": {"workload": W.DESCRIPTIONS[w.name], "name": w.name, "layout": w.layout,
-                   "mode": mode, "merge": ("in the partition kernel" if fused else "reduce kernel")
-                   if mode == "v2" else "none (v1)", "kv_bytes_per_step": kv, "total_bytes_per_step": int(total_bytes),
-                   "l2": f"rotate {copies} KV pools ({copies * pool_bytes} B >= 4x L2 {l2} B)"
-                   if copies * pool_bytes >= 4 * l2 else f"{copies} KV pools of {pool_bytes} B",
-                   "parallelism": f"replicas x{world}", "clock_soak_s": 0.0 if args.no_soak else 1.0,
-                   "ms_per_step_with_kernel_events": round(ms_total_instrumented / K, 6),
-                   "warm_l2": {"ms_per_step": round(ms_warm, 6),
-                               "value": round(whole_job_gbs(kv, 1, ms_warm), 3),
-                               "note": "one KV pool reused step after step (rank-local)"}},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "kernel": "pa_partition_kernel" if mode == "v2" else "pa_partition_kernel (v1)",
-                     "kernel_ms": round(k_ms, 6),
-                     "traffic": recorded_traffic(w.name, w.layout, mode)},
+        "config": line_cfg,
+        "roofline": rl,
+        "secondary": secondary,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (2 if mode == "v2" and not fused else 1),
+        "gpu_launches": launches,
         "clocks": clocks,
+        "timed_region_s": round(timed[1] - timed[0], 4),
     }
-    return line
 
 
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, world, rank):
-    if rank != 0:
+    """The fp64 oracle on the host cores, on a bounded sample of the same
+    workload per step.  With several ranks, rank 0 alone does the work."""
+    own_pg = False
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+            own_pg = True
+        dist.barrier()  # every rank has joined
+        print(f"bench: rank {rank} of {world} joined", file=sys.stderr, flush=True)
+        if rank != 0:
+            if own_pg:
+                dist.destroy_process_group()
+            return None
+    elif rank != 0:
         return None
     import oracle
     w = W.make_workload(args.config, args.layout)
@@ -465,6 +568,9 @@ def run_reference(args, world, rank):
     value = kv / dt / 1e9
     sample = (f"first {n} of {w.num_seqs} sequences per step (all heads, dense + partition "
               f"statistics in fp64), {kv} KV bytes")
+    if own_pg:
+        import torch.distributed as dist
+        dist.destroy_process_group()
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -478,7 +584,26 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------------------------ launcher
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as n ranks on this node (one per GPU) with torchrun's
+    launcher over 127.0.0.1; returns its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", str(Path(__file__).resolve()),
+           *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -487,22 +612,34 @@ def main(argv=None):
     ap.add_argument("--layout", default="split", choices=W.LAYOUTS)
     ap.add_argument("--mode", default="auto", choices=("auto", "v1", "v2"))
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--merge", default="auto", choices=("auto", "reduce"),
+                    help="auto: pass partition counters (the library may merge in the partition "
+                         "kernel); reduce: no counters, v2 always launches the reduce kernel")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help=f"skip the second target workload ({SECONDARY}) of the default run")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle wall time")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds for the reference arm")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(args.gpus, argv)
     world, rank, local = dist_setup()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}: launch one rank per GPU")
     if args.impl == "reference":
         line = run_reference(args, world, rank)
     else:
         line = run_ours(args, world, rank, local)
     if line is not None:
         print(json.dumps(line), flush=True)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -154,8 +154,8 @@ typedef struct pa_decode_args {
      * in one round of the persistent grid (num_seqs * num_kv_heads * P no more
      * than the resident CTAs), the Phase 2 merge of a (sequence, kv head) is
      * done inside the partition kernel by the CTA that finishes its last
-     * partition, and no second kernel is launched; otherwise the counters are
-     * not touched.  Each completed call leaves every counter at zero again;
+     * partition, and no second kernel is launched (pa_plan tells); otherwise
+     * the counters are not touched.  Each completed call leaves every counter at zero again;
      * after a PA_DEVERR_TIMEOUT the caller must zero them.  Calls that share
      * counters must not overlap on the GPU.  NULL = separate reduce kernel. */
     int32_t* partition_counters;
@@ -192,8 +192,9 @@ typedef struct pa_decode_args {
     int32_t num_query_tokens;  /* rows of query / out / workspace */
     int32_t max_query_len;     /* >= every qn, >= 1; max_query_len * group <= 16 */
     /* Optional HOST copy of seq_lens ([num_seqs] int32, read during the call,
-     * never by the device), used only by PA_MODE_AUTO to pick v1 or v2 with
-     * pa_choose_mode_for_lengths; NULL = pa_choose_mode (max_seq_len only). */
+     * never by the device).  PA_MODE_AUTO picks v1 or v2 with
+     * pa_choose_mode_for_lengths on it (NULL: every sequence taken as
+     * max_seq_len long). */
     const int32_t* seq_lens_host;
 } pa_decode_args;
 
@@ -272,26 +273,55 @@ size_t pa_workspace_bytes(int32_t rows, int32_t num_heads, int32_t head_size, in
 int32_t pa_partition_size(void);
 
 /*
- * v1 / v2 choice used by PA_MODE_AUTO, as a pure host function (sm_count is
- * the device's multiprocessor count).  The pages decide by tiles against SMs
- * (should_use_paged_v2 in attn_dispatch.py: v2 when num_kv_heads *
- * ceil(seq_len/512) > 2 * SM_COUNT on a 16-SM part); this library retunes that
- * rule for GB300, see pa_decode.cu.  Returns PA_MODE_V1 or PA_MODE_V2.
+ * v1 / v2 choice used by PA_MODE_AUTO, as a pure host function.  The pages
+ * decide by tiles against SMs (should_use_paged_v2 in
+ * "ex_engine/factors/attn_dispatch.py": v2 when num_kv_heads *
+ * ceil(seq_len/512) > 2 * SM_COUNT on a 16-SM part, with the one seq_len of
+ * the batch); this library retunes that rule for its persistent kernel, which
+ * runs both modes: v1 (one tile per (sequence, kv head), no partition
+ * statistics, no reduce launch) when max_seq_len <= PA_PARTITION_SIZE, or
+ * when the v1 tiles (num_seqs * num_kv_heads) are at least sm_count and the
+ * persistent grid's static assignment of them (sm_count * ctas_per_sm
+ * resident CTAs cut to equal rounds, as the launch does) gives its busiest
+ * CTA at most 10 % more pages than the mean; otherwise v2.
+ * pa_choose_mode takes every sequence to be max_seq_len long (callers with
+ * unequal lengths should pass them: pa_choose_mode_for_lengths, or
+ * seq_lens_host in the arguments).  sm_count is the device's multiprocessor
+ * count, ctas_per_sm the resident CTAs per SM of the partition kernel that
+ * the call runs (pa_plan reports it; <= 0 means 2, the figure of 16-bit
+ * caches).  Returns PA_MODE_V1 or PA_MODE_V2; sizes <= 0 give PA_MODE_V2
+ * (PA_MODE_V1 when max_seq_len <= PA_PARTITION_SIZE).
  */
-int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
-                       int32_t sm_count);
+int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t sm_count,
+                       int32_t ctas_per_sm);
+
+/* The same choice with the lengths known on the host (seq_lens_host,
+ * [num_seqs] int32, each clamped into [0, max_seq_len]; NULL behaves as
+ * pa_choose_mode). */
+int32_t pa_choose_mode_for_lengths(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                                   int32_t sm_count, int32_t ctas_per_sm, const int32_t* seq_lens_host);
+
+/* What pa_decode runs for a set of arguments (filled by pa_plan). */
+typedef struct pa_launch_plan {
+    int32_t mode;             /* PA_MODE_V1 or PA_MODE_V2 */
+    int32_t merge_in_kernel;  /* 1: the v2 Phase 2 merge runs in the partition kernel */
+    int32_t kernels;          /* kernels launched per call: 1 or 2 */
+    int32_t ctas_per_sm;      /* resident CTAs per SM of the partition kernel */
+    int32_t grid;             /* CTAs of the persistent partition-kernel grid */
+    int64_t tiles;            /* tiles of the partition kernel (an upper bound for unequal lengths) */
+} pa_launch_plan;
 
 /*
- * The same choice when the lengths are known on the host (seq_lens_host,
- * [num_seqs] int32; NULL behaves as pa_choose_mode).  v1 (one tile per
- * (sequence, kv head), no partition statistics, no reduce launch) is taken
- * when max_seq_len <= PA_PARTITION_SIZE, or when those tiles are at least as
- * many as the SMs and the persistent grid's static assignment of them gives
- * every CTA nearly the same number of pages (largest load at most 10 % above
- * the mean); otherwise v2.  Returns PA_MODE_V1 or PA_MODE_V2.
+ * The launch pa_decode would make for `args` on the current device, without
+ * launching anything: the mode (AUTO resolved as pa_decode resolves it),
+ * whether the merge runs in the partition kernel, the kernels per call and
+ * the partition kernel's grid.  Returns what pa_decode would return for the
+ * host-visible checks (pointers are checked for presence and alignment only,
+ * never read), PA_ERR_INVALID_ARG for a NULL plan, PA_ERR_LAUNCH when the
+ * device cannot be queried; `*plan` is zeroed first and stays zero for an
+ * empty batch.  (The pages have no counterpart.)
  */
-int32_t pa_choose_mode_for_lengths(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
-                                   int32_t sm_count, const int32_t* seq_lens_host);
+pa_status pa_plan(const pa_decode_args* args, pa_launch_plan* plan);
 
 /*
  * Test hook for the bounded waits of the kernels (failure detection without a

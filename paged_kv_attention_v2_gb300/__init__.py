@@ -17,7 +17,8 @@ from . import _abi
 from ._abi import (PA_BLOCK_SIZE, PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_TIMEOUT,
                    PA_PARTITION_SIZE, LibraryMissing)
 
-__all__ = ["pa_decode", "pa_decode_static_workspace", "alloc_workspace", "max_num_partitions", "choose_mode", "status_str",
+__all__ = ["pa_decode", "pa_decode_static_workspace", "alloc_workspace", "max_num_partitions", "choose_mode",
+           "plan", "plan_for", "status_str",
            "PaDecodeError", "PA_PARTITION_SIZE", "PA_BLOCK_SIZE", "PA_DEVERR_BLOCK_ID",
            "PA_DEVERR_SEQ_LEN", "PA_DEVERR_TIMEOUT", "LibraryMissing", "library"]
 
@@ -45,19 +46,41 @@ def max_num_partitions(max_seq_len: int) -> int:
 
 
 def choose_mode(num_seqs: int, num_kv_heads: int, max_seq_len: int, sm_count: int,
-                seq_lens_host=None) -> str:
-    """The library's AUTO choice; with seq_lens_host (host int32 lengths) the
-    length-aware rule of pa_choose_mode_for_lengths."""
+                seq_lens_host=None, ctas_per_sm: int = 2) -> str:
+    """The library's AUTO rule as a pure host function (pa_choose_mode, or
+    pa_choose_mode_for_lengths with seq_lens_host, host int32 lengths);
+    ctas_per_sm is the partition kernel's resident CTAs per SM (plan())."""
     if seq_lens_host is None:
-        m = library().pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count)
+        m = library().pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count, ctas_per_sm)
     else:
         import numpy as np
         lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
         if lens.shape != (num_seqs,):
             raise ValueError("seq_lens_host must hold num_seqs lengths")
         m = library().pa_choose_mode_for_lengths(num_seqs, num_kv_heads, max_seq_len, sm_count,
-                                                 lens.ctypes.data)
+                                                 ctas_per_sm, lens.ctypes.data)
     return "v1" if m == _abi.PA_MODE_V1 else "v2"
+
+
+def plan(args: _abi.PaDecodeArgs) -> dict:
+    """What pa_decode would launch for a prepared argument struct on the current
+    device (pa_plan): mode, in-kernel merge, kernels per call, the partition
+    kernel's CTAs per SM, grid and tile count."""
+    pl = _abi.PaLaunchPlan()
+    st = library().pa_plan(ctypes.byref(args), ctypes.byref(pl))
+    if st != _abi.PA_OK:
+        raise PaDecodeError(st)
+    return {"mode": "v1" if pl.mode == _abi.PA_MODE_V1 else "v2",
+            "merge_in_kernel": bool(pl.merge_in_kernel), "kernels": int(pl.kernels),
+            "ctas_per_sm": int(pl.ctas_per_sm), "grid": int(pl.grid), "tiles": int(pl.tiles)}
+
+
+def plan_for(out, query, key_cache, value_cache, block_tables, seq_lens, **kw) -> dict:
+    """plan() for the tensors and keywords pa_decode takes."""
+    import torch
+    args = make_args(out, query, key_cache, value_cache, block_tables, seq_lens, **kw)
+    with torch.cuda.device(query.device):
+        return plan(args)
 
 
 def _dtype_code(t):

@@ -34,7 +34,7 @@ PA_BLOCK_SIZE = 16
 
 # every function include/pa_decode.h declares
 EXPORTED = ("pa_decode", "pa_max_num_partitions", "pa_workspace_elems", "pa_choose_mode",
-            "pa_choose_mode_for_lengths", "pa_workspace_bytes", "pa_partition_size",
+            "pa_choose_mode_for_lengths", "pa_workspace_bytes", "pa_partition_size", "pa_plan",
             "pa_status_str", "pa_version", "pa_decode_static_workspace", "pa_debug_withhold_page")
 
 PA_STATIC_WORKSPACE_FLOATS = 4 * 1024 * 1024
@@ -81,6 +81,17 @@ class PaDecodeArgs(ctypes.Structure):
     ]
 
 
+class PaLaunchPlan(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int32),
+        ("merge_in_kernel", ctypes.c_int32),
+        ("kernels", ctypes.c_int32),
+        ("ctas_per_sm", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("tiles", ctypes.c_int64),
+    ]
+
+
 _lib = None
 
 
@@ -105,19 +116,21 @@ def load(path: Path | None = None):
     lib.pa_max_num_partitions.restype = ctypes.c_int32
     lib.pa_workspace_elems.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(ctypes.c_int64)] * 2
     lib.pa_workspace_elems.restype = ctypes.c_int
-    lib.pa_choose_mode.argtypes = [ctypes.c_int32] * 4
+    lib.pa_choose_mode.argtypes = [ctypes.c_int32] * 5
     lib.pa_choose_mode.restype = ctypes.c_int32
     lib.pa_workspace_bytes.argtypes = [ctypes.c_int32] * 4
     lib.pa_workspace_bytes.restype = ctypes.c_size_t
     lib.pa_partition_size.argtypes = []
     lib.pa_partition_size.restype = ctypes.c_int32
-    lib.pa_choose_mode_for_lengths.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_void_p]
+    lib.pa_choose_mode_for_lengths.argtypes = [ctypes.c_int32] * 5 + [ctypes.c_void_p]
     lib.pa_choose_mode_for_lengths.restype = ctypes.c_int32
     lib.pa_status_str.argtypes = [ctypes.c_int32]
     lib.pa_status_str.restype = ctypes.c_char_p
     lib.pa_version.restype = ctypes.c_int32
     lib.pa_decode_static_workspace.argtypes = [ctypes.POINTER(PaDecodeArgs), ctypes.c_void_p]
     lib.pa_decode_static_workspace.restype = ctypes.c_int
+    lib.pa_plan.argtypes = [ctypes.POINTER(PaDecodeArgs), ctypes.POINTER(PaLaunchPlan)]
+    lib.pa_plan.restype = ctypes.c_int
     lib.pa_debug_withhold_page.argtypes = [ctypes.c_int32, ctypes.c_int64]
     lib.pa_debug_withhold_page.restype = ctypes.c_int
     if path is None:

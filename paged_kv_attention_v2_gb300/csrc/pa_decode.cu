@@ -117,6 +117,213 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 std::atomic<int> g_withhold_page{0};
 std::atomic<int64_t> g_wait_limit_ns{0};
 
+/*
+ * v1 / v2 choice.  The pages pick v2 when the v2 tiles of one sequence (kv
+ * heads x partitions) exceed twice the SM count of their 16-SM part
+ * (should_use_paged_v2 in "ex_engine/factors/attn_dispatch.py").  Here both
+ * modes run the same persistent kernel, so the choice compares its two grids:
+ * v1 makes one tile per (sequence, kv head) over the whole sequence and writes
+ * the output directly; v2 makes one tile per 512-token partition and adds the
+ * partition statistics round trip, an epilogue per partition and the reduce.
+ * v1 measured 2-4 % faster than v2 when its tiles fill the GPU evenly (128 x
+ * 16384 on GB300: 1232 against 1288 us; 64 x 4096: 82.4 against 85.1 us) and
+ * far slower when one long sequence holds a CTA while the others idle.  So:
+ *  - one partition per sequence (max_seq_len <= 512): v1 (v2 would only add
+ *    the round trip);
+ *  - v1 tiles (num_seqs x num_kv_heads) fewer than the SMs: v2;
+ *  - otherwise v1 if the persistent grid's static round-robin of the v1 tiles
+ *    (sm_count x ctas_per_sm resident CTAs, cut to equal rounds, as the launch
+ *    does) loads its busiest CTA with at most 10 % more pages than the mean,
+ *    else v2.
+ * `len(i)` is the length of sequence i, clamped into [0, max_seq_len].
+ */
+template <class Len>
+int32_t choose_by_balance(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t sm_count,
+                          int32_t ctas_per_sm, Len len) {
+    if (max_seq_len <= PA_PARTITION_SIZE) return PA_MODE_V1;
+    if (num_seqs <= 0 || num_kv_heads <= 0 || sm_count <= 0) return PA_MODE_V2;
+    const int64_t tiles = (int64_t)num_seqs * num_kv_heads;
+    if (tiles < sm_count) return PA_MODE_V2;
+    const int64_t resident = (int64_t)sm_count * (ctas_per_sm > 0 ? ctas_per_sm : 2);
+    const int64_t rounds = (tiles + resident - 1) / resident;
+    const int64_t grid = (tiles + rounds - 1) / rounds;
+    std::vector<int64_t> load((size_t)grid, 0);
+    int64_t total = 0;
+    for (int32_t sq = 0; sq < num_seqs; ++sq) {
+        int64_t l = len(sq);
+        l = l < 0 ? 0 : (l > max_seq_len ? max_seq_len : l);
+        const int64_t pages = (l + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
+        for (int32_t h = 0; h < num_kv_heads; ++h) load[(size_t)(((int64_t)sq * num_kv_heads + h) % grid)] += pages;
+        total += pages * num_kv_heads;
+    }
+    int64_t mx = 0;
+    for (int64_t v : load) mx = v > mx ? v : mx;
+    return (double)mx * grid <= 1.1 * (double)total ? PA_MODE_V1 : PA_MODE_V2;
+}
+
+
+// Arguments of one call, checked and turned into kernel parameters.
+struct Prepared {
+    Params p;
+    pa::LaunchArgs la;
+    alignas(64) CUtensorMap tmk;
+    alignas(64) CUtensorMap tmv;
+    int kv = PA_KV_SAME;
+    int ctas_per_sm = 0;
+    bool empty = false;  // num_seqs == 0: nothing to launch
+};
+
+// The kernels of the (query type, cache type) pair: launch them, or with
+// `out` only report the partition kernel's occupancy, grid and merge choice.
+pa_status dispatch(Prepared& pr, pa::LaunchOut* out) {
+    pr.la.query = out;
+    const int kvk = pr.kv == PA_KV_FP8_E4M3 ? pa::kKvE4M3 : pa::kKvE5M2;
+    cudaError_t e;
+    switch (pr.la.dtype) {
+    case PA_DTYPE_F32: e = pa::launch_f32(pr.p, pr.la); break;
+    case PA_DTYPE_F16: e = pr.kv == PA_KV_SAME ? pa::launch_f16(pr.p, pr.la) : pa::launch_f16_fp8(pr.p, pr.la, kvk); break;
+    default: e = pr.kv == PA_KV_SAME ? pa::launch_bf16(pr.p, pr.la) : pa::launch_bf16_fp8(pr.p, pr.la, kvk); break;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+// Host-visible checks of pa_decode (every error returned before any launch),
+// then the kernel parameters, the v1 / v2 choice and the tile order.
+pa_status prepare(const pa_decode_args* a, void* stream, Prepared& pr) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (a->num_seqs < 0 || a->num_heads <= 0 || a->num_kv_heads <= 0 || a->max_seq_len < 0 ||
+        a->num_blocks < 0 || a->max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_heads % a->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (a->dtype != PA_DTYPE_F32 && a->dtype != PA_DTYPE_F16 && a->dtype != PA_DTYPE_BF16)
+        return PA_ERR_INVALID_ARG;
+    if (a->layout != PA_LAYOUT_SPLIT && a->layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
+    if (a->mode != PA_MODE_AUTO && a->mode != PA_MODE_V1 && a->mode != PA_MODE_V2)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(a->scale) || !std::isfinite(a->softcap) || !std::isfinite(a->k_scale) ||
+        !std::isfinite(a->v_scale))
+        return PA_ERR_INVALID_ARG;
+    const int kv = a->kv_dtype;
+    if (kv != PA_KV_SAME && kv != PA_KV_FP8_E4M3 && kv != PA_KV_FP8_E5M2) return PA_ERR_INVALID_ARG;
+    if (kv != PA_KV_SAME && a->dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
+    if (a->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
+    if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
+    const int group = a->num_heads / a->num_kv_heads;
+    if (group > 16) return PA_ERR_UNSUPPORTED;
+    // several query tokens per sequence: all tokens of a (sequence, kv head)
+    // share one tile, their group rows side by side (at most 16)
+    const bool multi = a->query_start != nullptr;
+    const int max_q = multi ? a->max_query_len : 1;
+    if (multi && (a->max_query_len < 1 || a->num_query_tokens < 0 || !aligned(a->query_start, 4)))
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)max_q * group > 16) return PA_ERR_UNSUPPORTED;
+    if (a->num_seqs == 0) {
+        pr.empty = true;
+        return PA_OK;
+    }
+    if (!a->out || !a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (a->num_blocks == 0) return PA_ERR_INVALID_ARG;
+    if ((int64_t)a->max_blocks_per_seq * PA_BLOCK_SIZE < (int64_t)a->max_seq_len)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(a->out, 16) || !aligned(a->query, 16) || !aligned(a->key_cache, 16) ||
+        !aligned(a->value_cache, 16) || !aligned(a->block_tables, 4) || !aligned(a->seq_lens, 4) ||
+        !aligned(a->alibi_slopes, 4) || !aligned(a->partition_counters, 4))
+        return PA_ERR_INVALID_ARG;
+    const int max_parts = pa_max_num_partitions(a->max_seq_len);
+    auto workspace_ok = [a] {
+        return a->exp_sums && a->max_logits && a->tmp_out && aligned(a->tmp_out, 16) &&
+               aligned(a->exp_sums, 4) && aligned(a->max_logits, 4);
+    };
+    // v2 asked for: the workspace is checked before anything touches the device
+    // (AUTO checks it once the mode is chosen)
+    if (a->mode == PA_MODE_V2 && !workspace_ok()) return PA_ERR_WORKSPACE;
+    if ((int64_t)a->num_seqs * max_q * a->num_heads >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)a->num_seqs * max_parts * a->num_kv_heads >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
+
+    int sm = 0;
+    if (sm_count_for_current_device(&sm) != 0) return PA_ERR_LAUNCH;
+
+    Params& p = pr.p;
+    std::memset(&p, 0, sizeof p);
+    p.query = a->query;
+    p.key_cache = a->key_cache;
+    p.value_cache = a->value_cache;
+    p.block_tables = a->block_tables;
+    p.seq_lens = a->seq_lens;
+    p.alibi = a->alibi_slopes;
+    p.out = a->out;
+    p.exp_sums = a->exp_sums;
+    p.max_logits = a->max_logits;
+    p.tmp_out = a->tmp_out;
+    p.dev_error = a->dev_error;
+    p.num_seqs = a->num_seqs;
+    p.num_heads = a->num_heads;
+    p.num_kv_heads = a->num_kv_heads;
+    p.group = group;
+    p.num_blocks = a->num_blocks;
+    p.max_blocks_per_seq = a->max_blocks_per_seq;
+    p.max_seq_len = a->max_seq_len;
+    p.max_parts = max_parts;
+    const float k_scale = (kv != PA_KV_SAME && a->k_scale > 0.f) ? a->k_scale : 1.f;
+    p.scale = a->scale * k_scale;  // q.(k_scale k8) = k_scale (q.k8): folded into the logit scale
+    p.v_scale = (kv != PA_KV_SAME && a->v_scale > 0.f) ? a->v_scale : 1.f;
+    p.softcap = a->softcap > 0.f ? a->softcap : 0.f;
+    p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
+    p.counters = a->partition_counters;
+    p.window_left = a->sliding_window > 0 ? a->sliding_window - 1 : -1;
+    p.query_start = a->query_start;
+    p.max_q_len = max_q;
+    p.num_q_rows = multi ? a->num_query_tokens : a->num_seqs;
+    p.fused = 0;  // decided at launch, once the persistent grid size is known
+    p.wait_limit_ns = (uint64_t)g_wait_limit_ns.load();
+    p.withhold_page = g_withhold_page.load();
+
+    pa::LaunchArgs& la = pr.la;
+    std::memset(&la, 0, sizeof la);
+    la.stream = static_cast<cudaStream_t>(stream);
+    la.tmk = &pr.tmk;
+    la.tmv = &pr.tmv;
+    std::memset(&pr.tmk, 0, sizeof pr.tmk);
+    std::memset(&pr.tmv, 0, sizeof pr.tmv);
+    la.sm_count = sm;
+    la.group_tiles = max_q * group > 8 ? 2 : 1;
+    la.layout = a->layout;
+    la.head_size = a->head_size;
+    la.dtype = a->dtype;
+    la.ev_begin = a->event_main_begin;
+    la.ev_end = a->event_main_end;
+    pr.kv = kv;
+
+    // resident CTAs per SM of the partition kernel of this call (the same
+    // kernel runs v1 and v2): the persistent grid and the v1 / v2 choice use it
+    {
+        pa::LaunchOut lo;
+        la.tiles_upper = 1;
+        if (dispatch(pr, &lo) != PA_OK) return PA_ERR_LAUNCH;
+        pr.ctas_per_sm = lo.occ;
+    }
+    int mode = a->mode;
+    if (mode == PA_MODE_AUTO)
+        mode = pa_choose_mode_for_lengths(a->num_seqs, a->num_kv_heads, a->max_seq_len, sm, pr.ctas_per_sm,
+                                          a->seq_lens_host);
+    const bool v1 = mode == PA_MODE_V1;
+    if (!v1 && !workspace_ok()) return PA_ERR_WORKSPACE;
+    p.v1 = v1 ? 1 : 0;
+    la.tiles_upper = (int64_t)a->num_seqs * (v1 ? 1 : max_parts) * a->num_kv_heads;
+    // KV copies marked evict_first while the partition outputs (at most the
+    // workspace) take no more than half of L2; with larger workspaces it was
+    // measured to slow the partition kernel (128 x 16384: +1.6 %)
+    {
+        int l2 = 0;
+        if (l2_bytes_for_current_device(&l2) != 0) return PA_ERR_LAUNCH;
+        const int64_t rows = multi ? a->num_query_tokens : a->num_seqs;
+        const int64_t tmp_bytes = v1 ? 0 : rows * a->num_heads * (int64_t)max_parts * a->head_size * 4;
+        p.kv_evict_first = tmp_bytes <= (int64_t)l2 / 2 ? 1 : 0;
+    }
+    return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -145,59 +352,21 @@ size_t pa_workspace_bytes(int32_t rows, int32_t num_heads, int32_t head_size, in
 
 int32_t pa_partition_size(void) { return PA_PARTITION_SIZE; }
 
-/*
- * v1 / v2 choice.  The pages pick v2 when the v2 tiles of one sequence
- * (kv heads x partitions) exceed twice the SM count.  Here the choice is
- * between two grids of the same persistent kernel: v1 makes one tile per
- * (sequence, kv head) and writes the output directly; v2 makes one tile per
- * 512-token partition and adds the partition statistics round trip and the
- * reduce launch.  With a single partition per sequence v2 only adds that
- * overhead, so v1 is chosen; with longer sequences v1 keeps one CTA busy per
- * (sequence, kv head), which leaves SMs idle unless there are many such pairs
- * per SM of equal length, so v2 is chosen.
- */
-int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
-                       int32_t sm_count) {
-    (void)num_seqs;
-    (void)num_kv_heads;
-    (void)sm_count;
-    if (max_seq_len <= PA_PARTITION_SIZE) return PA_MODE_V1;
-    return PA_MODE_V2;
+/* Without host lengths every sequence is taken to be max_seq_len long (the
+ * pages' rule decides from one length too). */
+int32_t pa_choose_mode(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len, int32_t sm_count,
+                       int32_t ctas_per_sm) {
+    return choose_by_balance(num_seqs, num_kv_heads, max_seq_len, sm_count, ctas_per_sm,
+                             [max_seq_len](int32_t) { return (int64_t)max_seq_len; });
 }
 
-/*
- * With the lengths known on the host: v1 needs no partition statistics, no
- * epilogue per 512 tokens and no reduce launch, which measured 2-4 % faster
- * than v2 for batches whose (sequence, kv head) tiles fill the GPU evenly
- * (128 x 16384 on GB300: 1232 against 1288 us; 64 x 4096: 82.4 against
- * 85.1 us), and far slower when one long sequence holds a CTA while the rest
- * idle (ragged batches).  So v1 is taken when its tiles are at least one per
- * SM and the static round-robin of the persistent grid (two CTAs per SM, cut
- * to equal rounds) loads the busiest CTA with at most 10 % more pages than the
- * mean.
- */
 int32_t pa_choose_mode_for_lengths(int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
-                                   int32_t sm_count, const int32_t* seq_lens_host) {
-    if (max_seq_len <= PA_PARTITION_SIZE) return PA_MODE_V1;
-    if (!seq_lens_host || num_seqs <= 0 || num_kv_heads <= 0 || sm_count <= 0) return PA_MODE_V2;
-    const int64_t tiles = (int64_t)num_seqs * num_kv_heads;
-    if (tiles < sm_count) return PA_MODE_V2;
-    const int64_t resident = 2 * (int64_t)sm_count;
-    const int64_t rounds = (tiles + resident - 1) / resident;
-    const int64_t grid = (tiles + rounds - 1) / rounds;
-    std::vector<int64_t> load((size_t)grid, 0);
-    int64_t total = 0;
-    for (int32_t sq = 0; sq < num_seqs; ++sq) {
-        int64_t len = seq_lens_host[sq];
-        len = len < 0 ? 0 : (len > max_seq_len ? max_seq_len : len);
-        const int64_t pages = (len + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE;
-        for (int32_t h = 0; h < num_kv_heads; ++h) load[(size_t)(((int64_t)sq * num_kv_heads + h) % grid)] += pages;
-        total += pages * num_kv_heads;
-    }
-    int64_t mx = 0;
-    for (int64_t v : load) mx = v > mx ? v : mx;
-    return (double)mx * grid <= 1.1 * (double)total ? PA_MODE_V1 : PA_MODE_V2;
+                                   int32_t sm_count, int32_t ctas_per_sm, const int32_t* seq_lens_host) {
+    if (!seq_lens_host) return pa_choose_mode(num_seqs, num_kv_heads, max_seq_len, sm_count, ctas_per_sm);
+    return choose_by_balance(num_seqs, num_kv_heads, max_seq_len, sm_count, ctas_per_sm,
+                             [seq_lens_host](int32_t i) { return (int64_t)seq_lens_host[i]; });
 }
+
 
 const char* pa_status_str(int32_t status) {
     switch (status) {
@@ -219,148 +388,40 @@ pa_status pa_debug_withhold_page(int32_t enable, int64_t wait_limit_ns) {
     return PA_OK;
 }
 
+pa_status pa_plan(const pa_decode_args* a, pa_launch_plan* plan) {
+    if (!plan) return PA_ERR_INVALID_ARG;
+    std::memset(plan, 0, sizeof *plan);
+    Prepared pr;
+    const pa_status st = prepare(a, nullptr, pr);
+    if (st != PA_OK || pr.empty) return st;
+    pa::LaunchOut lo;
+    const pa_status q = dispatch(pr, &lo);
+    if (q != PA_OK) return q;
+    plan->mode = pr.p.v1 ? PA_MODE_V1 : PA_MODE_V2;
+    plan->merge_in_kernel = lo.fused ? 1 : 0;
+    plan->kernels = (pr.p.v1 || lo.fused) ? 1 : 2;
+    plan->ctas_per_sm = pr.ctas_per_sm;
+    plan->grid = (int32_t)lo.grid;
+    plan->tiles = pr.la.tiles_upper;
+    return PA_OK;
+}
+
 pa_status pa_decode(const pa_decode_args* a, void* stream) {
-    if (!a) return PA_ERR_INVALID_ARG;
-    if (a->num_seqs < 0 || a->num_heads <= 0 || a->num_kv_heads <= 0 || a->max_seq_len < 0 ||
-        a->num_blocks < 0 || a->max_blocks_per_seq < 0)
-        return PA_ERR_INVALID_ARG;
-    if (a->num_heads % a->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-    if (a->dtype != PA_DTYPE_F32 && a->dtype != PA_DTYPE_F16 && a->dtype != PA_DTYPE_BF16)
-        return PA_ERR_INVALID_ARG;
-    if (a->layout != PA_LAYOUT_SPLIT && a->layout != PA_LAYOUT_NHD) return PA_ERR_INVALID_ARG;
-    if (a->mode != PA_MODE_AUTO && a->mode != PA_MODE_V1 && a->mode != PA_MODE_V2)
-        return PA_ERR_INVALID_ARG;
-    if (!std::isfinite(a->scale) || !std::isfinite(a->softcap) || !std::isfinite(a->k_scale) ||
-        !std::isfinite(a->v_scale))
-        return PA_ERR_INVALID_ARG;
-    const int kv = a->kv_dtype;
-    if (kv != PA_KV_SAME && kv != PA_KV_FP8_E4M3 && kv != PA_KV_FP8_E5M2) return PA_ERR_INVALID_ARG;
-    if (kv != PA_KV_SAME && a->dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
-    if (a->block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
-    if (a->head_size != 64 && a->head_size != 128) return PA_ERR_UNSUPPORTED;
-    const int group = a->num_heads / a->num_kv_heads;
-    if (group > 16) return PA_ERR_UNSUPPORTED;
-    // several query tokens per sequence: all tokens of a (sequence, kv head)
-    // share one tile, their group rows side by side (at most 16)
-    const bool multi = a->query_start != nullptr;
-    const int max_q = multi ? a->max_query_len : 1;
-    if (multi && (a->max_query_len < 1 || a->num_query_tokens < 0 || !aligned(a->query_start, 4)))
-        return PA_ERR_INVALID_ARG;
-    if ((int64_t)max_q * group > 16) return PA_ERR_UNSUPPORTED;
-    if (a->num_seqs == 0) return PA_OK;
-    if (!a->out || !a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->seq_lens)
-        return PA_ERR_INVALID_ARG;
-    if (a->num_blocks == 0) return PA_ERR_INVALID_ARG;
-    if ((int64_t)a->max_blocks_per_seq * PA_BLOCK_SIZE < (int64_t)a->max_seq_len)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned(a->out, 16) || !aligned(a->query, 16) || !aligned(a->key_cache, 16) ||
-        !aligned(a->value_cache, 16) || !aligned(a->block_tables, 4) || !aligned(a->seq_lens, 4) ||
-        !aligned(a->alibi_slopes, 4) || !aligned(a->partition_counters, 4))
-        return PA_ERR_INVALID_ARG;
-
-    int sm = 0;
-    int mode = a->mode;
-    if (mode == PA_MODE_AUTO) {
-        if (sm_count_for_current_device(&sm) != 0) return PA_ERR_LAUNCH;
-        mode = pa_choose_mode_for_lengths(a->num_seqs, a->num_kv_heads, a->max_seq_len, sm,
-                                          a->seq_lens_host);
-    }
-    const bool v1 = mode == PA_MODE_V1;
-    const int max_parts = pa_max_num_partitions(a->max_seq_len);
-    if (!v1) {
-        if (!a->exp_sums || !a->max_logits || !a->tmp_out) return PA_ERR_WORKSPACE;
-        if (!aligned(a->tmp_out, 16) || !aligned(a->exp_sums, 4) || !aligned(a->max_logits, 4))
-            return PA_ERR_WORKSPACE;
-    }
-    if (sm == 0 && sm_count_for_current_device(&sm) != 0) return PA_ERR_LAUNCH;
-    const int64_t units = (int64_t)a->num_seqs * (v1 ? 1 : max_parts);
-    const int64_t tiles = units * a->num_kv_heads;
-    if (tiles >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
-    // reduce grid: one CTA per (sequence, query token, head)
-    if ((int64_t)a->num_seqs * max_q * a->num_heads >= (int64_t)1 << 31) return PA_ERR_UNSUPPORTED;
-
-    Params p;
-    std::memset(&p, 0, sizeof p);
-    p.query = a->query;
-    p.key_cache = a->key_cache;
-    p.value_cache = a->value_cache;
-    p.block_tables = a->block_tables;
-    p.seq_lens = a->seq_lens;
-    p.alibi = a->alibi_slopes;
-    p.out = a->out;
-    p.exp_sums = a->exp_sums;
-    p.max_logits = a->max_logits;
-    p.tmp_out = a->tmp_out;
-    p.dev_error = a->dev_error;
-    p.num_seqs = a->num_seqs;
-    p.num_heads = a->num_heads;
-    p.num_kv_heads = a->num_kv_heads;
-    p.group = group;
-    p.num_blocks = a->num_blocks;
-    p.max_blocks_per_seq = a->max_blocks_per_seq;
-    p.max_seq_len = a->max_seq_len;
-    p.max_parts = max_parts;
-    const float k_scale = (kv != PA_KV_SAME && a->k_scale > 0.f) ? a->k_scale : 1.f;
-    p.scale = a->scale * k_scale;  // q.(k_scale k8) = k_scale (q.k8): folded into the logit scale
-    p.v_scale = (kv != PA_KV_SAME && a->v_scale > 0.f) ? a->v_scale : 1.f;
-    p.softcap = a->softcap > 0.f ? a->softcap : 0.f;
-    p.inv_softcap = a->softcap > 0.f ? 1.f / a->softcap : 0.f;
-    p.v1 = v1 ? 1 : 0;
-    p.counters = a->partition_counters;
-    p.window_left = a->sliding_window > 0 ? a->sliding_window - 1 : -1;
-    p.query_start = a->query_start;
-    p.max_q_len = max_q;
-    p.num_q_rows = multi ? a->num_query_tokens : a->num_seqs;
-    p.fused = 0;  // decided at launch, once the persistent grid size is known
-    p.wait_limit_ns = (uint64_t)g_wait_limit_ns.load();
-    // KV copies marked evict_first while the partition outputs (at most the
-    // workspace) take no more than half of L2; with larger workspaces it was
-    // measured to slow the partition kernel (128 x 16384: +1.6 %)
-    {
-        int l2 = 0;
-        if (l2_bytes_for_current_device(&l2) != 0) return PA_ERR_LAUNCH;
-        const int64_t rows = multi ? a->num_query_tokens : a->num_seqs;
-        const int64_t tmp_bytes = v1 ? 0 : rows * a->num_heads * (int64_t)max_parts * a->head_size * 4;
-        p.kv_evict_first = tmp_bytes <= (int64_t)l2 / 2 ? 1 : 0;
-    }
-    p.withhold_page = g_withhold_page.load();
-
-    alignas(64) CUtensorMap tmk, tmv;
-    std::memset(&tmk, 0, sizeof tmk);
-    std::memset(&tmv, 0, sizeof tmv);
-    const int group_tiles = max_q * group > 8 ? 2 : 1;
+    Prepared pr;
+    const pa_status st = prepare(a, stream, pr);
+    if (st != PA_OK || pr.empty) return st;
     // NHD pages come through tensor maps
     if (a->layout == PA_LAYOUT_NHD) {
         const int64_t rows = (int64_t)a->num_blocks * a->num_kv_heads * PA_BLOCK_SIZE;
         if (rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;  // tensor-map row coordinate is int32
-        const bool ok = kv != PA_KV_SAME
-                            ? make_nhd_map_fp8(&tmk, a->key_cache, rows, a->head_size) &&
-                                  make_nhd_map_fp8(&tmv, a->value_cache, rows, a->head_size)
-                            : make_nhd_map(&tmk, a->key_cache, rows, a->head_size, (pa_dtype)a->dtype) &&
-                                  make_nhd_map(&tmv, a->value_cache, rows, a->head_size, (pa_dtype)a->dtype);
+        const bool ok = pr.kv != PA_KV_SAME
+                            ? make_nhd_map_fp8(&pr.tmk, a->key_cache, rows, a->head_size) &&
+                                  make_nhd_map_fp8(&pr.tmv, a->value_cache, rows, a->head_size)
+                            : make_nhd_map(&pr.tmk, a->key_cache, rows, a->head_size, (pa_dtype)a->dtype) &&
+                                  make_nhd_map(&pr.tmv, a->value_cache, rows, a->head_size, (pa_dtype)a->dtype);
         if (!ok) return PA_ERR_LAUNCH;
     }
-
-    pa::LaunchArgs la;
-    la.stream = static_cast<cudaStream_t>(stream);
-    la.tmk = &tmk;
-    la.tmv = &tmv;
-    la.sm_count = sm;
-    la.tiles_upper = tiles;
-    la.group_tiles = group_tiles;
-    la.layout = a->layout;
-    la.head_size = a->head_size;
-    la.ev_begin = a->event_main_begin;
-    la.ev_end = a->event_main_end;
-
-    cudaError_t e;
-    const int kvk = kv == PA_KV_FP8_E4M3 ? pa::kKvE4M3 : pa::kKvE5M2;
-    switch (a->dtype) {
-    case PA_DTYPE_F32: e = pa::launch_f32(p, la); break;
-    case PA_DTYPE_F16: e = kv == PA_KV_SAME ? pa::launch_f16(p, la) : pa::launch_f16_fp8(p, la, kvk); break;
-    default: e = kv == PA_KV_SAME ? pa::launch_bf16(p, la) : pa::launch_bf16_fp8(p, la, kvk); break;
-    }
-    return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+    return dispatch(pr, nullptr);
 }
 
 }  // extern "C"

@@ -49,6 +49,7 @@ constexpr int kStagesFp8Pairs = 8; // fp8 NHD caches with one n-tile: two pages 
 constexpr int kStagesF32 = 4;      // fp32 caches, one n-tile (two CTAs per SM)
 constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
 constexpr int kConsumerWarps = 4;  // consumer warps per CTA
+constexpr int kPrefetchPages = 16; // pages of the first tile prefetched into L2 before the grid wait
 constexpr int kReduceWarpMaxParts = 64;  // warp-per-row reduce up to this many partitions per row
 
 constexpr int kReduceWarpsPerCta = 8;  // warp-per-row reduce: rows per CTA
@@ -214,6 +215,53 @@ __device__ __forceinline__ bool consumer_sync(const Smem& sm, uint32_t& phase, i
 
 // ------------------------------------------------------------------ producer
 
+// The (sequence, partition) of tile unit u when every sequence of the batch
+// has max_parts partitions and there is no window (v1: one unit per
+// sequence).  The producer's walk of seq_lens finds the real one; this guess
+// lets the first tile's loads start before that walk.
+__device__ __forceinline__ void guess_unit(const Params& p, int u, int& seq, int& part) {
+    if (p.v1) {
+        seq = u;
+        part = 0;
+    } else {
+        seq = u / p.max_parts;
+        part = u - seq * p.max_parts;
+    }
+}
+
+// Run before the wait for the previous grid in the stream (programmatic
+// dependent launch), while that grid finishes: prefetch into L2 the first
+// pages of K and V of this CTA's first tile (guessed as above) and its query
+// rows.  The inputs may still be written by the previous grid, so everything
+// read here only steers the prefetch: lengths and block ids are read through
+// L2 only (no L1 line is left behind for the reads after the wait), lengths
+// are clamped and block ids outside the pool are skipped.
+template <class C, int HEAD>
+__device__ void prefetch_first_tile(const Params& p, int lane) {
+    if (p.window_left >= 0 || p.withhold_page) return;
+    const int Hkv = p.num_kv_heads;
+    const int u = (int)blockIdx.x / Hkv, kvh = (int)blockIdx.x - u * Hkv;
+    int seq, part;
+    guess_unit(p, u, seq, part);
+    if (seq >= p.num_seqs) return;
+    const int len = clamp_len(p, __ldcg(p.seq_lens + seq));
+    const int tb = part * kPart;
+    const int te = p.v1 ? len : min(len, tb + kPart);
+    const int npg = min(kPrefetchPages, tile_pages(tb, te));
+    if (lane < npg) {
+        const int blk = __ldcg(p.block_tables + (int64_t)seq * p.max_blocks_per_seq + tb / kBS + lane);
+        if ((unsigned)blk < (unsigned)p.num_blocks) {
+            const int64_t off = ((int64_t)blk * Hkv + kvh) * C::kPageBytes;
+            bulk_prefetch_l2(static_cast<const char*>(p.key_cache) + off, C::kPageBytes);
+            bulk_prefetch_l2(static_cast<const char*>(p.value_cache) + off, C::kPageBytes);
+        }
+    }
+    if (!C::kMQ && lane == 31)
+        bulk_prefetch_l2(static_cast<const char*>(p.query) +
+                             ((int64_t)seq * p.num_heads + (int64_t)kvh * p.group) * HEAD * C::kElem,
+                         (uint32_t)(p.group * HEAD * C::kElem));
+}
+
 struct ProducerTile {
     int seq, kvh, part, tb, te, len, npages, q0, qn;
     bool valid;
@@ -266,9 +314,9 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     // in parallel with the walk, and keep them only if the walk confirms the tile.
     int spec_seq = -1, spec_tb = 0, spec_ids = 0;
     if (!p.v1 && p.window_left < 0) {
-        const int u = blockIdx.x / Hkv;
-        spec_seq = u / p.max_parts;
-        spec_tb = (u - spec_seq * p.max_parts) * kPart;
+        int spec_part;
+        guess_unit(p, (int)blockIdx.x / Hkv, spec_seq, spec_part);
+        spec_tb = spec_part * kPart;
         const int idx = spec_tb / kBS + lane;
         if (spec_seq < S && idx < p.max_blocks_per_seq)
             spec_ids = __ldg(p.block_tables + (int64_t)spec_seq * p.max_blocks_per_seq + idx);
@@ -536,69 +584,82 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
 // Fused v2 merge, run by the NC consumer warps of the CTA that finished the
 // last partition of (d.seq, d.kvh): Phase 2 for the group's heads, reading the
 // partition statistics the other CTAs wrote (L2 loads: never a stale L1 line).
+// The fused path has at most PA_FUSED_MAX_PARTITIONS partitions per row, so a
+// thread issues every load of two (row, 4-column) items -- statistics and
+// partition outputs of all partitions -- before any arithmetic: one round
+// trip to L2 per pair of items.
 template <typename T, int HEAD, int NC, bool MQ>
 __device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
     constexpr int D4 = HEAD / 4;
+    constexpr int PM = PA_FUSED_MAX_PARTITIONS;
+    constexpr int NI = 1;  // items in flight per thread
     const int G = p.group;
     const int qn = MQ ? d.qn : 1;
-    for (int idx = tid; idx < qn * G * D4; idx += NC * 32) {
-        const int h = idx / D4, d4 = idx - h * D4;
-        const int qi = MQ ? h / G : 0;
-        const int hi = d.len - qn + qi;                       // the query token's position
-        const int P = hi >= 0 ? (hi + kPart) / kPart : 0;      // partitions up to it
-        const int p0 = window_lo_at(p, hi) / kPart;            // partitions before p0: outside the window
-        const int64_t sh = (int64_t)(d.q0 + qi) * p.num_heads + d.kvh * G + (h - qi * G);
-        const float* ml = p.max_logits + sh * p.max_parts;
-        const float* es = p.exp_sums + sh * p.max_parts;
-        const float* tmp = p.tmp_out + sh * p.max_parts * HEAD + 4 * d4;
-        float M = -INFINITY, W = 0.f;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q0 = p0; q0 < P; q0 += 4) {
-            float mq[4], eq[4];
-            float4 t[4];
+    const int n = qn * G * D4;
+    for (int idx0 = tid; idx0 < n; idx0 += NI * NC * 32) {
+        float mq[NI][PM], eq[NI][PM];
+        float4 t[NI][PM];
+        int64_t sh[NI];
+        int d4s[NI];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = q0 + u;
-                if (q < P) {
-                    mq[u] = __ldcg(ml + q);
-                    eq[u] = __ldcg(es + q);
-                    t[u] = __ldcg(reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD));
-                } else {
-                    mq[u] = -INFINITY;
-                    eq[u] = 0.f;
-                    t[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int it = 0; it < NI; ++it) {
+            const int idx = idx0 + it * NC * 32;
+            int P = 0, p0 = 0;
+            sh[it] = 0;
+            d4s[it] = 0;
+            if (idx < n) {
+                const int h = idx / D4;
+                d4s[it] = idx - h * D4;
+                const int qi = MQ ? h / G : 0;
+                const int hi = d.len - qn + qi;                  // the query token's position
+                P = hi >= 0 ? min((hi + kPart) / kPart, PM) : 0;  // partitions up to it
+                p0 = window_lo_at(p, hi) / kPart;                 // before p0: outside the window
+                sh[it] = (int64_t)(d.q0 + qi) * p.num_heads + d.kvh * G + (h - qi * G);
             }
+            const float* ml = p.max_logits + sh[it] * p.max_parts;
+            const float* es = p.exp_sums + sh[it] * p.max_parts;
+            const float* tmp = p.tmp_out + sh[it] * p.max_parts * HEAD + 4 * d4s[it];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (mq[u] == -INFINITY) continue;
-                if (mq[u] > M) {  // online rescale to the new running max
-                    const float sc = (M == -INFINITY) ? 0.f : expf(M - mq[u]);
-                    a.x *= sc;
-                    a.y *= sc;
-                    a.z *= sc;
-                    a.w *= sc;
-                    W *= sc;
-                    M = mq[u];
+            for (int q = 0; q < PM; ++q) {
+                if (q >= p0 && q < P) {
+                    mq[it][q] = __ldcg(ml + q);
+                    eq[it][q] = __ldcg(es + q);
+                    t[it][q] = __ldcg(reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD));
+                } else {
+                    mq[it][q] = -INFINITY;
+                    eq[it][q] = 0.f;
+                    t[it][q] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const float c = expf(mq[u] - M) * eq[u];
-                a.x += c * t[u].x;
-                a.y += c * t[u].y;
-                a.z += c * t[u].z;
-                a.w += c * t[u].w;
-                W += c;
             }
         }
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        T* dst = static_cast<T*>(p.out) + sh * HEAD + 4 * d4;
-        if constexpr (std::is_same<T, float>::value) {
-            *reinterpret_cast<float4*>(dst) = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        } else {
-            constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
-            uint2 v;
-            v.x = pack2<BF>(a.x * inv, a.y * inv);
-            v.y = pack2<BF>(a.z * inv, a.w * inv);
-            *reinterpret_cast<uint2*>(dst) = v;
+#pragma unroll
+        for (int it = 0; it < NI; ++it) {
+            if (idx0 + it * NC * 32 >= n) break;
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < PM; ++q) M = fmaxf(M, mq[it][q]);
+            float W = 0.f;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < PM; ++q) {
+                const float c = mq[it][q] == -INFINITY ? 0.f : expf(mq[it][q] - M) * eq[it][q];
+                a.x += c * t[it][q].x;
+                a.y += c * t[it][q].y;
+                a.z += c * t[it][q].z;
+                a.w += c * t[it][q].w;
+                W += c;
+            }
+            const float inv = W > 0.f ? 1.f / W : 0.f;
+            T* dst = static_cast<T*>(p.out) + sh[it] * HEAD + 4 * d4s[it];
+            if constexpr (std::is_same<T, float>::value) {
+                *reinterpret_cast<float4*>(dst) = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+            } else {
+                constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+                uint2 v;
+                v.x = pack2<BF>(a.x * inv, a.y * inv);
+                v.y = pack2<BF>(a.z * inv, a.w * inv);
+                *reinterpret_cast<uint2*>(dst) = v;
+            }
         }
     }
 }
@@ -639,10 +700,11 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     if (!consumer_sync(sm, mphase, lane)) return false;  // epilogue done, merge buffers free
     if (!p.fused || p.v1) return true;
     if (tid == 0) {
-        __threadfence();  // this CTA's partition results before its arrival
         const int P = (d.len + kPart - 1) / kPart - window_lo(p, d.len, d.qn) / kPart;
         const int units = P > 0 ? P : 1;
-        const int old = atomicAdd(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
+        // releases this CTA's partition results (every warp's, seen through the
+        // barrier above) before the count; acquires the others' with it
+        const int old = atom_add_acq_rel_gpu(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
         sm.abort[2] = (old == units - 1) ? 1 : 0;
     }
     if (!consumer_sync(sm, mphase, lane)) return false;
@@ -1730,6 +1792,7 @@ __global__ void __launch_bounds__((NC + 1) * 32,
     sm.wait_ns = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == NC) prefetch_first_tile<C, HEAD>(p, lane);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(sm.full + s * 8, 1);

@@ -11,8 +11,16 @@
 
 namespace pa {
 
+// What a launch would do, reported instead of launching (see LaunchArgs::query).
+struct LaunchOut {
+    int occ = 0;        // resident CTAs per SM of the partition kernel
+    int64_t grid = 0;   // CTAs of its persistent grid
+    bool fused = false; // Phase 2 merge inside the partition kernel (no reduce launch)
+};
+
 struct LaunchArgs {
     cudaStream_t stream;
+    LaunchOut* query;        // non-null: fill it and launch nothing
     const CUtensorMap* tmk;  // NHD 16-bit only (otherwise unused placeholders)
     const CUtensorMap* tmv;
     int sm_count;
@@ -20,6 +28,7 @@ struct LaunchArgs {
     int group_tiles;         // 1 or 2: n-tiles of 8 query heads
     int layout;
     int head_size;
+    int dtype;               // pa_dtype of the query
     void* ev_begin;
     void* ev_end;
 };
@@ -71,6 +80,12 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     p.fused = (!p.v1 && p.counters && p.max_parts <= PA_FUSED_MAX_PARTITIONS &&
                la.tiles_upper <= grid) ? 1 : 0;
     *fused = p.fused != 0;
+    if (la.query) {
+        la.query->occ = occ;
+        la.query->grid = grid;
+        la.query->fused = *fused;
+        return cudaSuccess;
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -164,7 +179,7 @@ cudaError_t launch_family(const Params& p, const LaunchArgs& la) {
         e = la.group_tiles == 2 ? launch_layout<T, 64, 2, KV>(p, la, &fused)
                                 : launch_layout<T, 64, 1, KV>(p, la, &fused);
     }
-    if (e != cudaSuccess || p.v1 || fused) return e;
+    if (e != cudaSuccess || p.v1 || fused || la.query) return e;
     if (p.query_start)
         return la.head_size == 128 ? launch_reduce<T, 128, true>(p, la) : launch_reduce<T, 64, true>(p, la);
     return la.head_size == 128 ? launch_reduce<T, 128, false>(p, la) : launch_reduce<T, 64, false>(p, la);

@@ -115,6 +115,12 @@ __device__ __forceinline__ void tensor3d_g2s_hint(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (a hint: no completion, no data
+// returned).  src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -180,6 +186,15 @@ __device__ __forceinline__ float2 ld_global_v2_hint(const float* ptr, uint64_t p
                  : "l"(ptr), "l"(pol)
                  : "memory");
     return v;
+}
+
+// atomicAdd with acquire-release semantics at GPU scope: releases this
+// thread's earlier writes (and those it observed) before the add, acquires
+// the writes released before the value it reads.  Returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* ptr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------------- named barrier

@@ -46,19 +46,14 @@ def to_device(w, device="cuda:0"):
     return d
 
 
-def auto_mode(w, device="cuda:0"):
-    """What mode "auto" picks for w (with its host lengths, as run_gpu passes them)."""
-    sm = torch.cuda.get_device_properties(device).multi_processor_count
-    return pa.choose_mode(w.num_seqs, w.num_kv_heads, w.max_seq_len, sm, w.seq_lens)
-
-
 def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_lens=None,
             block_tables=None, poison_workspace=True, counters=None, calls=1):
     """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error.
 
     mode "v2f" is v2 with partition counters (the merge inside the partition
-    kernel when the partition count allows it); `counters` may pass an existing
-    counter tensor, which must be all zero again after every call."""
+    kernel where the library's rule allows it); `counters` may pass an
+    existing counter tensor, which must be all zero again after every call.
+    The result holds the library's plan of the call ("plan")."""
     dev = dev or to_device(w, device)
     fused = mode == "v2f"
     if fused:
@@ -76,17 +71,19 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
         for t in ws.values():
             t.fill_(float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device=device)
+    call = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
+                alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
+                mode=mode, dev_error=err, partition_counters=counters,
+                seq_lens_host=w.seq_lens if mode == "auto" else None,
+                window_left=getattr(w, "window_left", -1),
+                kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
+                v_scale=getattr(w, "v_scale", 1.0), **mq, **ws)
+    tensors = (out, dev["query"], dev["key_cache"], dev["value_cache"],
+               dev["block_tables"] if block_tables is None else block_tables,
+               dev["seq_lens"] if seq_lens is None else seq_lens)
+    plan = pa.plan_for(*tensors, **call)
     for _ in range(calls):
-        pa.pa_decode(out, dev["query"], dev["key_cache"], dev["value_cache"],
-                     dev["block_tables"] if block_tables is None else block_tables,
-                     dev["seq_lens"] if seq_lens is None else seq_lens,
-                     num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=msl,
-                     alibi_slopes=dev["alibi_slopes"], softcap=w.softcap, layout=w.layout,
-                     mode=mode, dev_error=err, partition_counters=counters,
-                     seq_lens_host=w.seq_lens if mode == "auto" else None,
-                     window_left=getattr(w, "window_left", -1),
-                     kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
-                     v_scale=getattr(w, "v_scale", 1.0), **mq, **ws)
+        pa.pa_decode(*tensors, **call)
     torch.cuda.synchronize(device)
     if counters is not None:
         assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"
@@ -96,6 +93,7 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
         "exp_sums": ws["exp_sums"].double().cpu().numpy(),
         "tmp_out": ws["tmp_out"].double().cpu().numpy(),
         "dev_error": int(err.item()),
+        "plan": plan,
     }
 
 
@@ -106,7 +104,18 @@ def _violations(gpu, ref, atol, rtol):
     return bad
 
 
+def tolerance_used(w, gpu_out, ref_out) -> float:
+    """Largest |gpu - ref| / (atol + rtol |ref|) over the elements: the share of
+    the tolerance the worst element uses (above 1 fails; NaN gives inf)."""
+    atol, rtol = OUT_TOL[w.dtype]
+    g, r = np.asarray(gpu_out), np.asarray(ref_out)
+    q = np.abs(g - r) / (atol + rtol * np.abs(r))
+    return float(np.inf) if np.isnan(q).any() else float(q.max(initial=0.0))
+
+
 def check_out(w, gpu_out, ref_out, seqs=None, what="out"):
+    """Element-by-element tolerance check; returns the share of the tolerance
+    the worst element uses."""
     atol, rtol = OUT_TOL[w.dtype]
     sel = slice(None) if seqs is None else np.asarray(seqs)
     g, r = gpu_out[sel], ref_out[sel]
@@ -117,6 +126,7 @@ def check_out(w, gpu_out, ref_out, seqs=None, what="out"):
         raise AssertionError(f"{w.name}/{w.layout} {what}: {int(bad.sum())} of {bad.size} "
                              f"elements out of tolerance; first at {idx}: gpu {g[idx]!r} "
                              f"ref {r[idx]!r}; worst excess {err:.3e}")
+    return tolerance_used(w, g, r)
 
 
 def stat_rows(w, s):

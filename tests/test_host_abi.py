@@ -63,9 +63,34 @@ def test_workspace_elems(lib):
 
 
 def test_choose_mode(lib):
-    assert pa.choose_mode(32, 4, 512, 152) == "v1"
-    assert pa.choose_mode(32, 4, 4096, 152) == "v2"
-    assert pa.choose_mode(4, 4, 100000, 152) == "v2"
+    """Without host lengths every sequence counts as max_seq_len long: v1 once
+    the (sequence, kv head) tiles are at least one per SM."""
+    assert pa.choose_mode(32, 4, 512, 152) == "v1"       # one partition
+    assert pa.choose_mode(32, 4, 4096, 152) == "v2"      # 128 tiles < 152 SMs
+    assert pa.choose_mode(4, 4, 100000, 152) == "v2"     # 16 tiles
+    assert pa.choose_mode(38, 4, 4096, 152) == "v1"      # 152 tiles
+    assert pa.choose_mode(128, 8, 16384, 152) == "v1"    # 1024 tiles, 4 equal rounds
+    for c in (1, 2, 3, 0):
+        assert pa.choose_mode(128, 8, 16384, 152, ctas_per_sm=c) == "v1"
+    assert lib.pa_choose_mode(0, 8, 16384, 152, 2) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode(8, 8, 16384, 0, 2) == _abi.PA_MODE_V2
+
+
+def test_choose_mode_models_the_resident_ctas_of_the_path():
+    """The balance test runs on the grid of the kernel that is launched: the
+    same lengths can be even on one grid and uneven on another.  76 sequences
+    x 4 kv heads = 304 tiles, the first 38 sequences twice as long: one CTA per
+    SM (fp32 with two n-tiles) gives 152 CTAs that each take one long and one
+    short tile; two or three per SM (16-bit, fp8 split) give one tile per CTA,
+    so the long tiles set the time."""
+    import numpy as np
+    lens = np.array([8192] * 38 + [4096] * 38, dtype=np.int32)
+    assert pa.choose_mode(76, 4, 8192, 152, lens, ctas_per_sm=1) == "v1"
+    assert pa.choose_mode(76, 4, 8192, 152, lens, ctas_per_sm=2) == "v2"
+    assert pa.choose_mode(76, 4, 8192, 152, lens, ctas_per_sm=3) == "v2"
+    # interleaved long / short: every CTA of the 152-CTA grid gets two of a kind
+    inter = np.array([8192, 4096] * 38, dtype=np.int32)
+    assert pa.choose_mode(76, 4, 8192, 152, inter, ctas_per_sm=1) == "v2"
 
 
 def test_pages_dispatch_rule_worked_example():
@@ -207,7 +232,7 @@ def test_length_aware_dispatch():
     lens[7] = 100                                                            # one short sequence
     assert pa.choose_mode(128, 8, 16384, sm, lens) == "v1"
     assert pa.choose_mode(8, 2, 512, sm, np.full(8, 512)) == "v1"
-    assert pa.choose_mode(128, 8, 16384, sm) == "v2"                          # no host lengths
+    assert pa.choose_mode(128, 8, 16384, sm) == "v1"                          # no host lengths: even
     with pytest.raises(ValueError):
         pa.choose_mode(4, 2, 4096, sm, np.full(3, 4096))
 
@@ -220,18 +245,19 @@ def test_length_aware_dispatch_edges(lib):
     sm = 152
     lens = np.full(128, 16384, dtype=np.int32)
     ptr = lens.ctypes.data
-    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, 0, ptr) == _abi.PA_MODE_V2
-    assert lib.pa_choose_mode_for_lengths(0, 8, 16384, sm, ptr) == _abi.PA_MODE_V2
-    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, None) == _abi.PA_MODE_V2
-    assert lib.pa_choose_mode_for_lengths(128, 8, 300, sm, None) == _abi.PA_MODE_V1
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, 0, 2, ptr) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode_for_lengths(0, 8, 16384, sm, 2, ptr) == _abi.PA_MODE_V2
+    # no lengths: every sequence max_seq_len long, an even batch
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, 2, None) == _abi.PA_MODE_V1
+    assert lib.pa_choose_mode_for_lengths(128, 8, 300, sm, 2, None) == _abi.PA_MODE_V1
     zeros = np.zeros(128, dtype=np.int32)
-    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, zeros.ctypes.data) == _abi.PA_MODE_V1
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, 2, zeros.ctypes.data) == _abi.PA_MODE_V1
     # lengths beyond max_seq_len count as max_seq_len, negative ones as 0
     over = np.full(128, 1 << 30, dtype=np.int32)
-    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, over.ctypes.data) == _abi.PA_MODE_V1
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, 2, over.ctypes.data) == _abi.PA_MODE_V1
     mixed = lens.copy()
     mixed[::2] = -5  # every other sequence empty: the round-robin load is uneven
-    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, mixed.ctypes.data) == _abi.PA_MODE_V2
+    assert lib.pa_choose_mode_for_lengths(128, 8, 16384, sm, 2, mixed.ctypes.data) == _abi.PA_MODE_V2
 
 
 def test_workspace_bytes_and_partition_size(lib):

@@ -1,6 +1,7 @@
 """The N > 1 path of bench.py on CPU: two gloo ranks (replicas, no collective
 on the data path).  The whole-job value is the bytes of all replicas over the
-slowest replica's step time, and only rank 0 runs the reference arm."""
+slowest replica's step time, and only rank 0 runs the reference arm.  The CLI
+case runs `bench.py --gpus 2` itself, which launches the two ranks."""
 from __future__ import annotations
 
 import os
@@ -37,6 +38,8 @@ def _rank_main(rank: int, world: int, port: int, out):
         class Args:
             steps, warmup, config, layout, ref_budget = 1, 0, "tiny", "split", 1.0
         ref = bench.run_reference(Args, world, rank) if rank != 0 else "rank0"
+        if rank == 0:
+            dist.barrier()  # the barrier rank 1 takes inside run_reference
         out.put((rank, ms, gbs, ref))
         dist.barrier()
     finally:
@@ -59,3 +62,33 @@ def test_two_replicas_take_the_slowest_and_sum_the_bytes():
         assert ms == 2.0                                  # max over ranks
         assert abs(gbs - 2 * 1e9 / 2e-3 / 1e9) < 1e-9     # 2 GB over 2 ms
     assert res[1][3] is None                              # rank 1: no reference work
+
+
+def test_cli_gpus_2_launches_two_ranks_and_prints_one_line():
+    """`bench.py --gpus 2` with no launcher around it starts two ranks (torch's
+    launcher over 127.0.0.1), each joins the process group, and rank 0 alone
+    prints one JSON line for the whole job."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--config", "tiny", "--steps", "1", "--warmup", "3", "--ref-budget", "2"],
+                       cwd=str(ROOT), env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["config"]["name"] == "tiny" and d["value"] > 0
+    for rank in range(2):
+        assert f"rank {rank} of 2 joined" in r.stderr
+
+
+def test_cli_rejects_a_world_size_that_differs_from_gpus():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--config", "tiny"], cwd=str(ROOT), env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
