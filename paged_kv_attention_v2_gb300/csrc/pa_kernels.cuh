@@ -354,15 +354,18 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         t.valid = true;
         return t;
     };
-    // Block ids of pages [pc, pc + 32) of tile t, one per lane (range-checked).
+    // Block ids of pages [pc, pc + 32) of tile t, one per lane.  The load is
+    // only issued here; its range check (check_ids) comes where the ids are
+    // used, so that no copy waits on the load.
     auto load_ids = [&](const ProducerTile& t, int pc) {
-        int blk = 0;
-        if (t.valid && pc + lane < t.npages) {
-            blk = __ldg(p.block_tables + (int64_t)t.seq * p.max_blocks_per_seq + t.tb / kBS + pc + lane);
-            if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                report(p, PA_DEVERR_BLOCK_ID);
-                blk = 0;
-            }
+        return (t.valid && pc + lane < t.npages)
+                   ? __ldg(p.block_tables + (int64_t)t.seq * p.max_blocks_per_seq + t.tb / kBS + pc + lane)
+                   : 0;
+    };
+    auto check_ids = [&](int blk) {
+        if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            report(p, PA_DEVERR_BLOCK_ID);
+            blk = 0;
         }
         return blk;
     };
@@ -371,18 +374,15 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     int k = 0;       // tiles issued by this CTA
     bool ok = true;
     ProducerTile cur = next_tile();
-    int ids;
-    if (cur.valid && cur.seq == spec_seq && cur.tb == spec_tb) {
-        ids = lane < cur.npages ? spec_ids : 0;
-        if ((unsigned)ids >= (unsigned)p.num_blocks) {
-            report(p, PA_DEVERR_BLOCK_ID);
-            ids = 0;
-        }
-    } else {
-        ids = load_ids(cur, 0);
-    }
+    int ids = check_ids((cur.valid && cur.seq == spec_seq && cur.tb == spec_tb) ? (lane < cur.npages ? spec_ids : 0)
+                                                                                  : load_ids(cur, 0));
     while (ok && cur.valid) {
-        const ProducerTile nxt = next_tile();  // walk ahead while this tile's pages stream
+        // The next tile is walked to, and its first block ids loaded, only once
+        // the first batch of this tile's copies is out (the walk may load
+        // lengths): nothing delays the first copies of a tile.
+        ProducerTile nxt;
+        nxt.valid = false;
+        bool have_nxt = false;
 
         const int slot = k % C::kTD;
         if (lane == 0) {
@@ -412,8 +412,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
 
         for (int pc = 0; pc < cur.npages && ok; pc += 32) {
             const int n = min(32, cur.npages - pc);
-            // block ids of the next 32 pages (this tile or the next one), loaded early
-            const int ids_next = (pc + 32 < cur.npages) ? load_ids(cur, pc + 32) : load_ids(nxt, 0);
+            int ids_next = 0;  // block ids of the next 32 pages (this tile or the next one)
             // Issue in batches of up to STAGES stages (kPPS consecutive pages
             // each), one stage per lane: the stages of a batch are distinct, so
             // each lane waits for exactly the previous use of its own stage.
@@ -464,10 +463,24 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                 }
                 ok = __all_sync(0xffffffffu, lok);
                 g += (uint32_t)nb;
+                if (b0 == 0) {  // first batch out: load the next ids while the rest streams
+                    if (pc + 32 < cur.npages) {
+                        ids_next = load_ids(cur, pc + 32);
+                    } else {
+                        if (!have_nxt) {
+                            nxt = next_tile();
+                            have_nxt = true;
+                        }
+                        ids_next = load_ids(nxt, 0);
+                    }
+                }
             }
-            ids = ids_next;
+            ids = check_ids(ids_next);
         }
-        if (cur.npages == 0) ids = load_ids(nxt, 0);
+        if (!have_nxt) {
+            nxt = next_tile();
+            if (cur.npages == 0) ids = check_ids(load_ids(nxt, 0));
+        }
         ++k;
         cur = nxt;
     }
