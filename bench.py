@@ -214,7 +214,7 @@ class Setup:
     KV pools that the steps rotate through, so the bytes touched between two
     uses of a pool exceed 4x the L2 size."""
 
-    def __init__(self, w, mode_arg, dev, pa, counters=True):
+    def __init__(self, w, mode_arg, dev, pa, counters=True, dynamic=True):
         import torch
         self.w, self.dev = w, dev
         cdt = w.cache_dtype
@@ -234,7 +234,8 @@ class Setup:
         # partitions inside the partition kernel where its rule allows
         self.ws = pa.alloc_workspace(w.num_seqs, w.num_heads, w.head_size, w.max_seq_len, dev,
                                      num_kv_heads=w.num_kv_heads if counters else None,
-                                     num_query_tokens=None if self.qs is None else w.num_query_tokens)
+                                     num_query_tokens=None if self.qs is None else w.num_query_tokens,
+                                     tile_counters=dynamic)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         common = dict(num_kv_heads=w.num_kv_heads, scale=w.scale, max_seq_len=w.max_seq_len,
                       kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
@@ -382,6 +383,7 @@ def config_record(w, S, r, args, world):
             "merge": ("in the partition kernel" if plan["merge_in_kernel"] else "reduce kernel")
             if plan["mode"] == "v2" else "none (v1)",
             "partition_grid": plan["grid"], "ctas_per_sm": plan["ctas_per_sm"],
+            "schedule": "dynamic" if plan["dynamic_schedule"] else "static",
             "kv_bytes_per_step": w.kv_bytes, "total_bytes_per_step": total_bytes(w, S, plan["mode"]),
             "l2": f"rotate {S.copies} KV pools ({S.copies * S.pool_bytes} B >= 4x L2 {S.l2} B)"
             if S.copies * S.pool_bytes >= 4 * S.l2 else f"{S.copies} KV pools of {S.pool_bytes} B",
@@ -418,7 +420,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = peaks()
 
     w = W.make_workload(args.config, args.layout)
-    S = Setup(w, args.mode, dev, pa, counters=args.merge == "auto")
+    S = Setup(w, args.mode, dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic")
     r = measure(S, args.steps, args.warmup, world, soak, sampler)
     kv = w.kv_bytes
     value = whole_job_gbs(kv, world, r["ms_step"])
@@ -480,7 +482,7 @@ def run_ours(args, world, rank, local):
     secondary = None
     if not args.no_secondary and args.config != SECONDARY:
         w2 = W.make_workload(SECONDARY, "split")
-        S2 = Setup(w2, "auto", dev, pa, counters=args.merge == "auto")
+        S2 = Setup(w2, "auto", dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic")
         r2 = measure(S2, args.steps, args.warmup, world, soak, sampler)
         v2 = whole_job_gbs(w2.kv_bytes, world, r2["ms_step"])
         secondary = {SECONDARY: {
@@ -615,6 +617,9 @@ def main(argv=None):
     ap.add_argument("--merge", default="auto", choices=("auto", "reduce"),
                     help="auto: pass partition counters (the library may merge in the partition "
                          "kernel); reduce: no counters, v2 always launches the reduce kernel")
+    ap.add_argument("--schedule", default="dynamic", choices=("dynamic", "static"),
+                    help="dynamic: pass tile counters (tiles claimed by whichever CTA is free); "
+                         "static: the round-robin schedule")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",

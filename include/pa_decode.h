@@ -196,6 +196,17 @@ typedef struct pa_decode_args {
      * pa_choose_mode_for_lengths on it (NULL: every sequence taken as
      * max_seq_len long). */
     const int32_t* seq_lens_host;
+    /* Optional [2] int32 device counters, both zero before the first call.
+     * Given, and seq_lens_host shows sequences of different partition counts
+     * (v2) or page counts (v1), the persistent partition kernel hands out its
+     * tiles dynamically: each CTA starts on its own first tile and claims
+     * every later one from a grid-wide counter, so CTAs whose tiles are
+     * shorter take more of them and the CTAs finish closer together
+     * (pa_plan tells); otherwise the counters are not touched and the tiles
+     * go round-robin over a grid cut to equal rounds.  Each completed call
+     * leaves both at zero; after a PA_DEVERR_TIMEOUT the caller must zero
+     * them.  Calls that share them must not overlap on the GPU. */
+    int32_t* tile_counters;
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the
@@ -308,6 +319,8 @@ typedef struct pa_launch_plan {
     int32_t kernels;          /* kernels launched per call: 1 or 2 */
     int32_t ctas_per_sm;      /* resident CTAs per SM of the partition kernel */
     int32_t grid;             /* CTAs of the persistent partition-kernel grid */
+    int32_t dynamic_schedule; /* 1: tiles claimed from tile_counters */
+    int32_t reserved;
     int64_t tiles;            /* tiles of the partition kernel (an upper bound for unequal lengths) */
 } pa_launch_plan;
 

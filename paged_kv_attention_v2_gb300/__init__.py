@@ -72,7 +72,8 @@ def plan(args: _abi.PaDecodeArgs) -> dict:
         raise PaDecodeError(st)
     return {"mode": "v1" if pl.mode == _abi.PA_MODE_V1 else "v2",
             "merge_in_kernel": bool(pl.merge_in_kernel), "kernels": int(pl.kernels),
-            "ctas_per_sm": int(pl.ctas_per_sm), "grid": int(pl.grid), "tiles": int(pl.tiles)}
+            "ctas_per_sm": int(pl.ctas_per_sm), "grid": int(pl.grid),
+            "dynamic_schedule": bool(pl.dynamic_schedule), "tiles": int(pl.tiles)}
 
 
 def plan_for(out, query, key_cache, value_cache, block_tables, seq_lens, **kw) -> dict:
@@ -90,9 +91,11 @@ def _dtype_code(t):
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device,
-                    num_kv_heads: int | None = None, num_query_tokens: int | None = None):
+                    num_kv_heads: int | None = None, num_query_tokens: int | None = None,
+                    tile_counters: bool = False):
     """torch-allocated v2 workspace: dict(exp_sums, max_logits, tmp_out), plus
-    zeroed partition_counters when num_kv_heads is given (fused merge).  With
+    zeroed partition_counters when num_kv_heads is given (fused merge) and
+    zeroed tile_counters when asked for (dynamic tile schedule).  With
     several query tokens per sequence the statistics have one row per query
     token (num_query_tokens rows)."""
     import torch
@@ -102,6 +105,8 @@ def alloc_workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: 
     if num_kv_heads is not None:
         extra["partition_counters"] = torch.zeros((num_seqs, num_kv_heads), dtype=torch.int32,
                                                   device=device)
+    if tile_counters:
+        extra["tile_counters"] = torch.zeros(2, dtype=torch.int32, device=device)
     return {**extra,
         "exp_sums": torch.empty((rows, num_heads, P), dtype=torch.float32, device=device),
         "max_logits": torch.empty((rows, num_heads, P), dtype=torch.float32, device=device),
@@ -121,7 +126,8 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               event_begin=None, event_end=None, partition_counters=None,
               window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
               v_scale: float = 1.0, query_start=None,
-              max_query_len: int | None = None, seq_lens_host=None) -> _abi.PaDecodeArgs:
+              max_query_len: int | None = None, seq_lens_host=None,
+              tile_counters=None) -> _abi.PaDecodeArgs:
     """Build the C argument struct.  The library validates sizes and types it can
     see; this also checks what only the tensors know: the caches' element size
     and element count against kv_dtype, head_size and num_kv_heads.
@@ -134,7 +140,9 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
     sequence: query / out rows are query tokens, and max_query_len (>= every
     sequence's token count) is required with it.  seq_lens_host (a host copy of
     seq_lens: numpy array or CPU tensor) lets mode "auto" choose by the actual
-    lengths; the struct keeps a reference to it."""
+    lengths; the struct keeps a reference to it.  tile_counters (int32 [2],
+    zeroed once, e.g. from alloc_workspace(..., tile_counters=True)) turns on
+    the dynamic tile schedule."""
     num_rows, num_heads, head_size = query.shape
     num_seqs = seq_lens.shape[0]
     if tuple(out.shape) != tuple(query.shape):
@@ -181,6 +189,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         query_start=_ptr(query_start), num_query_tokens=num_rows if query_start is not None else 0,
         max_query_len=int(max_query_len) if query_start is not None else 0,
         seq_lens_host=None if host_lens is None else host_lens.ctypes.data,
+        tile_counters=_ptr(tile_counters),
     )
     a._keep_host_lens = host_lens  # the pointer above stays valid as long as the struct lives
     return a

@@ -78,6 +78,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("num_query_tokens", ctypes.c_int32),
         ("max_query_len", ctypes.c_int32),
         ("seq_lens_host", ctypes.c_void_p),
+        ("tile_counters", ctypes.c_void_p),
     ]
 
 
@@ -88,6 +89,8 @@ class PaLaunchPlan(ctypes.Structure):
         ("kernels", ctypes.c_int32),
         ("ctas_per_sm", ctypes.c_int32),
         ("grid", ctypes.c_int32),
+        ("dynamic_schedule", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("tiles", ctypes.c_int64),
     ]
 

@@ -39,13 +39,11 @@ constexpr int kKvSame = 0;      // same 16-bit / 32-bit type as the query
 constexpr int kKvE4M3 = 1;      // fp8 E4M3
 constexpr int kKvE5M2 = 2;      // fp8 E5M2
 
-// Shape of the partition kernel.  Ring stages per cache type: one 16-token
-// page of K and V each, except fp8 NHD tiles of one n-tile (two pages each);
-// fp8 split pages take 12 stages so that three CTAs share an SM, fp32 pages
-// with two n-tiles 8 stages of 16 KB (one CTA per SM).
+// Shape of the partition kernel.  Ring stages per cache type, one 16-token
+// page of K and V each: fp8 pages take 12 stages so that three CTAs share an
+// SM, fp32 pages with two n-tiles 8 stages of 16 KB (one CTA per SM).
 constexpr int kStages16 = 8;       // 16-bit caches
-constexpr int kStagesFp8 = 12;     // fp8 caches, one page per stage
-constexpr int kStagesFp8Pairs = 8; // fp8 NHD caches with one n-tile: two pages per stage
+constexpr int kStagesFp8 = 12;     // fp8 caches (three CTAs per SM fit)
 constexpr int kStagesF32 = 4;      // fp32 caches, one n-tile (two CTAs per SM)
 constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
 constexpr int kConsumerWarps = 4;  // consumer warps per CTA
@@ -80,6 +78,7 @@ struct Params {
     uint64_t wait_limit_ns;  // limit of every barrier wait (0: kWaitLimitNs)
     int withhold_page;       // test hook: CTA 0 withholds its first page copy (a wait runs out)
     int kv_evict_first;      // KV page copies marked evict_first (partition outputs small against L2)
+    int32_t* tile_ctr;       // [2] dynamic schedule: tiles claimed, CTAs done (NULL: static schedule)
 };
 
 struct TileDesc {
@@ -146,13 +145,12 @@ struct Cfg {
     static constexpr int kElem = sizeof(T);                // query / output element
     static constexpr int kKvElem = KV == kKvSame ? (int)sizeof(T) : 1;
     static constexpr int kPageBytes = kBS * HEAD * kKvElem;  // one page of K (or of V)
-    // Pages per stage.  fp8 NHD with one n-tile takes two: one barrier round,
-    // max reduction and rescale per two pages pays for its value transposes
-    // (measured: long100k_fp8 95.4 -> 86.7 µs); for the split layout the third
-    // CTA per SM that one-page stages leave room for is worth more (76.2 against
-    // 86.6 µs), and 16-row tiles would spill.
-    static constexpr int kPPS = (KV != kKvSame && NT == 1 && LAYOUT == kNHD) ? 2 : 1;
-    static constexpr int kStageBytes = 2 * kPPS * kPageBytes;  // K pages, then V pages
+    // One page of K and one of V per ring stage.  (Two pages per fp8 NHD stage
+    // halve its barrier rounds, max reductions and rescales, but their 8 KB
+    // stages leave room for two CTAs per SM, against three with one-page
+    // stages: measured, long100k_fp8 NHD 83.1 -> 75.9 µs and gqa4k_fp8 NHD
+    // 34.2 -> 32.7 µs for the one-page stages.)
+    static constexpr int kStageBytes = 2 * kPageBytes;  // K page, then V page
     static constexpr int kMaxG = NT * 8;                   // rows (heads x query tokens) handled
     static constexpr int kQBytes = kMaxG * HEAD * kElem;
     static constexpr int kTD = 2;                          // tile descriptor ring depth
@@ -323,15 +321,31 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     }
     load_chunk(0);
 
-    // Tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ... (kv head fastest).
+    // Tiles of this CTA (kv head fastest): blockIdx.x, then blockIdx.x +
+    // gridDim.x, ... (static schedule) or, with tile counters, whatever tile
+    // index the grid-wide counter hands out next (dynamic schedule: a CTA
+    // that streams faster takes more tiles).  A claim is made one tile ahead
+    // by lane 0, so its round trip overlaps a whole tile; the claimed indices
+    // of a CTA increase, as the walk of seq_lens below needs.
     int tile = blockIdx.x;
+    const bool dyn = p.tile_ctr != nullptr;
+    int claimed = 0;  // lane 0: the tile after `tile` (dynamic schedule)
+    auto claim = [&]() {
+        if (lane == 0) claimed = (int)gridDim.x + atomicAdd(p.tile_ctr, 1);
+    };
+    if (dyn) claim();
     auto next_tile = [&]() {
         ProducerTile t;
         t.valid = false;
         t.seq = t.part = t.tb = t.te = t.len = t.npages = t.q0 = t.qn = 0;
         const int u = tile / Hkv;
         t.kvh = tile - u * Hkv;
-        tile += gridDim.x;
+        if (dyn) {
+            tile = __shfl_sync(0xffffffffu, claimed, 0);
+            claim();
+        } else {
+            tile += gridDim.x;
+        }
         while (cb < S && u >= cu + c_total) {
             cu += c_total;
             cb += 32;
@@ -413,16 +427,12 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         for (int pc = 0; pc < cur.npages && ok; pc += 32) {
             const int n = min(32, cur.npages - pc);
             int ids_next = 0;  // block ids of the next 32 pages (this tile or the next one)
-            // Issue in batches of up to STAGES stages (kPPS consecutive pages
-            // each), one stage per lane: the stages of a batch are distinct, so
-            // each lane waits for exactly the previous use of its own stage.
-            constexpr int PPS = C::kPPS;
-            const int nst = (n + PPS - 1) / PPS;
-            for (int b0 = 0; b0 < nst && ok; b0 += STAGES) {
-                const int nb = min(STAGES, nst - b0);
-                int bq[PPS];
-#pragma unroll
-                for (int q = 0; q < PPS; ++q) bq[q] = __shfl_sync(0xffffffffu, ids, ((b0 + lane) * PPS + q) & 31);
+            // Issue in batches of up to STAGES pages, one stage per lane: the
+            // stages of a batch are distinct, so each lane waits for exactly the
+            // previous use of its own stage.
+            for (int b0 = 0; b0 < n && ok; b0 += STAGES) {
+                const int nb = min(STAGES, n - b0);
+                const int blk = __shfl_sync(0xffffffffu, ids, (b0 + lane) & 31);
                 bool lok = true;
                 if (lane < nb) {
                     const uint32_t gg = g + (uint32_t)lane;
@@ -432,32 +442,25 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
                     // waiting for it runs out of time (bounded, no fault)
                     const bool withhold = p.withhold_page && blockIdx.x == 0 && gg == 0;
                     if (lok && !withhold) {
-                        const int npg = min(PPS, n - (b0 + lane) * PPS);  // pages of this stage
                         const uint32_t fb = sm.full + st * 8;
-                        const uint32_t dk0 = sm.ring + st * C::kStageBytes;
-                        const uint32_t dv0 = dk0 + PPS * C::kPageBytes;
-                        mbar_arrive_expect_tx(fb, (uint32_t)npg * 2 * C::kPageBytes);
-#pragma unroll
-                        for (int q = 0; q < PPS; ++q) {
-                            if (q >= npg) break;
-                            const uint32_t dk = dk0 + q * C::kPageBytes, dv = dv0 + q * C::kPageBytes;
-                            const int64_t page = (int64_t)bq[q] * Hkv + cur.kvh;
-                            if constexpr (C::kTensorMap && C::kKvElem == 1) {
-                                // fp8 NHD: one box of 16 token rows x HEAD bytes per page
-                                const int y = (int)(page * kBS);
-                                tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
-                                tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
-                            } else if constexpr (C::kTensorMap) {
-                                // 16-bit / fp32 NHD: the whole page in one box of the
-                                // 3-D view (128-byte chunk of a row, row, chunk index),
-                                // staged as HEAD * elem / 128 blocks of 16 rows x 128 bytes
-                                const int y = (int)(page * kBS);
-                                tensor3d_g2s_hint(dk, tmk, 0, y, 0, fb, kvpol);
-                                tensor3d_g2s_hint(dv, tmv, 0, y, 0, fb, kvpol);
-                            } else {
-                                bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
-                                bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
-                            }
+                        const uint32_t dk = sm.ring + st * C::kStageBytes, dv = dk + C::kPageBytes;
+                        mbar_arrive_expect_tx(fb, 2 * C::kPageBytes);
+                        const int64_t page = (int64_t)blk * Hkv + cur.kvh;
+                        if constexpr (C::kTensorMap && C::kKvElem == 1) {
+                            // fp8 NHD: one box of 16 token rows x HEAD bytes per page
+                            const int y = (int)(page * kBS);
+                            tensor2d_g2s_hint(dk, tmk, 0, y, fb, kvpol);
+                            tensor2d_g2s_hint(dv, tmv, 0, y, fb, kvpol);
+                        } else if constexpr (C::kTensorMap) {
+                            // 16-bit / fp32 NHD: the whole page in one box of the
+                            // 3-D view (128-byte chunk of a row, row, chunk index),
+                            // staged as HEAD * elem / 128 blocks of 16 rows x 128 bytes
+                            const int y = (int)(page * kBS);
+                            tensor3d_g2s_hint(dk, tmk, 0, y, 0, fb, kvpol);
+                            tensor3d_g2s_hint(dv, tmv, 0, y, 0, fb, kvpol);
+                        } else {
+                            bulk_g2s_hint(dk, kbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
+                            bulk_g2s_hint(dv, vbase + page * C::kPageBytes, C::kPageBytes, fb, kvpol);
                         }
                     }
                 }
@@ -503,6 +506,12 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
         for (uint32_t st = 0; st < STAGES && st < g; ++st) {
             const uint32_t last = g - 1 - ((g - 1 - st) % STAGES);
             mbar_wait(sm.full + st * 8, (last / STAGES) & 1, sm.abort + 1, sm.wait_ns);
+        }
+        // Dynamic schedule: the last CTA to be done with claiming (its arrival
+        // releases its claims) sets both counters back to zero for the next call.
+        if (dyn && atom_add_acq_rel_gpu(p.tile_ctr + 1, 1) == (int)gridDim.x - 1) {
+            p.tile_ctr[0] = 0;
+            p.tile_ctr[1] = 0;
         }
     }
 }
@@ -594,117 +603,29 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
     }
 }
 
-// Fused v2 merge, run by the NC consumer warps of the CTA that finished the
-// last partition of (d.seq, d.kvh): Phase 2 for the group's heads, reading the
-// partition statistics the other CTAs wrote (L2 loads: never a stale L1 line).
-// The fused path has at most PA_FUSED_MAX_PARTITIONS partitions per row, so a
-// thread issues every load of two (row, 4-column) items -- statistics and
-// partition outputs of all partitions -- before any arithmetic: one round
-// trip to L2 per pair of items.
-template <typename T, int HEAD, int NC, bool MQ>
-__device__ void fused_merge(const Params& p, const TileDesc& d, int tid) {
-    constexpr int D4 = HEAD / 4;
-    constexpr int PM = PA_FUSED_MAX_PARTITIONS;
-    constexpr int NI = 1;  // items in flight per thread
-    const int G = p.group;
-    const int qn = MQ ? d.qn : 1;
-    const int n = qn * G * D4;
-    for (int idx0 = tid; idx0 < n; idx0 += NI * NC * 32) {
-        float mq[NI][PM], eq[NI][PM];
-        float4 t[NI][PM];
-        int64_t sh[NI];
-        int d4s[NI];
-#pragma unroll
-        for (int it = 0; it < NI; ++it) {
-            const int idx = idx0 + it * NC * 32;
-            int P = 0, p0 = 0;
-            sh[it] = 0;
-            d4s[it] = 0;
-            if (idx < n) {
-                const int h = idx / D4;
-                d4s[it] = idx - h * D4;
-                const int qi = MQ ? h / G : 0;
-                const int hi = d.len - qn + qi;                  // the query token's position
-                P = hi >= 0 ? min((hi + kPart) / kPart, PM) : 0;  // partitions up to it
-                p0 = window_lo_at(p, hi) / kPart;                 // before p0: outside the window
-                sh[it] = (int64_t)(d.q0 + qi) * p.num_heads + d.kvh * G + (h - qi * G);
-            }
-            const float* ml = p.max_logits + sh[it] * p.max_parts;
-            const float* es = p.exp_sums + sh[it] * p.max_parts;
-            const float* tmp = p.tmp_out + sh[it] * p.max_parts * HEAD + 4 * d4s[it];
-#pragma unroll
-            for (int q = 0; q < PM; ++q) {
-                if (q >= p0 && q < P) {
-                    mq[it][q] = __ldcg(ml + q);
-                    eq[it][q] = __ldcg(es + q);
-                    t[it][q] = __ldcg(reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD));
-                } else {
-                    mq[it][q] = -INFINITY;
-                    eq[it][q] = 0.f;
-                    t[it][q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-        }
-#pragma unroll
-        for (int it = 0; it < NI; ++it) {
-            if (idx0 + it * NC * 32 >= n) break;
-            float M = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < PM; ++q) M = fmaxf(M, mq[it][q]);
-            float W = 0.f;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < PM; ++q) {
-                const float c = mq[it][q] == -INFINITY ? 0.f : expf(mq[it][q] - M) * eq[it][q];
-                a.x += c * t[it][q].x;
-                a.y += c * t[it][q].y;
-                a.z += c * t[it][q].z;
-                a.w += c * t[it][q].w;
-                W += c;
-            }
-            const float inv = W > 0.f ? 1.f / W : 0.f;
-            T* dst = static_cast<T*>(p.out) + sh[it] * HEAD + 4 * d4s[it];
-            if constexpr (std::is_same<T, float>::value) {
-                *reinterpret_cast<float4*>(dst) = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-            } else {
-                constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
-                uint2 v;
-                v.x = pack2<BF>(a.x * inv, a.y * inv);
-                v.y = pack2<BF>(a.z * inv, a.w * inv);
-                *reinterpret_cast<uint2*>(dst) = v;
-            }
-        }
-    }
-}
+template <typename T, int HEAD, bool L2ONLY>
+__device__ __forceinline__ void merge_row_warp(const Params& p, int64_t row, int h, int len, int qn, int qi,
+                                               int lane);
 
-// After the merge: statistics to absolute ALiBi positions, padding of the
-// unused partitions, counter back to zero for the next call.
-template <int NC, bool MQ>
-__device__ void fused_finish_stats(const Params& p, const TileDesc& d, int tid) {
-    const int G = p.group, Pm = p.max_parts;
-    const int qn = MQ ? d.qn : 1;
-    for (int idx = tid; idx < qn * G * Pm; idx += NC * 32) {
-        const int h = idx / Pm, q = idx - h * Pm;
-        const int qi = MQ ? h / G : 0;
-        const int hi = d.len - qn + qi;
-        const int P = hi >= 0 ? (hi + kPart) / kPart : 0;
-        const int p0 = window_lo_at(p, hi) / kPart;
-        const int head = d.kvh * G + (h - qi * G);
-        const int64_t o = ((int64_t)(d.q0 + qi) * p.num_heads + head) * Pm + q;
-        if (q < P && q >= p0) {
-            if (p.alibi) p.max_logits[o] += __ldg(p.alibi + head) * (float)(d.len - 1);
-        } else {
-            p.max_logits[o] = -INFINITY;
-            p.exp_sums[o] = 0.f;
-        }
+// The rows of one (sequence, kv head), one per consumer warp at a time.  Not
+// inlined: its loads then never share a register allocation with the page
+// loop (three fp8 CTAs per SM need the kernel within 128 registers).
+template <typename T, int HEAD, int NC, bool MQ>
+__device__ __noinline__ void merge_group(const Params& p, int seq_kvh_base, int q0, int qn, int len, int warp,
+                                         int lane) {
+    const int G = p.group;
+    for (int r = warp; r < qn * G; r += NC) {
+        const int qi = MQ ? r / G : 0;
+        merge_row_warp<T, HEAD, true>(p, (int64_t)q0 + qi, seq_kvh_base + (r - qi * G), len, qn, qi, lane);
     }
-    if (tid == 0) p.counters[(int64_t)d.seq * p.num_kv_heads + d.kvh] = 0;
 }
 
 // End of a tile for the consumer warps: epilogue (merge of the warps' partial
 // states, partition statistics or output row), then in fused v2 mode the
 // arrival count of the (sequence, kv head) and, for its last partition, the
-// Phase 2 merge.  Returns false if a bounded wait gave up.
+// Phase 2 merge: one (query row, head) per consumer warp at a time, the same
+// row merge as the reduce kernel, with L2-only loads.  Returns false if a
+// bounded wait gave up.
 template <class C, typename T, int HEAD, int NC>
 __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, int warp, int lane,
                             uint32_t& mphase) {
@@ -714,19 +635,16 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     if (!p.fused || p.v1) return true;
     if (tid == 0) {
         const int P = (d.len + kPart - 1) / kPart - window_lo(p, d.len, d.qn) / kPart;
-        const int units = P > 0 ? P : 1;
+        int* counter = p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh;
         // releases this CTA's partition results (every warp's, seen through the
         // barrier above) before the count; acquires the others' with it
-        const int old = atom_add_acq_rel_gpu(p.counters + (int64_t)d.seq * p.num_kv_heads + d.kvh, 1);
-        sm.abort[2] = (old == units - 1) ? 1 : 0;
+        const int last = atom_add_acq_rel_gpu(counter, 1) == (P > 0 ? P : 1) - 1;
+        if (last) *counter = 0;  // every tile has arrived: zero again for the next call
+        sm.abort[2] = last ? 1 : 0;
     }
     if (!consumer_sync(sm, mphase, lane)) return false;
-    if (sm.abort[2]) {
-        __threadfence();  // the other CTAs' partition results, seen through their arrivals
-        fused_merge<T, HEAD, NC, C::kMQ>(p, d, tid);
-        if (!consumer_sync(sm, mphase, lane)) return false;  // statistics read before rewritten
-        fused_finish_stats<NC, C::kMQ>(p, d, tid);
-    }
+    if (sm.abort[2])
+        merge_group<T, HEAD, NC, C::kMQ>(p, d.kvh * p.group, d.q0, C::kMQ ? d.qn : 1, d.len, warp, lane);
     return true;
 }
 
@@ -1246,14 +1164,9 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
         }
 
-        // kPPS consecutive pages per ring stage: one barrier round, one max
-        // reduction and one rescale of the accumulators per stage
-        constexpr int PPS = C::kPPS;
-        constexpr int STOK = PPS * kBS;  // tokens per stage
         const int npages = tile_pages(d.tok_begin, d.tok_end);
-        const int nstages = (npages + PPS - 1) / PPS;
         const int page0 = d.tok_begin / kBS * kBS;
-        for (int j = warp; j < nstages; j += NC) {
+        for (int j = warp; j < npages; j += NC) {
             const uint32_t gg = gbase + (uint32_t)j;
             const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
             if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
@@ -1261,87 +1174,67 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 *sm.abort = 1;
                 return;
             }
-            const uint32_t kp = sm.ring + st * C::kStageBytes;  // key page q at kp + q * kPageBytes
-            const uint32_t vp = kp + PPS * C::kPageBytes;       // value page q at vp + q * kPageBytes
-            const int tok0 = page0 + j * STOK;
-            const int valid = min(STOK, d.tok_end - tok0);
-            const bool edge = tok0 < lo_all || tok0 + STOK - 1 > hi_all;  // some key masked
-            if (valid < STOK) {
-#pragma unroll
-                for (int q = 0; q < PPS; ++q) {
-                    const int vq = min(max(valid - q * kBS, 0), kBS);  // valid tokens of page q
-                    if (vq < kBS) {
-                        if constexpr (LAYOUT == kNHD)
-                            zero_v_tail8_nhd<HEAD>(vp + q * C::kPageBytes, vq, lane);
-                        else
-                            zero_v_tail8<HEAD>(vp + q * C::kPageBytes, vq, lane);
-                    }
-                }
+            const uint32_t kp = sm.ring + st * C::kStageBytes;
+            const uint32_t vp = kp + C::kPageBytes;
+            const int tok0 = page0 + j * kBS;
+            const int valid = min(kBS, d.tok_end - tok0);  // slots >= valid: past the sequence
+            const bool edge = tok0 < lo_all || tok0 + kBS - 1 > hi_all;  // some key masked
+            if (valid < kBS) {
+                if constexpr (LAYOUT == kNHD)
+                    zero_v_tail8_nhd<HEAD>(vp, valid, lane);
+                else
+                    zero_v_tail8<HEAD>(vp, valid, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
 
-            // S^T[row][head] per page: key page [d/16][token][16 bytes] (split)
-            // or [token][d] with swizzled 16-byte chunks (NHD)
-            float s[PPS][NT][4], s2[PPS][NT][4];
+            // S^T[row][head]: key page [d/16][token][16 bytes] (split) or [token][d]
+            // with swizzled 16-byte chunks (NHD)
+            float s[NT][4], s2[NT][4];
 #pragma unroll
-            for (int q = 0; q < PPS; ++q)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[q][nt][e] = s2[q][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
             // one ldmatrix.x4 fetches the four 32-bit words (tokens tlo / thi,
             // k-steps kk / kk + 1) that four separate loads would
 #pragma unroll
             for (int kk = 0; kk < KT; kk += 2) {
+                uint32_t w[4];
+                ldsm_x4(kp + k8_frag_off<LAYOUT, HEAD>(lane, kk), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                for (int q = 0; q < PPS; ++q) {
-                    uint32_t w[4];
-                    ldsm_x4(kp + q * C::kPageBytes + k8_frag_off<LAYOUT, HEAD>(lane, kk), w[0], w[1], w[2], w[3]);
+                for (int u = 0; u < 2; ++u) {
+                    uint32_t a0, a1, a2, a3;
+                    fp8x4_to_f16<KV>(w[2 * u], a0, a2);
+                    fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        uint32_t a0, a1, a2, a3;
-                        fp8x4_to_f16<KV>(w[2 * u], a0, a2);
-                        fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            if (u)
-                                mma_16816<false>(s2[q][nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
-                            else
-                                mma_16816<false>(s[q][nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
-                        }
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (u)
+                            mma_16816<false>(s2[nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
+                        else
+                            mma_16816<false>(s[nt], a0, a1, a2, a3, qb[nt][kk + u][0], qb[nt][kk + u][1]);
                     }
                 }
             }
 
-            uint32_t pb[PPS][NT][2];
+            uint32_t pb[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float z[PPS][4];
+                float z[4];
 #pragma unroll
-                for (int q = 0; q < PPS; ++q) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float v = (s[q][nt][e] + s2[q][nt][e]) * p.scale;
-                        if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
-                        if (has_alibi)
-                            v += sl[nt][e & 1] * (float)(tok0 + q * kBS + ((e >> 1) ? thi : tlo) - origin);
-                        z[q][e] = v;
-                    }
-                    if (edge) {
-                        const int t0 = tok0 + q * kBS + tlo, t1 = tok0 + q * kBS + thi;
-                        if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[q][0] = -INFINITY;
-                        if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[q][1] = -INFINITY;
-                        if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[q][2] = -INFINITY;
-                        if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[q][3] = -INFINITY;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    float v = (s[nt][e] + s2[nt][e]) * p.scale;
+                    if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
+                    if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + ((e >> 1) ? thi : tlo) - origin);
+                    z[e] = v;
                 }
-                float mx0 = fmaxf(z[0][0], z[0][2]), mx1 = fmaxf(z[0][1], z[0][3]);
-#pragma unroll
-                for (int q = 1; q < PPS; ++q) {
-                    mx0 = fmaxf(mx0, fmaxf(z[q][0], z[q][2]));
-                    mx1 = fmaxf(mx1, fmaxf(z[q][1], z[q][3]));
+                if (edge) {
+                    const int t0 = tok0 + tlo, t1 = tok0 + thi;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
                 }
+                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -1349,28 +1242,22 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 }
                 const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
                 // several query tokens: a row with no key in its range so far keeps
-                // max -inf (masked stages only); take 0 as reference so no -inf - -inf
-                // appears.  One token: every stage holds a key of every row.
+                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
+                // appears.  One token: every page holds a key of every row.
                 const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
                 const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
                 const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
                 const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
                 m[nt][0] = mn0;
                 m[nt][1] = mn1;
-                float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-                for (int q = 0; q < PPS; ++q) {
-                    const float p0 = exp2f((z[q][0] - mr0) * kLog2e);
-                    const float p1 = exp2f((z[q][1] - mr1) * kLog2e);
-                    const float p2 = exp2f((z[q][2] - mr0) * kLog2e);
-                    const float p3 = exp2f((z[q][3] - mr1) * kLog2e);
-                    ls0 += p0 + p2;
-                    ls1 += p1 + p3;
-                    pb[q][nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tlo
-                    pb[q][nt][1] = movmatrix_trans(pack2<false>(p2, p3));
-                }
-                l[nt][0] = l[nt][0] * al0 + ls0;
-                l[nt][1] = l[nt][1] * al1 + ls1;
+                const float p0 = exp2f((z[0] - mr0) * kLog2e);
+                const float p1 = exp2f((z[1] - mr1) * kLog2e);
+                const float p2 = exp2f((z[2] - mr0) * kLog2e);
+                const float p3 = exp2f((z[3] - mr1) * kLog2e);
+                pb[nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tlo
+                pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));
+                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
 #pragma unroll
                 for (int mt = 0; mt < KT; ++mt) {
                     acc[mt][nt][0] *= al0;
@@ -1380,39 +1267,36 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 }
             }
 
-            // acc^T[head dim][head] += V^T . P^T, page by page.  Split value page
-            // [d][16 tokens]: one 32-bit load is four permuted tokens of a head
-            // dim.  NHD page [token][d]: one load is four head dims of a token;
-            // movmatrix turns each 8 x 8 block (tokens x head dims 16mt + 4cq +
-            // {0,1} or {2,3}) into the A fragment, whose rows are then head dims
-            // 16mt + tau(r) (rows r) and 16mt + tau(r) + 2 (rows r + 8).
+            // acc^T[head dim][head] += V^T . P^T.  Split value page [d][16
+            // tokens]: one 32-bit load is four permuted tokens of a head dim.  NHD
+            // page [token][d]: one load is four head dims of a token; movmatrix
+            // turns each 8 x 8 block (tokens x head dims 16mt + 4cq + {0,1} or
+            // {2,3}) into the A fragment, whose rows are then head dims 16mt +
+            // tau(r) (rows r) and 16mt + tau(r) + 2 (rows r + 8).
 #pragma unroll
             for (int mt = 0; mt < KT; mt += 2) {
+                // words of rows r and r + 8 (head dims, or tokens for NHD) of
+                // m-tiles mt and mt + 1 in one ldmatrix.x4
+                uint32_t w[4];
+                ldsm_x4(vp + v8_frag_off<LAYOUT, HEAD>(lane, mt), w[0], w[1], w[2], w[3]);
 #pragma unroll
-                for (int q = 0; q < PPS; ++q) {
-                    // words of rows r and r + 8 (head dims, or tokens for NHD) of
-                    // m-tiles mt and mt + 1 in one ldmatrix.x4
-                    uint32_t w[4];
-                    ldsm_x4(vp + q * C::kPageBytes + v8_frag_off<LAYOUT, HEAD>(lane, mt), w[0], w[1], w[2], w[3]);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        uint32_t a0, a1, a2, a3;
-                        if constexpr (LAYOUT == kNHD) {
-                            uint32_t lo0, hi0, lo1, hi1;
-                            fp8x4_to_f16<KV>(w[2 * u], lo0, hi0);
-                            fp8x4_to_f16<KV>(w[2 * u + 1], lo1, hi1);
-                            a0 = movmatrix_trans(lo0);
-                            a1 = movmatrix_trans(hi0);
-                            a2 = movmatrix_trans(lo1);
-                            a3 = movmatrix_trans(hi1);
-                        } else {
-                            fp8x4_to_f16<KV>(w[2 * u], a0, a2);
-                            fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_16816<false>(acc[mt + u][nt], a0, a1, a2, a3, pb[q][nt][0], pb[q][nt][1]);
+                for (int u = 0; u < 2; ++u) {
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (LAYOUT == kNHD) {
+                        uint32_t lo0, hi0, lo1, hi1;
+                        fp8x4_to_f16<KV>(w[2 * u], lo0, hi0);
+                        fp8x4_to_f16<KV>(w[2 * u + 1], lo1, hi1);
+                        a0 = movmatrix_trans(lo0);
+                        a1 = movmatrix_trans(hi0);
+                        a2 = movmatrix_trans(lo1);
+                        a3 = movmatrix_trans(hi1);
+                    } else {
+                        fp8x4_to_f16<KV>(w[2 * u], a0, a2);
+                        fp8x4_to_f16<KV>(w[2 * u + 1], a1, a3);
                     }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816<false>(acc[mt + u][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
             }
             __syncwarp();
@@ -1456,7 +1340,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
             *sm.abort = 1;
             return;
         }
-        gbase += (uint32_t)nstages;
+        gbase += (uint32_t)npages;
     }
 }
 
@@ -1978,35 +1862,24 @@ __global__ void __launch_bounds__(WARPS * 32) pa_reduce_kernel(const Params p) {
     }
 }
 
-// Phase 2 with one warp per (sequence, query token, head) row, for batches of
-// many rows with few partitions each (a CTA per row would need several waves
-// of mostly idle CTAs).  Lane i holds the statistics of partitions i, i + 32,
-// ... and HEAD/32 columns of every partition output; the first eight partition
-// outputs are loaded together with the statistics, so a row of up to eight
-// partitions costs one round trip.  No shared memory, no block barrier.
-template <typename T, int HEAD, bool MQ>
-__global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel(const Params p) {
+// Phase 2 of one (query row, head) by one warp: M = max_p m_p, w_p = exp(m_p
+// - M) e_p / sum, out = sum_p w_p tmp_p.  Lane i holds the statistics of
+// partitions p0 + i, p0 + i + 32, ... and HEAD/32 columns of every partition
+// output; the first eight partition outputs are loaded together with the
+// statistics, so a row of up to eight partitions costs one round trip.  Then
+// the row's statistics move to absolute ALiBi positions and its unused
+// partitions are padded (every read of them is above, in this warp).
+// L2ONLY: every load through L2 only (the merge inside the partition kernel
+// reads what other CTAs of the same grid wrote); otherwise the partition
+// outputs are read with an evict_first hint (their last use).
+template <typename T, int HEAD, bool L2ONLY>
+__device__ __forceinline__ void merge_row_warp(const Params& p, int64_t row, int h, int len, int qn, int qi,
+                                               int lane) {
     constexpr int VEC = HEAD / 32;  // columns per lane: 4 (HEAD 128) or 2 (HEAD 64)
     constexpr int PRE = 8;          // partition outputs loaded before the weights are known
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_launch_dependents();
-    pdl_wait_primary();
-
-    const int64_t rid = (int64_t)blockIdx.x * kReduceWarpsPerCta + warp;
-    const int64_t nrows = (int64_t)p.num_seqs * (MQ ? p.max_q_len : 1) * p.num_heads;
-    if (rid >= nrows) return;
-    const int sq = (int)(rid / p.num_heads), h = (int)(rid - (int64_t)sq * p.num_heads);
-    const int s = MQ ? sq / p.max_q_len : sq, qi = MQ ? sq - s * p.max_q_len : 0;
-    int q0 = s, qn = 1;
-    if constexpr (MQ) {
-        query_rows(p, s, q0, qn);
-        if (qi >= qn) return;
-    }
-    const int len = clamp_len(p, p.seq_lens[s]);
     const int hi = len - qn + qi;                      // the query token's position
     const int P = hi >= 0 ? (hi + kPart) / kPart : 0;  // partitions holding its keys
     const int p0 = window_lo_at(p, hi) / kPart;        // partitions before p0: outside the window
-    const int64_t row = (int64_t)q0 + qi;
     const int64_t sb = (row * p.num_heads + h) * p.max_parts;
     float* ml = p.max_logits + sb;
     float* es = p.exp_sums + sb;
@@ -2016,13 +1889,16 @@ __global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel
     const uint64_t pol = l2_policy_evict_first();  // partition outputs: last use
     auto load_out = [&](int q, float (&t)[VEC]) {
         if constexpr (VEC == 4) {
-            const float4 v = ld_global_v4_hint(tmp + (int64_t)q * HEAD, pol);
+            const float4 v = L2ONLY ? __ldcg(reinterpret_cast<const float4*>(tmp + (int64_t)q * HEAD))
+                                    : ld_global_v4_hint(tmp + (int64_t)q * HEAD, pol);
             t[0] = v.x; t[1] = v.y; t[2] = v.z; t[3] = v.w;
         } else {
-            const float2 v = ld_global_v2_hint(tmp + (int64_t)q * HEAD, pol);
+            const float2 v = L2ONLY ? __ldcg(reinterpret_cast<const float2*>(tmp + (int64_t)q * HEAD))
+                                    : ld_global_v2_hint(tmp + (int64_t)q * HEAD, pol);
             t[0] = v.x; t[1] = v.y;
         }
     };
+    auto ld_stat = [&](const float* a) { return L2ONLY ? __ldcg(a) : *a; };
     float pre[PRE][VEC];
 #pragma unroll
     for (int k = 0; k < PRE; ++k) {
@@ -2034,13 +1910,13 @@ __global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel
         }
     }
     const int q1 = p0 + lane;
-    const float m1 = q1 < P ? ml[q1] : -INFINITY;
-    const float e1 = q1 < P ? es[q1] : 0.f;
+    const float m1 = q1 < P ? ld_stat(ml + q1) : -INFINITY;
+    const float e1 = q1 < P ? ld_stat(es + q1) : 0.f;
 
     // global max and weight sum over the row's partitions (lanes, then the warp)
     float M = m1, W = m1 == -INFINITY ? 0.f : e1;
     for (int q = q1 + 32; q < P; q += 32) {
-        const float m = ml[q], e = es[q];
+        const float m = ld_stat(ml + q), e = ld_stat(es + q);
         if (m == -INFINITY) continue;
         if (m > M) {
             W = (M == -INFINITY) ? 0.f : W * expf(M - m);
@@ -2074,8 +1950,8 @@ __global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel
             const int q = qb + lane;
             c = 0.f;
             if (q < P) {
-                const float m = ml[q];
-                c = m == -INFINITY ? 0.f : expf(m - M) * es[q] * invW;
+                const float m = ld_stat(ml + q);
+                c = m == -INFINITY ? 0.f : expf(m - M) * ld_stat(es + q) * invW;
             }
         }
         float t[PRE][VEC];
@@ -2125,6 +2001,29 @@ __global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel
             es[q] = 0.f;
         }
     }
+}
+
+// Phase 2 with one warp per (sequence, query token, head) row, for batches of
+// many rows with few partitions each (a CTA per row would need several waves
+// of mostly idle CTAs).  No shared memory, no block barrier.
+template <typename T, int HEAD, bool MQ>
+__global__ void __launch_bounds__(kReduceWarpsPerCta * 32) pa_reduce_warp_kernel(const Params p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait_primary();
+
+    const int64_t rid = (int64_t)blockIdx.x * kReduceWarpsPerCta + warp;
+    const int64_t nrows = (int64_t)p.num_seqs * (MQ ? p.max_q_len : 1) * p.num_heads;
+    if (rid >= nrows) return;
+    const int sq = (int)(rid / p.num_heads), h = (int)(rid - (int64_t)sq * p.num_heads);
+    const int s = MQ ? sq / p.max_q_len : sq, qi = MQ ? sq - s * p.max_q_len : 0;
+    int q0 = s, qn = 1;
+    if constexpr (MQ) {
+        query_rows(p, s, q0, qn);
+        if (qi >= qn) return;
+    }
+    const int len = clamp_len(p, p.seq_lens[s]);
+    merge_row_warp<T, HEAD, false>(p, (int64_t)q0 + qi, h, len, qn, qi, lane);
 }
 
 }  // namespace pa

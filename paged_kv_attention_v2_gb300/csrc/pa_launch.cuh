@@ -45,8 +45,7 @@ constexpr int kMaxDevices = 64;
 template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     constexpr int STAGES = std::is_same<T, float>::value ? (NT == 1 ? kStagesF32 : kStagesF32x2)
-                           : (KV == kKvSame ? kStages16
-                                            : (NT == 1 && LAYOUT == kNHD ? kStagesFp8Pairs : kStagesFp8));
+                           : (KV == kKvSame ? kStages16 : kStagesFp8);
     constexpr int NC = kConsumerWarps;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
     auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
@@ -72,7 +71,9 @@ cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
     // number of tiles instead of a last round that leaves most CTAs idle
     // (1024 tiles: 256 CTAs x 4 instead of 304 CTAs with 112 doing a 4th).
     // tiles_upper is exact for equal lengths and only an upper bound otherwise.
-    {
+    // The dynamic schedule keeps every resident CTA: its tiles go to whichever
+    // CTA is free, so no CTA waits on a fixed share.
+    if (!p_in.tile_ctr) {
         const int64_t rounds = (la.tiles_upper + grid - 1) / grid;
         grid = (la.tiles_upper + rounds - 1) / rounds;
     }

@@ -65,7 +65,11 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
     multi = dev["query_start"] is not None
     R = w.num_query_tokens if multi else S  # rows of query / out / workspace
     out = torch.full((R, H, d), float("nan"), dtype=torch_dtype(w.dtype), device=device)
-    ws = pa.alloc_workspace(S, H, d, msl, device, num_query_tokens=R if multi else None)
+    # modes "auto" and "v2f" take the dynamic tile schedule, "v1" and "v2" the static one
+    dynamic = mode == "auto" or fused
+    ws = pa.alloc_workspace(S, H, d, msl, device, num_query_tokens=R if multi else None,
+                            tile_counters=dynamic)
+    tctr = ws.pop("tile_counters", None)
     mq = {"query_start": dev["query_start"], "max_query_len": w.max_query_len} if multi else {}
     if poison_workspace:
         for t in ws.values():
@@ -77,7 +81,7 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                 seq_lens_host=w.seq_lens if mode == "auto" else None,
                 window_left=getattr(w, "window_left", -1),
                 kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
-                v_scale=getattr(w, "v_scale", 1.0), **mq, **ws)
+                v_scale=getattr(w, "v_scale", 1.0), tile_counters=tctr, **mq, **ws)
     tensors = (out, dev["query"], dev["key_cache"], dev["value_cache"],
                dev["block_tables"] if block_tables is None else block_tables,
                dev["seq_lens"] if seq_lens is None else seq_lens)
@@ -87,6 +91,8 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
     torch.cuda.synchronize(device)
     if counters is not None:
         assert int(counters.abs().sum().item()) == 0, "partition counters not returned to zero"
+    if tctr is not None:
+        assert int(tctr.abs().sum().item()) == 0, "tile counters not returned to zero"
     return {
         "out": out.double().cpu().numpy(),
         "max_logits": ws["max_logits"].double().cpu().numpy(),

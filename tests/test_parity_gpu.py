@@ -388,7 +388,7 @@ def test_cuda_graph_capture_replays_the_same_result(mode):
 
 
 def _plan(name, H, Hkv, d, dtype, lens, layout="split", kv=None, mode="auto", counters=True,
-          q_len=None):
+          q_len=None, dynamic=False):
     """pa_plan for a batch shape; the tensors only carry shapes (plan reads no memory)."""
     S, L = len(lens), int(max(lens))
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
@@ -401,7 +401,7 @@ def _plan(name, H, Hkv, d, dtype, lens, layout="split", kv=None, mode="auto", co
     sl = torch.zeros(S, dtype=torch.int32, device="cuda:0")
     import paged_kv_attention_v2_gb300 as pa
     ws = pa.alloc_workspace(S, H, d, L, "cuda:0", num_kv_heads=Hkv if counters else None,
-                            num_query_tokens=None if q_len is None else rows)
+                            num_query_tokens=None if q_len is None else rows, tile_counters=dynamic)
     extra = {}
     if q_len is not None:
         extra = dict(query_start=torch.arange(0, rows + 1, q_len, dtype=torch.int32, device="cuda:0"),
@@ -420,6 +420,10 @@ def test_plan_reports_each_path():
     assert g["ctas_per_sm"] == 2 and g["tiles"] == 1024
     rounds = -(-1024 // (sm * 2))
     assert g["grid"] == -(-1024 // rounds)
+    g = _plan("gqa4k", 28, 4, 128, "f16", [4096] * 32, dynamic=True)   # equal tiles: static
+    assert (g["dynamic_schedule"], g["grid"]) == (False, 256 if sm == 152 else g["grid"])
+    g = _plan("mixed", 28, 4, 128, "f16", [4096, 2000] * 16, dynamic=True)  # every resident CTA
+    assert (g["dynamic_schedule"], g["grid"]) == (True, min(g["tiles"], sm * 2))
     g = _plan("one_round", 28, 4, 128, "f16", [4096] * 4)           # 128 tiles: one round
     assert (g["mode"], g["merge_in_kernel"], g["kernels"], g["grid"]) == ("v2", True, 1, 128)
     g = _plan("one_round", 28, 4, 128, "f16", [4096] * 4, counters=False)
@@ -428,7 +432,7 @@ def test_plan_reports_each_path():
     assert (g["mode"], g["merge_in_kernel"], g["kernels"], g["tiles"]) == ("v2", False, 2, 3136)
     assert g["grid"] == -(-3136 // -(-3136 // (sm * 2)))
     assert _plan("fp8", 28, 4, 128, "f16", [4096] * 32, kv="e4m3")["ctas_per_sm"] == 3
-    assert _plan("fp8", 28, 4, 128, "f16", [4096] * 32, kv="e4m3", layout="nhd")["ctas_per_sm"] == 2
+    assert _plan("fp8", 28, 4, 128, "f16", [4096] * 32, kv="e4m3", layout="nhd")["ctas_per_sm"] == 3
     assert _plan("f32", 28, 4, 128, "f32", [4096] * 32)["ctas_per_sm"] == 2
     assert _plan("f32", 64, 4, 128, "f32", [4096] * 32)["ctas_per_sm"] == 1   # group 16: two n-tiles
     g = _plan("large", 64, 8, 128, "bf16", [16384] * 128)
