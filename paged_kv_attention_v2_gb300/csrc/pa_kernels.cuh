@@ -648,6 +648,106 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
     return true;
 }
 
+// ------------------------------------------------------------ online softmax
+
+// Logits may exceed the running reference max by this much (natural-log units,
+// 8 ln 2) before the reference moves: p = exp(z - m) then stays below 2^8,
+// well inside the range of the fp16 / bf16 P operand.
+constexpr float kLazyMax = 5.545177444479562f;
+
+// One page of the online softmax of [Online normalizer calculation for
+// softmax, Alg. 3] as the partition loop of paged attention uses it: rows are
+// the page's tokens, columns this lane's heads.  z holds the logits (-inf where
+// masked) and becomes p = exp(z - m).  The reference m of each head is the
+// same in every lane of the warp; it moves only when some logit exceeds it by
+// more than kLazyMax, and then to the running max of the whole warp (three
+// shuffle rounds), with l and acc rescaled.  Otherwise a page costs no
+// shuffle and no rescale.  mx keeps this lane's running max, for the exact
+// statistics at the end of the tile (settle_max).
+template <int NT, int KT, bool MQ>
+__device__ __forceinline__ void softmax_page(float (&z)[NT][4], float (&m)[NT][2], float (&mx)[NT][2],
+                                             float (&l)[NT][2], float (&acc)[KT][NT][4], bool edge) {
+    bool need = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const float a = fmaxf(z[nt][0], z[nt][2]), b = fmaxf(z[nt][1], z[nt][3]);
+        mx[nt][0] = fmaxf(mx[nt][0], a);
+        mx[nt][1] = fmaxf(mx[nt][1], b);
+        need |= (a - m[nt][0] > kLazyMax) || (b - m[nt][1] > kLazyMax);  // -inf - -inf: false
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float mn0 = mx[nt][0], mn1 = mx[nt][1];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mn0 = fmaxf(mn0, __shfl_xor_sync(0xffffffffu, mn0, o));
+                mn1 = fmaxf(mn1, __shfl_xor_sync(0xffffffffu, mn1, o));
+            }
+            // several query tokens: a row with no key in its range so far keeps
+            // max -inf (masked pages only); take 0 as reference so no -inf - -inf
+            // appears.  One token: every page holds a key of every row.
+            const float mr0 = (MQ && mn0 == -INFINITY) ? 0.f : mn0;
+            const float mr1 = (MQ && mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
+            const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+            l[nt][0] *= al0;
+            l[nt][1] *= al1;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+                acc[mt][nt][0] *= al0;
+                acc[mt][nt][1] *= al1;
+                acc[mt][nt][2] *= al0;
+                acc[mt][nt][3] *= al1;
+            }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const float mr0 = (MQ && edge && m[nt][0] == -INFINITY) ? 0.f : m[nt][0];
+        const float mr1 = (MQ && edge && m[nt][1] == -INFINITY) ? 0.f : m[nt][1];
+        z[nt][0] = exp2f((z[nt][0] - mr0) * kLog2e);
+        z[nt][1] = exp2f((z[nt][1] - mr1) * kLog2e);
+        z[nt][2] = exp2f((z[nt][2] - mr0) * kLog2e);
+        z[nt][3] = exp2f((z[nt][3] - mr1) * kLog2e);
+        l[nt][0] += z[nt][0] + z[nt][2];
+        l[nt][1] += z[nt][1] + z[nt][3];
+    }
+}
+
+// End of a warp's pages of a tile: move the reference of each head to the
+// warp's exact running max (what the partition statistics hold), rescaling l
+// and acc once.
+template <int NT, int KT>
+__device__ __forceinline__ void settle_max(float (&m)[NT][2], float (&mx)[NT][2], float (&l)[NT][2],
+                                           float (&acc)[KT][NT][4]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float mn0 = mx[nt][0], mn1 = mx[nt][1];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mn0 = fmaxf(mn0, __shfl_xor_sync(0xffffffffu, mn0, o));
+            mn1 = fmaxf(mn1, __shfl_xor_sync(0xffffffffu, mn1, o));
+        }
+        // equal (also both -inf: no key seen): nothing to move
+        const float al0 = mn0 == m[nt][0] ? 1.f : exp2f((m[nt][0] - mn0) * kLog2e);
+        const float al1 = mn1 == m[nt][1] ? 1.f : exp2f((m[nt][1] - mn1) * kLog2e);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+        l[nt][0] *= al0;
+        l[nt][1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+            acc[mt][nt][0] *= al0;
+            acc[mt][nt][1] *= al1;
+            acc[mt][nt][2] *= al0;
+            acc[mt][nt][3] *= al1;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ consumers
 
 // Byte offset of this lane's ldmatrix row address inside a K page for k-step kk
@@ -806,11 +906,11 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;  // ALiBi positions are taken relative to this token
 
-        float m[NT][2], l[NT][2];
+        float m[NT][2], l[NT][2], mx[NT][2];  // reference max, sum, this lane's running max
         float acc[KT][NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            m[nt][0] = m[nt][1] = -INFINITY;
+            m[nt][0] = m[nt][1] = mx[nt][0] = mx[nt][1] = -INFINITY;
             l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt)
@@ -863,55 +963,50 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
 
+            // One n-tile: the page's V fragments go to registers here and the
+            // stage back to the producer, before the softmax and P.V, so the
+            // stage is refilled while they run (two n-tiles have no registers
+            // to spare and load V in the P.V loop).
+            constexpr bool kEarlyV = NT == 1;
+            uint32_t vf[kEarlyV ? KT : 1][4];
+            if constexpr (kEarlyV) {
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    if constexpr (LAYOUT == kSplit)
+                        ldsm_x4(vp + v_frag_off<LAYOUT>(lane, mt), vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3]);
+                    else
+                        ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), vf[mt][0], vf[mt][1], vf[mt][2],
+                                      vf[mt][3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            }
+
             // logits, online softmax, P as B fragments of P.V
             const int tlo = tok0 + r;  // this thread's tokens: tlo (e=0,1), tlo+8 (e=2,3)
             uint32_t pb[NT][2], pbl[NT][2];
+            float z[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float z[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = s[nt][e] * p.scale;
                     if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tlo + ((e >> 1) << 3) - origin);
-                    z[e] = v;
+                    z[nt][e] = v;
                 }
                 if (edge) {
                     const int t0 = tok0 + r, t1 = t0 + 8;
-                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
-                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
-                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
-                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[nt][0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[nt][1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[nt][2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[nt][3] = -INFINITY;
                 }
-                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+            }
+            softmax_page<NT, KT, C::kMQ>(z, m, mx, l, acc, edge);
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                // several query tokens: a row with no key in its range so far keeps
-                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
-                // appears.  One token: every page holds a key of every row.
-                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
-                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
-                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
-                m[nt][0] = mn0;
-                m[nt][1] = mn1;
-                const float p0 = exp2f((z[0] - mr0) * kLog2e);
-                const float p1 = exp2f((z[1] - mr1) * kLog2e);
-                const float p2 = exp2f((z[2] - mr0) * kLog2e);
-                const float p3 = exp2f((z[3] - mr1) * kLog2e);
-                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
-                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
-#pragma unroll
-                for (int mt = 0; mt < KT; ++mt) {
-                    acc[mt][nt][0] *= al0;
-                    acc[mt][nt][1] *= al1;
-                    acc[mt][nt][2] *= al0;
-                    acc[mt][nt][3] *= al1;
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                const float p0 = z[nt][0], p1 = z[nt][1], p2 = z[nt][2], p3 = z[nt][3];
                 const uint32_t x0 = pack2<BF>(p0, p1);  // token r,   heads 2cq, 2cq+1
                 const uint32_t x1 = pack2<BF>(p2, p3);  // token r+8
                 pb[nt][0] = movmatrix_trans(x0);         // -> B[k = token 2cq..][n = head r]
@@ -929,21 +1024,30 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                if constexpr (LAYOUT == kSplit)
+                if constexpr (kEarlyV) {
+                    a0 = vf[mt][0];
+                    a1 = vf[mt][1];
+                    a2 = vf[mt][2];
+                    a3 = vf[mt][3];
+                } else if constexpr (LAYOUT == kSplit) {
                     ldsm_x4(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
-                else
+                } else {
                     ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                     if constexpr (BF) mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pbl[nt][0], pbl[nt][1]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            if constexpr (!kEarlyV) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            }
         }
 
         // this warp's partial state -> shared memory
+        settle_max<NT, KT>(m, mx, l, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -1152,11 +1256,11 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
         const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;
 
-        float m[NT][2], l[NT][2];
+        float m[NT][2], l[NT][2], mx[NT][2];  // reference max, sum, this lane's running max
         float acc[KT][NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            m[nt][0] = m[nt][1] = -INFINITY;
+            m[nt][0] = m[nt][1] = mx[nt][0] = mx[nt][1] = -INFINITY;
             l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt)
@@ -1216,55 +1320,43 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 }
             }
 
+            // One n-tile: the page's V words go to registers here and the stage
+            // back to the producer, before the softmax, the conversion and P.V.
+            constexpr bool kEarlyV = NT == 1;
+            uint32_t vw[kEarlyV ? KT / 2 : 1][4];
+            if constexpr (kEarlyV) {
+#pragma unroll
+                for (int mt = 0; mt < KT; mt += 2)
+                    ldsm_x4(vp + v8_frag_off<LAYOUT, HEAD>(lane, mt), vw[mt / 2][0], vw[mt / 2][1],
+                            vw[mt / 2][2], vw[mt / 2][3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            }
+
             uint32_t pb[NT][2];
+            float z[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float z[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = (s[nt][e] + s2[nt][e]) * p.scale;
                     if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + ((e >> 1) ? thi : tlo) - origin);
-                    z[e] = v;
+                    z[nt][e] = v;
                 }
                 if (edge) {
                     const int t0 = tok0 + tlo, t1 = tok0 + thi;
-                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
-                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
-                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
-                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[nt][0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[nt][1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[nt][2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[nt][3] = -INFINITY;
                 }
-                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+            }
+            softmax_page<NT, KT, C::kMQ>(z, m, mx, l, acc, edge);
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                // several query tokens: a row with no key in its range so far keeps
-                // max -inf (masked pages only); take 0 as reference so no -inf - -inf
-                // appears.  One token: every page holds a key of every row.
-                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
-                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
-                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
-                m[nt][0] = mn0;
-                m[nt][1] = mn1;
-                const float p0 = exp2f((z[0] - mr0) * kLog2e);
-                const float p1 = exp2f((z[1] - mr1) * kLog2e);
-                const float p2 = exp2f((z[2] - mr0) * kLog2e);
-                const float p3 = exp2f((z[3] - mr1) * kLog2e);
-                pb[nt][0] = movmatrix_trans(pack2<false>(p0, p1));  // k-index 2cq.. = tokens tlo
-                pb[nt][1] = movmatrix_trans(pack2<false>(p2, p3));
-                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
-                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
-#pragma unroll
-                for (int mt = 0; mt < KT; ++mt) {
-                    acc[mt][nt][0] *= al0;
-                    acc[mt][nt][1] *= al1;
-                    acc[mt][nt][2] *= al0;
-                    acc[mt][nt][3] *= al1;
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                pb[nt][0] = movmatrix_trans(pack2<false>(z[nt][0], z[nt][1]));  // k-index 2cq.. = tokens tlo
+                pb[nt][1] = movmatrix_trans(pack2<false>(z[nt][2], z[nt][3]));
             }
 
             // acc^T[head dim][head] += V^T . P^T.  Split value page [d][16
@@ -1278,7 +1370,14 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 // words of rows r and r + 8 (head dims, or tokens for NHD) of
                 // m-tiles mt and mt + 1 in one ldmatrix.x4
                 uint32_t w[4];
-                ldsm_x4(vp + v8_frag_off<LAYOUT, HEAD>(lane, mt), w[0], w[1], w[2], w[3]);
+                if constexpr (kEarlyV) {
+                    w[0] = vw[mt / 2][0];
+                    w[1] = vw[mt / 2][1];
+                    w[2] = vw[mt / 2][2];
+                    w[3] = vw[mt / 2][3];
+                } else {
+                    ldsm_x4(vp + v8_frag_off<LAYOUT, HEAD>(lane, mt), w[0], w[1], w[2], w[3]);
+                }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     uint32_t a0, a1, a2, a3;
@@ -1299,10 +1398,13 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                         mma_16816<false>(acc[mt + u][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            if constexpr (!kEarlyV) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty + st * 8);
+            }
         }
 
+        settle_max<NT, KT>(m, mx, l, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -1661,11 +1763,13 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
 // fp32 tensor-core consumer holds Q as two tf32 terms (~213): cap them so that
 // two CTAs share an SM, as they do for one n-tile of 16-bit inputs.  fp32 with
 // two n-tiles fills an SM's shared memory with one CTA (16 KB stages): no cap.
+// fp8 with one n-tile: capped for three CTAs per SM (128 registers: fifteen
+// warps put four on some SM sub-partition, whose register file is 16 K).
 template <typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC, int KV, bool MQ>
 __global__ void __launch_bounds__((NC + 1) * 32,
                                   (std::is_same<T, float>::value && NT > 1)
                                       ? 1
-                                      : ((NT > 1 || std::is_same<T, float>::value) ? 2 : 1))
+                                      : ((NT > 1 || std::is_same<T, float>::value) ? 2 : (KV != kKvSame ? 3 : 1)))
     pa_partition_kernel(const Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
