@@ -40,13 +40,18 @@ constexpr int kKvE4M3 = 1;      // fp8 E4M3
 constexpr int kKvE5M2 = 2;      // fp8 E5M2
 
 // Shape of the partition kernel.  Ring stages per cache type, one 16-token
-// page of K and V each: fp8 pages take 12 stages so that three CTAs share an
-// SM, fp32 pages with two n-tiles 8 stages of 16 KB (one CTA per SM).
-constexpr int kStages16 = 8;       // 16-bit caches
+// page of K and V each: 16-bit pages with one n-tile take 10 stages and five
+// consumer warps (two CTAs of 106 KB per SM), with two n-tiles 8 stages and
+// four warps (their merge buffers are twice as large); fp8 pages 12 stages so
+// that three CTAs share an SM, fp32 pages with two n-tiles 8 stages of 16 KB
+// (one CTA per SM).  The stages are a multiple of the consumer warps.
+constexpr int kStages16 = 10;      // 16-bit caches, one n-tile (five consumer warps)
+constexpr int kStages16x2 = 8;     // 16-bit caches, two n-tiles
 constexpr int kStagesFp8 = 12;     // fp8 caches (three CTAs per SM fit)
 constexpr int kStagesF32 = 4;      // fp32 caches, one n-tile (two CTAs per SM)
 constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
 constexpr int kConsumerWarps = 4;  // consumer warps per CTA
+constexpr int kConsumerWarps16 = 5;  // consumer warps per CTA, 16-bit caches with one n-tile
 constexpr int kPrefetchPages = 16; // pages of the first tile prefetched into L2 before the grid wait
 constexpr int kReduceWarpMaxParts = 64;  // warp-per-row reduce up to this many partitions per row
 
@@ -1534,11 +1539,11 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
         const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;
 
-        float m[NT][2], l[NT][2];
+        float m[NT][2], l[NT][2], mx[NT][2];  // reference max, sum, this lane's running max
         float acc[MT][NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            m[nt][0] = m[nt][1] = -INFINITY;
+            m[nt][0] = m[nt][1] = mx[nt][0] = mx[nt][1] = -INFINITY;
             l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
@@ -1622,50 +1627,30 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
 
             // logits, online softmax, P^T as B fragments (hi and lo) per n-tile
             uint32_t pbh[NT][2][2], pbl[NT][2][2];
+            float z[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float z[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = (s[nt][e] + s2[nt][e]) * p.scale;
                     if (has_cap) v = p.softcap * tanhf(v * p.inv_softcap);
                     if (has_alibi) v += sl[nt][e & 1] * (float)(tok0 + r + ((e >> 1) << 3) - origin);
-                    z[e] = v;
+                    z[nt][e] = v;
                 }
                 if (edge) {
                     const int t0 = tok0 + r, t1 = t0 + 8;
-                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[0] = -INFINITY;
-                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[1] = -INFINITY;
-                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[2] = -INFINITY;
-                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[3] = -INFINITY;
+                    if (t0 < klo[nt][0] || t0 > khi[nt][0]) z[nt][0] = -INFINITY;
+                    if (t0 < klo[nt][1] || t0 > khi[nt][1]) z[nt][1] = -INFINITY;
+                    if (t1 < klo[nt][0] || t1 > khi[nt][0]) z[nt][2] = -INFINITY;
+                    if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[nt][3] = -INFINITY;
                 }
-                float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+            }
+            softmax_page<NT, MT, C::kMQ>(z, m, mx, l, acc, edge);
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                const float mr0 = (C::kMQ && edge && mn0 == -INFINITY) ? 0.f : mn0;
-                const float mr1 = (C::kMQ && edge && mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = exp2f((m[nt][0] - mr0) * kLog2e);
-                const float al1 = exp2f((m[nt][1] - mr1) * kLog2e);
-                m[nt][0] = mn0;
-                m[nt][1] = mn1;
-                float pv[4];
-                pv[0] = exp2f((z[0] - mr0) * kLog2e);  // (token r,     row 2cq)
-                pv[1] = exp2f((z[1] - mr1) * kLog2e);  // (token r,     row 2cq + 1)
-                pv[2] = exp2f((z[2] - mr0) * kLog2e);  // (token r + 8, row 2cq)
-                pv[3] = exp2f((z[3] - mr1) * kLog2e);  // (token r + 8, row 2cq + 1)
-                l[nt][0] = l[nt][0] * al0 + (pv[0] + pv[2]);
-                l[nt][1] = l[nt][1] * al1 + (pv[1] + pv[3]);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    acc[mt][nt][0] *= al0;
-                    acc[mt][nt][1] *= al1;
-                    acc[mt][nt][2] *= al0;
-                    acc[mt][nt][3] *= al1;
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                // z[nt]: p of (token r, row 2cq), (token r, row 2cq + 1),
+                // (token r + 8, row 2cq), (token r + 8, row 2cq + 1)
+                const float* pv = z[nt];
                 // B fragments of P^T for k-steps ks = 0, 1 (tokens 8ks..8ks+7):
                 // b0 = P[row r][token 8ks + tk0], b1 = P[row r][token 8ks + tk1],
                 // held by lanes (token % 8, row / 2), element by row parity and ks
@@ -1722,6 +1707,7 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
         }
 
         float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+        settle_max<NT, MT>(m, mx, l, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
