@@ -199,6 +199,18 @@ struct Smem {
     uint64_t wait_ns;        // limit of every barrier wait
 };
 
+// Ring stage and phase parity of the page NC pages further on (a consumer
+// warp's next page of the tile): no division per page.
+template <int STAGES, int NC>
+__device__ __forceinline__ void advance_stage(uint32_t& st, uint32_t& ph) {
+    static_assert(NC <= STAGES, "a warp's next page is at most one lap ahead");
+    st += NC;
+    if (st >= STAGES) {
+        st -= STAGES;
+        ph ^= 1u;
+    }
+}
+
 // Bounded wait by every lane of a warp; the result is the same in all lanes.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
@@ -925,9 +937,14 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 
         const int npages = tile_pages(d.tok_begin, d.tok_end);
         const int page0 = d.tok_begin / kBS * kBS;  // first token of the tile's first page
-        for (int j = warp; j < npages; j += NC) {
-            const uint32_t gg = gbase + (uint32_t)j;
-            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+        // stage and phase of page j: advanced per page with one n-tile, computed
+        // per page with two (whose registers are all taken)
+        uint32_t st = (gbase + (uint32_t)warp) % STAGES, ph = ((gbase + (uint32_t)warp) / STAGES) & 1;
+        for (int j = warp; j < npages; j += NC, advance_stage<STAGES, NC>(st, ph)) {
+            if constexpr (NT > 1) {
+                st = (gbase + (uint32_t)j) % STAGES;
+                ph = ((gbase + (uint32_t)j) / STAGES) & 1;
+            }
             if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
@@ -1275,9 +1292,14 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
 
         const int npages = tile_pages(d.tok_begin, d.tok_end);
         const int page0 = d.tok_begin / kBS * kBS;
-        for (int j = warp; j < npages; j += NC) {
-            const uint32_t gg = gbase + (uint32_t)j;
-            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+        // stage and phase of page j: advanced per page with one n-tile, computed
+        // per page with two (whose registers are all taken)
+        uint32_t st = (gbase + (uint32_t)warp) % STAGES, ph = ((gbase + (uint32_t)warp) / STAGES) & 1;
+        for (int j = warp; j < npages; j += NC, advance_stage<STAGES, NC>(st, ph)) {
+            if constexpr (NT > 1) {
+                st = (gbase + (uint32_t)j) % STAGES;
+                ph = ((gbase + (uint32_t)j) / STAGES) & 1;
+            }
             if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
@@ -1558,9 +1580,14 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
         // P^T k-index cq holds token cq (split) or 2cq (NHD), cq + 4 token cq + 4 or 2cq + 1
         const int tk0 = LAYOUT == kSplit ? cq : 2 * cq, tk1 = LAYOUT == kSplit ? cq + 4 : 2 * cq + 1;
         const int src0 = 4 * tk0 + (r >> 1), src1 = 4 * tk1 + (r >> 1);
-        for (int j = warp; j < npages; j += NC) {
-            const uint32_t gg = gbase + (uint32_t)j;
-            const uint32_t st = gg % STAGES, ph = (gg / STAGES) & 1;
+        // stage and phase of page j: advanced per page with one n-tile, computed
+        // per page with two (whose registers are all taken)
+        uint32_t st = (gbase + (uint32_t)warp) % STAGES, ph = ((gbase + (uint32_t)warp) / STAGES) & 1;
+        for (int j = warp; j < npages; j += NC, advance_stage<STAGES, NC>(st, ph)) {
+            if constexpr (NT > 1) {
+                st = (gbase + (uint32_t)j) % STAGES;
+                ph = ((gbase + (uint32_t)j) / STAGES) & 1;
+            }
             if (!warp_wait(sm.full + st * 8, ph, sm.abort, sm.wait_ns)) {
                 report(p, PA_DEVERR_TIMEOUT);
                 *sm.abort = 1;
