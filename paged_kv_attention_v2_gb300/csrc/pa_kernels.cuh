@@ -40,18 +40,19 @@ constexpr int kKvE4M3 = 1;      // fp8 E4M3
 constexpr int kKvE5M2 = 2;      // fp8 E5M2
 
 // Shape of the partition kernel.  Ring stages per cache type, one 16-token
-// page of K and V each: 16-bit pages with one n-tile take 10 stages and five
-// consumer warps (two CTAs of 106 KB per SM), with two n-tiles 8 stages and
-// four warps (their merge buffers are twice as large); fp8 pages 12 stages so
-// that three CTAs share an SM, fp32 pages with two n-tiles 8 stages of 16 KB
-// (one CTA per SM).  The stages are a multiple of the consumer warps.
-constexpr int kStages16 = 10;      // 16-bit caches, one n-tile (five consumer warps)
+// page of K and V each.  One n-tile of 16-bit or fp32 pages: five consumer
+// warps, with 10 stages (16-bit) or 5 stages of 16 KB (fp32), two CTAs of
+// ~110 KB per SM; two n-tiles: four warps (their merge buffers are twice as
+// large), 8 stages (16-bit) or 8 stages of 16 KB (fp32, one CTA per SM); fp8
+// pages: four warps and 12 stages, so that three CTAs share an SM.  The
+// stages are a multiple of the consumer warps.
+constexpr int kStages16 = 10;      // 16-bit caches, one n-tile
 constexpr int kStages16x2 = 8;     // 16-bit caches, two n-tiles
 constexpr int kStagesFp8 = 12;     // fp8 caches (three CTAs per SM fit)
-constexpr int kStagesF32 = 4;      // fp32 caches, one n-tile (two CTAs per SM)
+constexpr int kStagesF32 = 5;      // fp32 caches, one n-tile (two CTAs per SM)
 constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
 constexpr int kConsumerWarps = 4;  // consumer warps per CTA
-constexpr int kConsumerWarps16 = 5;  // consumer warps per CTA, 16-bit caches with one n-tile
+constexpr int kConsumerWarps5 = 5; // consumer warps per CTA, 16-bit or fp32 caches with one n-tile
 constexpr int kPrefetchPages = 16; // pages of the first tile prefetched into L2 before the grid wait
 constexpr int kReduceWarpMaxParts = 64;  // warp-per-row reduce up to this many partitions per row
 

@@ -44,10 +44,9 @@ constexpr int kMaxDevices = 64;
 // CTAs; the separate reduce kernel spreads them over the whole GPU instead.
 template <typename T, int HEAD, int NT, int LAYOUT, int KV, bool MQ>
 cudaError_t launch_main(const Params& p_in, const LaunchArgs& la, bool* fused) {
-    constexpr bool k16 = KV == kKvSame && !std::is_same<T, float>::value;
     constexpr int STAGES = std::is_same<T, float>::value ? (NT == 1 ? kStagesF32 : kStagesF32x2)
                            : (KV == kKvSame ? (NT == 1 ? kStages16 : kStages16x2) : kStagesFp8);
-    constexpr int NC = (k16 && NT == 1) ? kConsumerWarps16 : kConsumerWarps;
+    constexpr int NC = (KV == kKvSame && NT == 1) ? kConsumerWarps5 : kConsumerWarps;
     using C = Cfg<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
     auto kern = pa_partition_kernel<T, HEAD, NT, LAYOUT, STAGES, NC, KV, MQ>;
 
