@@ -673,15 +673,16 @@ __device__ bool tile_finish(const Params& p, const TileDesc& d, const Smem& sm, 
 // well inside the range of the fp16 / bf16 P operand.
 constexpr float kLazyMax = 5.545177444479562f;
 
-// One page of the online softmax of [Online normalizer calculation for
-// softmax, Alg. 3] as the partition loop of paged attention uses it: rows are
-// the page's tokens, columns this lane's heads.  z holds the logits (-inf where
-// masked) and becomes p = exp(z - m).  The reference m of each head is the
-// same in every lane of the warp; it moves only when some logit exceeds it by
-// more than kLazyMax, and then to the running max of the whole warp (three
-// shuffle rounds), with l and acc rescaled.  Otherwise a page costs no
-// shuffle and no rescale.  mx keeps this lane's running max, for the exact
-// statistics at the end of the tile (settle_max).
+// One page of the online softmax (running max and sum, rescaled as new
+// logits arrive) with which a tile streams one partition of Phase 1
+// ("paged_attention_v2_pytorch.py -- BI-V100 PagedAttention V2", per-partition
+// attention): rows are the page's tokens, columns this lane's heads.  z holds
+// the logits (-inf where masked) and becomes p = exp(z - m).  The reference m
+// of each head is the same in every lane of the warp; it moves only when some
+// logit exceeds it by more than kLazyMax, and then to the running max of the
+// whole warp (three shuffle rounds), with l and acc rescaled.  Otherwise a
+// page costs no shuffle and no rescale.  mx keeps this lane's running max, for
+// the exact statistics at the end of the tile (settle_max).
 template <int NT, int KT, bool MQ>
 __device__ __forceinline__ void softmax_page(float (&z)[NT][4], float (&m)[NT][2], float (&mx)[NT][2],
                                              float (&l)[NT][2], float (&acc)[KT][NT][4], bool edge) {
