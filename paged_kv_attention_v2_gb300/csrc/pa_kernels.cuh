@@ -42,12 +42,12 @@ constexpr int kKvE5M2 = 2;      // fp8 E5M2
 // Shape of the partition kernel.  Ring stages per cache type, one 16-token
 // page of K and V each.  One n-tile of 16-bit or fp32 pages: five consumer
 // warps, with 10 stages (16-bit) or 5 stages of 16 KB (fp32), two CTAs of
-// ~110 KB per SM; two n-tiles: four warps (their merge buffers are twice as
-// large), 8 stages (16-bit) or 8 stages of 16 KB (fp32, one CTA per SM); fp8
-// pages: four warps and 12 stages, so that three CTAs share an SM.  The
-// stages are a multiple of the consumer warps.
+// ~110 KB per SM; two n-tiles: four warps, 10 stages for 16-bit pages (two
+// page streams of two warps, one n-tile each) or 8 stages of 16 KB for fp32
+// (one CTA per SM); fp8 pages: four warps and 12 stages, so that three CTAs
+// share an SM.  The stages are a multiple of the page streams.
 constexpr int kStages16 = 10;      // 16-bit caches, one n-tile
-constexpr int kStages16x2 = 8;     // 16-bit caches, two n-tiles
+constexpr int kStages16x2 = 10;    // 16-bit caches, two n-tiles (paired page streams)
 constexpr int kStagesFp8 = 12;     // fp8 caches (three CTAs per SM fit)
 constexpr int kStagesF32 = 5;      // fp32 caches, one n-tile (two CTAs per SM)
 constexpr int kStagesF32x2 = 8;    // fp32 caches, two n-tiles (one CTA per SM)
@@ -158,6 +158,11 @@ struct Cfg {
     // 34.2 -> 32.7 µs for the one-page stages.)
     static constexpr int kStageBytes = 2 * kPageBytes;  // K page, then V page
     static constexpr int kMaxG = NT * 8;                   // rows (heads x query tokens) handled
+    // 16-bit caches with two n-tiles: warps in pairs of page streams, one
+    // n-tile each (consumer_mma); every page is consumed by two warps.
+    static constexpr bool kPairs = NT == 2 && KV == kKvSame && !kF32;
+    static constexpr int kMergeRows = kPairs ? 8 : kMaxG;  // merge-buffer rows per warp
+    static constexpr int kPageWarps = kPairs ? 2 : 1;      // warps that release each page
     static constexpr int kQBytes = kMaxG * HEAD * kElem;
     static constexpr int kTD = 2;                          // tile descriptor ring depth
     static constexpr int kMergeStride = HEAD + 4;          // floats; +4 breaks bank conflicts
@@ -170,20 +175,22 @@ struct Cfg {
     static constexpr int oRing = 0;
     static constexpr int oQ = oRing + STAGES * kStageBytes;
     static constexpr int oMerge = oQ + kTD * kQBytes;
-    static constexpr int oML = oMerge + NC * kMaxG * kMergeStride * 4;
-    static constexpr int oDesc = oML + NC * kMaxG * 8;
+    static constexpr int oML = oMerge + NC * kMergeRows * kMergeStride * 4;
+    static constexpr int oDesc = oML + NC * kMergeRows * 8;
     static constexpr int oBar = (oDesc + kTD * (int)sizeof(TileDesc) + 7) & ~7;
     static constexpr int oAbort = oBar + (2 * STAGES + 2 * kTD + 1) * 8;
     static constexpr int kSmemBytes = oAbort + 16 + 1024;  // + slack for 1024-B alignment
 
     static_assert(kPageBytes % 1024 == 0 || !kTensorMap, "swizzled pages need 1024-B alignment");
-    // Within a tile, page j goes to consumer warp j % NC and to ring stage
-    // (base + j) % STAGES.  With STAGES a multiple of NC every page of a stage
-    // inside one tile belongs to the same warp, so no warp ever waits on a
-    // stage's full barrier more than one phase ahead (a parity wait cannot
-    // tell phase n from phase n + 2).  Across tiles the tile-end barrier of
+    // Within a tile, page j goes to page stream j % (NC / kPageWarps) (one
+    // warp, or two with paired streams, each releasing it) and to ring stage
+    // (base + j) % STAGES.  With STAGES a multiple of the streams every page of
+    // a stage inside one tile belongs to the same stream, so no warp ever waits
+    // on a stage's full barrier more than one phase ahead (a parity wait
+    // cannot tell phase n from phase n + 2): the stage is refilled only once
+    // both warps of a pair released it.  Across tiles the tile-end barrier of
     // the consumer warps gives the same guarantee.
-    static_assert(STAGES % NC == 0, "ring stages must be a multiple of the consumer warps");
+    static_assert(STAGES % (NC / kPageWarps) == 0, "ring stages must be a multiple of the page streams");
     static_assert(STAGES <= 32, "one producer lane per stage");
     static_assert(kQBytes % 16 == 0, "bulk copy size");
 };
@@ -548,18 +555,22 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
     // row v of the merge buffers: query token v / G, head kvh * G + v % G
     const int qn = C::kMQ ? d.qn : 1;
     const int n = qn * G * D4;
-    float2 e[ITEMS][NC];
-    float4 a[ITEMS][NC];
+    // warps holding a partial state of row h: all of them, or with paired page
+    // streams the WR warps of the row's n-tile (its rows at h % 8 of their buffers)
+    constexpr int WR = NC / C::kPageWarps;
+    float2 e[ITEMS][WR];
+    float4 a[ITEMS][WR];
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
         const int idx = tid + it * NC * 32;
         const int h = idx / D4, d4 = idx - h * D4;
+        const int w0 = C::kPairs ? (h >> 3) * WR : 0, hl = C::kPairs ? (h & 7) : h;
 #pragma unroll
-        for (int w = 0; w < NC; ++w) {
+        for (int w = 0; w < WR; ++w) {
             if (idx < n) {
-                e[it][w] = sm.ml[w * C::kMaxG + h];
+                e[it][w] = sm.ml[(w0 + w) * C::kMergeRows + hl];
                 a[it][w] = *reinterpret_cast<const float4*>(
-                    sm.merge + (w * C::kMaxG + h) * C::kMergeStride + 4 * d4);
+                    sm.merge + ((w0 + w) * C::kMergeRows + hl) * C::kMergeStride + 4 * d4);
             } else {
                 e[it][w] = make_float2(-INFINITY, 0.f);
                 a[it][w] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -573,11 +584,11 @@ __device__ void tile_epilogue(const Params& p, const TileDesc& d, const Smem& sm
         const int h = idx / D4, d4 = idx - h * D4;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NC; ++w) M = fmaxf(M, e[it][w].x);
+        for (int w = 0; w < WR; ++w) M = fmaxf(M, e[it][w].x);
         float L = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < NC; ++w) {
+        for (int w = 0; w < WR; ++w) {
             const float c = (e[it][w].x == -INFINITY) ? 0.f : exp2f((e[it][w].x - M) * kLog2e);
             L += c * e[it][w].y;
             o.x += c * a[it][w].x;
@@ -855,6 +866,14 @@ template <class C, typename T, int HEAD, int NT, int LAYOUT, int STAGES, int NC>
 __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane) {
     constexpr bool BF = C::kBF16;
     constexpr int KT = HEAD / 16;  // k-steps of Q.K^T, m-tiles of P.V
+    // Two n-tiles: the warps work in pairs of page streams, one n-tile each
+    // (rows nt0 * 8 .. nt0 * 8 + 7) on the pages j = pfirst (mod PSTRIDE), so
+    // every page is read by two warps, each with one n-tile's registers.
+    constexpr bool kPairs = C::kPairs;
+    constexpr int NTW = kPairs ? 1 : NT;          // n-tiles per warp
+    constexpr int PSTRIDE = kPairs ? NC / 2 : NC; // warps per page stream
+    const int nt0 = kPairs ? warp / PSTRIDE : 0;
+    const int pfirst = kPairs ? warp % PSTRIDE : warp;
     const int G = p.group;
     const int r = lane >> 2, cq = lane & 3;
     const bool has_alibi = p.alibi != nullptr;
@@ -874,11 +893,11 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         const int GE = qn * G;  // rows of N: query token v / G, head kvh * G + v % G
 
         // Q as B fragments: B[k = head dim][n = row], rows >= GE are zero.
-        uint32_t qb[NT][KT][2];
+        uint32_t qb[NTW][KT][2];
         const uint32_t qs = sm.q + slot * C::kQBytes;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int h = nt * 8 + r;
+        for (int nt = 0; nt < NTW; ++nt) {
+            const int h = (nt0 + nt) * 8 + r;
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t b0 = 0, b1 = 0;
@@ -894,22 +913,22 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.td_empty + slot * 8);  // Q and descriptor are in registers
 
-        float sl[NT][2];
+        float sl[NTW][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int h = nt * 8 + 2 * cq + e;
+                const int h = (nt0 + nt) * 8 + 2 * cq + e;
                 sl[nt][e] = (has_alibi && h < GE) ? __ldg(p.alibi + d.kvh * G + h % G) : 0.f;
             }
         // key range of each of this lane's rows: its query token's position and
         // window, within the tile (padded rows get the tile's range)
-        int klo[NT][2], khi[NT][2];
+        int klo[NTW][2], khi[NTW][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int v = nt * 8 + 2 * cq + e;
+                const int v = (nt0 + nt) * 8 + 2 * cq + e;
                 int lo = d.tok_begin, hi = d.tok_end - 1;
                 if (C::kMQ && v < GE) {
                     const int pos = d.len - qn + v / G;
@@ -925,10 +944,10 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         const int lo_all = C::kMQ ? max(d.tok_begin, window_lo_at(p, d.len - 1)) : d.tok_begin;
         const int origin = d.tok_end - 1;  // ALiBi positions are taken relative to this token
 
-        float m[NT][2], l[NT][2], mx[NT][2];  // reference max, sum, this lane's running max
-        float acc[KT][NT][4];
+        float m[NTW][2], l[NTW][2], mx[NTW][2];  // reference max, sum, this lane's running max
+        float acc[KT][NTW][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
             m[nt][0] = m[nt][1] = mx[nt][0] = mx[nt][1] = -INFINITY;
             l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
@@ -939,11 +958,11 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 
         const int npages = tile_pages(d.tok_begin, d.tok_end);
         const int page0 = d.tok_begin / kBS * kBS;  // first token of the tile's first page
-        // stage and phase of page j: advanced per page with one n-tile, computed
-        // per page with two (whose registers are all taken)
-        uint32_t st = (gbase + (uint32_t)warp) % STAGES, ph = ((gbase + (uint32_t)warp) / STAGES) & 1;
-        for (int j = warp; j < npages; j += NC, advance_stage<STAGES, NC>(st, ph)) {
-            if constexpr (NT > 1) {
+        // stage and phase of page j: advanced per page with one n-tile per warp,
+        // computed per page with two (whose registers are all taken)
+        uint32_t st = (gbase + (uint32_t)pfirst) % STAGES, ph = ((gbase + (uint32_t)pfirst) / STAGES) & 1;
+        for (int j = pfirst; j < npages; j += PSTRIDE, advance_stage<STAGES, PSTRIDE>(st, ph)) {
+            if constexpr (NTW > 1) {
                 st = (gbase + (uint32_t)j) % STAGES;
                 ph = ((gbase + (uint32_t)j) / STAGES) & 1;
             }
@@ -965,9 +984,9 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 
             // S^T[token][head] = K . Q^T
             // two accumulator chains (even / odd k-steps) for MMA latency hiding
-            float s[NT][4], s2[NT][4];
+            float s[NTW][4], s2[NTW][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
 #pragma unroll
@@ -975,7 +994,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(kp + k_frag_off<LAYOUT>(lane, kk), a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
+                for (int nt = 0; nt < NTW; ++nt) {
                     if (kk & 1)
                         mma_16816<BF>(s2[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
                     else
@@ -983,7 +1002,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
 
@@ -991,7 +1010,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
             // stage back to the producer, before the softmax and P.V, so the
             // stage is refilled while they run (two n-tiles have no registers
             // to spare and load V in the P.V loop).
-            constexpr bool kEarlyV = NT == 1;
+            constexpr bool kEarlyV = NTW == 1;
             uint32_t vf[kEarlyV ? KT : 1][4];
             if constexpr (kEarlyV) {
 #pragma unroll
@@ -1008,10 +1027,10 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
 
             // logits, online softmax, P as B fragments of P.V
             const int tlo = tok0 + r;  // this thread's tokens: tlo (e=0,1), tlo+8 (e=2,3)
-            uint32_t pb[NT][2], pbl[NT][2];
-            float z[NT][4];
+            uint32_t pb[NTW][2], pbl[NTW][2];
+            float z[NTW][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float v = s[nt][e] * p.scale;
@@ -1027,9 +1046,9 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                     if (t1 < klo[nt][1] || t1 > khi[nt][1]) z[nt][3] = -INFINITY;
                 }
             }
-            softmax_page<NT, KT, C::kMQ>(z, m, mx, l, acc, edge);
+            softmax_page<NTW, KT, C::kMQ>(z, m, mx, l, acc, edge);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < NTW; ++nt) {
                 const float p0 = z[nt][0], p1 = z[nt][1], p2 = z[nt][2], p3 = z[nt][3];
                 const uint32_t x0 = pack2<BF>(p0, p1);  // token r,   heads 2cq, 2cq+1
                 const uint32_t x1 = pack2<BF>(p2, p3);  // token r+8
@@ -1059,7 +1078,7 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                     ldsm_x4_trans(vp + v_frag_off<LAYOUT>(lane, mt), a0, a1, a2, a3);
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
+                for (int nt = 0; nt < NTW; ++nt) {
                     mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                     if constexpr (BF) mma_16816<BF>(acc[mt][nt], a0, a1, a2, a3, pbl[nt][0], pbl[nt][1]);
                 }
@@ -1071,18 +1090,18 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
         }
 
         // this warp's partial state -> shared memory
-        settle_max<NT, KT>(m, mx, l, acc);
+        settle_max<NTW, KT>(m, mx, l, acc);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
                 l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], o);
                 l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], o);
             }
         }
-        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+        float* mw = sm.merge + warp * C::kMergeRows * C::kMergeStride;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
             const int h0 = nt * 8 + 2 * cq;
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
@@ -1093,8 +1112,8 @@ __device__ void consumer_mma(const Params& p, const Smem& sm, int warp, int lane
                 mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
             }
             if (r == 0) {
-                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
-                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+                sm.ml[warp * C::kMergeRows + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMergeRows + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
             }
         }
         if (!consumer_sync(sm, mphase, lane)) {  // all partial states written
@@ -1442,7 +1461,7 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], o);
             }
         }
-        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+        float* mw = sm.merge + warp * C::kMergeRows * C::kMergeStride;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int h0 = nt * 8 + 2 * cq;
@@ -1457,8 +1476,8 @@ __device__ void consumer_mma_fp8(const Params& p, const Smem& sm, int warp, int 
                 mw[(h0 + 1) * C::kMergeStride + d1] = acc[mt][nt][3];
             }
             if (r == 0) {
-                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
-                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+                sm.ml[warp * C::kMergeRows + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMergeRows + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
             }
         }
         if (!consumer_sync(sm, mphase, lane)) {
@@ -1735,7 +1754,7 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
             if (lane == 0) mbar_arrive(sm.empty + st * 8);
         }
 
-        float* mw = sm.merge + warp * C::kMaxG * C::kMergeStride;
+        float* mw = sm.merge + warp * C::kMergeRows * C::kMergeStride;
         settle_max<NT, MT>(m, mx, l, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -1754,8 +1773,8 @@ __device__ void consumer_tf32(const Params& p, const Smem& sm, int warp, int lan
                 mw[(h0 + 1) * C::kMergeStride + d0 + 8] = acc[mt][nt][3];
             }
             if (r == 0) {
-                sm.ml[warp * C::kMaxG + h0] = make_float2(m[nt][0], l[nt][0]);
-                sm.ml[warp * C::kMaxG + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
+                sm.ml[warp * C::kMergeRows + h0] = make_float2(m[nt][0], l[nt][0]);
+                sm.ml[warp * C::kMergeRows + h0 + 1] = make_float2(m[nt][1], l[nt][1]);
             }
         }
         if (!consumer_sync(sm, mphase, lane)) {
@@ -1812,7 +1831,7 @@ __global__ void __launch_bounds__((NC + 1) * 32,
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(sm.full + s * 8, 1);
-            mbar_init(sm.empty + s * 8, 1);
+            mbar_init(sm.empty + s * 8, C::kPageWarps);
         }
         for (int s = 0; s < C::kTD; ++s) {
             mbar_init(sm.td_full + s * 8, 1);

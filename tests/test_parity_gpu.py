@@ -113,6 +113,8 @@ EDGE = [
     ("group8", "f16", "nhd", 16, 2, 128, (300, 1500), True, 0.0, 1.0),
     ("group9_two_ntiles", "f16", "split", 18, 2, 128, (33, 900), False, 0.0, 1.0),
     ("group16", "bf16", "nhd", 32, 2, 128, (1, 2000), False, 20.0, 2.0),
+    ("group12_split_alibi_softcap", "f16", "split", 24, 2, 128, (15, 513, 1700), True, 30.0, 2.0),
+    ("group16_head64_split", "bf16", "split", 32, 2, 64, (16, 1030), False, 0.0, 1.0),
     ("head64_f16", "f16", "split", 8, 4, 64, (17, 530, 1200), True, 0.0, 1.0),
     ("head64_bf16_nhd", "bf16", "nhd", 6, 3, 64, (5, 1030), False, 10.0, 3.0),
     ("f32_head128", "f32", "split", 6, 2, 128, (40, 555), True, 0.0, 1.0),
