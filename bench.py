@@ -214,7 +214,7 @@ class Setup:
     KV pools that the steps rotate through, so the bytes touched between two
     uses of a pool exceed 4x the L2 size."""
 
-    def __init__(self, w, mode_arg, dev, pa, counters=True, dynamic=True):
+    def __init__(self, w, mode_arg, dev, pa, counters=True, dynamic=True, metadata_ready=True):
         import torch
         self.w, self.dev = w, dev
         cdt = w.cache_dtype
@@ -242,7 +242,11 @@ class Setup:
                       alibi_slopes=self.al, softcap=w.softcap, layout=w.layout, mode=mode_arg,
                       dev_error=self.err, query_start=self.qs,
                       max_query_len=None if self.qs is None else w.max_query_len,
-                      seq_lens_host=w.seq_lens, **self.ws)
+                      seq_lens_host=w.seq_lens,
+                      # block tables and lengths are written once here, never by a
+                      # kernel in the stream: the kernel may read them early
+                      metadata_ready=metadata_ready, **self.ws)
+        self.metadata_ready = metadata_ready
         self.cargs = [pa.make_args(self.out, self.q, self.kcs[i], self.vcs[i], self.bt, self.sl, **common)
                       for i in range(self.copies)]
         # what one call runs (mode, in-kernel merge, kernels per call), as the library plans it
@@ -384,6 +388,7 @@ def config_record(w, S, r, args, world):
             if plan["mode"] == "v2" else "none (v1)",
             "partition_grid": plan["grid"], "ctas_per_sm": plan["ctas_per_sm"],
             "schedule": "dynamic" if plan["dynamic_schedule"] else "static",
+            "metadata_ready": S.metadata_ready,
             "kv_bytes_per_step": w.kv_bytes, "total_bytes_per_step": total_bytes(w, S, plan["mode"]),
             "l2": f"rotate {S.copies} KV pools ({S.copies * S.pool_bytes} B >= 4x L2 {S.l2} B)"
             if S.copies * S.pool_bytes >= 4 * S.l2 else f"{S.copies} KV pools of {S.pool_bytes} B",
@@ -420,7 +425,8 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = peaks()
 
     w = W.make_workload(args.config, args.layout)
-    S = Setup(w, args.mode, dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic")
+    S = Setup(w, args.mode, dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic",
+              metadata_ready=args.metadata == "ready")
     r = measure(S, args.steps, args.warmup, world, soak, sampler)
     kv = w.kv_bytes
     value = whole_job_gbs(kv, world, r["ms_step"])
@@ -482,7 +488,8 @@ def run_ours(args, world, rank, local):
     secondary = None
     if not args.no_secondary and args.config != SECONDARY:
         w2 = W.make_workload(SECONDARY, "split")
-        S2 = Setup(w2, "auto", dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic")
+        S2 = Setup(w2, "auto", dev, pa, counters=args.merge == "auto", dynamic=args.schedule == "dynamic",
+                   metadata_ready=args.metadata == "ready")
         r2 = measure(S2, args.steps, args.warmup, world, soak, sampler)
         v2 = whole_job_gbs(w2.kv_bytes, world, r2["ms_step"])
         secondary = {SECONDARY: {
@@ -620,6 +627,9 @@ def main(argv=None):
     ap.add_argument("--schedule", default="dynamic", choices=("dynamic", "static"),
                     help="dynamic: pass tile counters (tiles claimed by whichever CTA is free); "
                          "static: the round-robin schedule")
+    ap.add_argument("--metadata", default="ready", choices=("ready", "late"),
+                    help="ready: block tables and lengths are final when a step is enqueued (the "
+                         "kernel reads them before waiting for the previous kernel); late: after")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",

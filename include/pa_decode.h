@@ -207,6 +207,15 @@ typedef struct pa_decode_args {
      * leaves both at zero; after a PA_DEVERR_TIMEOUT the caller must zero
      * them.  Calls that share them must not overlap on the GPU. */
     int32_t* tile_counters;
+    /* 1: block_tables, seq_lens and query_start are final when pa_decode is
+     * enqueued -- no kernel earlier in the stream writes them (a host copy
+     * before the call is fine).  The partition kernel then reads them, and
+     * walks to its first tile, before it waits for the previous kernel in the
+     * stream (programmatic dependent launch), so that wait no longer covers a
+     * round trip to memory.  The query, the caches and the workspace are still
+     * touched only after that wait.  0 (a zero-initialised struct): every
+     * input is read after the wait. */
+    int32_t metadata_ready;
 } pa_decode_args;
 
 /* Largest partition count per sequence for which the merge runs inside the

@@ -127,7 +127,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
               window_left: int = -1, kv_dtype: str | None = None, k_scale: float = 1.0,
               v_scale: float = 1.0, query_start=None,
               max_query_len: int | None = None, seq_lens_host=None,
-              tile_counters=None) -> _abi.PaDecodeArgs:
+              tile_counters=None, metadata_ready: bool = False) -> _abi.PaDecodeArgs:
     """Build the C argument struct.  The library validates sizes and types it can
     see; this also checks what only the tensors know: the caches' element size
     and element count against kv_dtype, head_size and num_kv_heads.
@@ -142,7 +142,9 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
     seq_lens: numpy array or CPU tensor) lets mode "auto" choose by the actual
     lengths; the struct keeps a reference to it.  tile_counters (int32 [2],
     zeroed once, e.g. from alloc_workspace(..., tile_counters=True)) turns on
-    the dynamic tile schedule."""
+    the dynamic tile schedule.  metadata_ready promises that no earlier kernel
+    in the stream writes block_tables, seq_lens or query_start (the kernel may
+    read them before it waits for that kernel)."""
     num_rows, num_heads, head_size = query.shape
     num_seqs = seq_lens.shape[0]
     if tuple(out.shape) != tuple(query.shape):
@@ -189,7 +191,7 @@ def make_args(out, query, key_cache, value_cache, block_tables, seq_lens, *, num
         query_start=_ptr(query_start), num_query_tokens=num_rows if query_start is not None else 0,
         max_query_len=int(max_query_len) if query_start is not None else 0,
         seq_lens_host=None if host_lens is None else host_lens.ctypes.data,
-        tile_counters=_ptr(tile_counters),
+        tile_counters=_ptr(tile_counters), metadata_ready=1 if metadata_ready else 0,
     )
     a._keep_host_lens = host_lens  # the pointer above stays valid as long as the struct lives
     return a

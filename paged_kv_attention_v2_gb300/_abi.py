@@ -79,6 +79,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("max_query_len", ctypes.c_int32),
         ("seq_lens_host", ctypes.c_void_p),
         ("tile_counters", ctypes.c_void_p),
+        ("metadata_ready", ctypes.c_int32),
     ]
 
 

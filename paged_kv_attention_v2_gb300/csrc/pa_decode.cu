@@ -279,6 +279,7 @@ pa_status prepare(const pa_decode_args* a, void* stream, Prepared& pr) {
     p.wait_limit_ns = (uint64_t)g_wait_limit_ns.load();
     p.withhold_page = g_withhold_page.load();
     p.tile_ctr = nullptr;  // set below once the mode is known
+    p.metadata_ready = a->metadata_ready ? 1 : 0;
 
     pa::LaunchArgs& la = pr.la;
     std::memset(&la, 0, sizeof la);

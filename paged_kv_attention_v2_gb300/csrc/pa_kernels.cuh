@@ -85,6 +85,7 @@ struct Params {
     int withhold_page;       // test hook: CTA 0 withholds its first page copy (a wait runs out)
     int kv_evict_first;      // KV page copies marked evict_first (partition outputs small against L2)
     int32_t* tile_ctr;       // [2] dynamic schedule: tiles claimed, CTAs done (NULL: static schedule)
+    int metadata_ready;      // block tables / lengths / query_start final: read before the grid wait
 };
 
 struct TileDesc {
@@ -345,6 +346,10 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
             spec_ids = __ldg(p.block_tables + (int64_t)spec_seq * p.max_blocks_per_seq + idx);
     }
     load_chunk(0);
+    // Final metadata: lengths and block ids are read before the wait for the
+    // previous grid, which must be done before the grid-wide tile counter
+    // (dynamic schedule: here), the copies and the workspace are touched.
+    if (p.metadata_ready && p.tile_ctr) pdl_wait_primary();
 
     // Tiles of this CTA (kv head fastest): blockIdx.x, then blockIdx.x +
     // gridDim.x, ... (static schedule) or, with tile counters, whatever tile
@@ -415,6 +420,7 @@ __device__ void producer(const Params& p, const Smem& sm, const CUtensorMap* tmk
     ProducerTile cur = next_tile();
     int ids = check_ids((cur.valid && cur.seq == spec_seq && cur.tb == spec_tb) ? (lane < cur.npages ? spec_ids : 0)
                                                                                   : load_ids(cur, 0));
+    if (p.metadata_ready && !p.tile_ctr) pdl_wait_primary();  // static schedule: first tile found
     while (ok && cur.valid) {
         // The next tile is walked to, and its first block ids loaded, only once
         // the first batch of this tile's copies is out (the walk may load
@@ -1851,7 +1857,11 @@ __global__ void __launch_bounds__((NC + 1) * 32,
     }
     __syncthreads();
     pdl_launch_dependents();  // the reduce kernel may be scheduled; it waits for our completion
-    pdl_wait_primary();       // earlier work in the stream (inputs, workspace readers) is done
+    // Earlier work in the stream (inputs, workspace readers) must be done.
+    // With final metadata only the producer waits, once it has its first tile
+    // (producer); every other warp reaches global memory only after that
+    // through the producer's barriers.
+    if (!p.metadata_ready) pdl_wait_primary();
 
     if (warp == NC) {
         producer<C, HEAD, STAGES>(p, sm, &tmk, &tmv, lane);

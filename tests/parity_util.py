@@ -47,13 +47,15 @@ def to_device(w, device="cuda:0"):
 
 
 def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_lens=None,
-            block_tables=None, poison_workspace=True, counters=None, calls=1):
+            block_tables=None, poison_workspace=True, counters=None, calls=1, metadata_ready=False):
     """Run pa_decode on device; returns dict of float64 numpy arrays + dev_error.
 
     mode "v2f" is v2 with partition counters (the merge inside the partition
     kernel where the library's rule allows it); `counters` may pass an
     existing counter tensor, which must be all zero again after every call.
-    The result holds the library's plan of the call ("plan")."""
+    metadata_ready lets the kernel read the block tables and lengths before it
+    waits for the previous kernel in the stream.  The result holds the
+    library's plan of the call ("plan")."""
     dev = dev or to_device(w, device)
     fused = mode == "v2f"
     if fused:
@@ -81,7 +83,8 @@ def run_gpu(w, mode="auto", device="cuda:0", dev=None, max_seq_len=None, seq_len
                 seq_lens_host=w.seq_lens if mode == "auto" else None,
                 window_left=getattr(w, "window_left", -1),
                 kv_dtype=getattr(w, "kv_dtype", None), k_scale=getattr(w, "k_scale", 1.0),
-                v_scale=getattr(w, "v_scale", 1.0), tile_counters=tctr, **mq, **ws)
+                v_scale=getattr(w, "v_scale", 1.0), tile_counters=tctr,
+                metadata_ready=metadata_ready, **mq, **ws)
     tensors = (out, dev["query"], dev["key_cache"], dev["value_cache"],
                dev["block_tables"] if block_tables is None else block_tables,
                dev["seq_lens"] if seq_lens is None else seq_lens)

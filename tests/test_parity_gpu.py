@@ -351,6 +351,37 @@ def test_multi_token_bad_query_start_is_flagged_not_faulted():
     check_out(w, g["out"][:2], ref["out"][:2])  # sequence 0 is untouched
 
 
+EARLY = [
+    # name, dtype, kv, layout, H, Hkv, lens, q_len, window_left, mode
+    ("early_uniform_v2", "f16", None, "split", 28, 4, (2048,) * 40, None, -1, "v2"),
+    ("early_ragged_dynamic", "bf16", None, "nhd", 16, 4, tuple(17 + 331 * i for i in range(48)), None, -1,
+     "auto"),
+    ("early_fused_one_round", "f16", None, "split", 8, 2, (1025, 3000, 77, 0), None, -1, "v2f"),
+    ("early_v1_window", "bf16", None, "split", 8, 2, (300, 1500, 2600), None, 700, "v1"),
+    ("early_tokens_fp8", "f16", "e4m3", "split", 8, 2, (600, 1300, 2049), [2, 1, 3], -1, "v2"),
+]
+
+
+@pytest.mark.parametrize("case", EARLY, ids=[c[0] for c in EARLY])
+def test_metadata_ready_reads_before_the_grid_wait(case):
+    """metadata_ready: the partition kernel reads block tables and lengths
+    (and walks to its first tile) before it waits for the previous kernel in
+    the stream.  Three calls back to back, so each starts while the previous
+    call's kernels run: outputs and statistics against the oracle, the
+    counters back at zero (static, dynamic and in-kernel-merge paths, v1)."""
+    name, dtype, kv, layout, H, Hkv, lens, ql, wl, mode = case
+    spec = W.small_spec(name=name, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_size=128,
+                        dtype=dtype, seq_lens=lens, q_len=ql, kv_dtype=kv)
+    w = W.make_workload(spec, layout)
+    w.window_left = wl
+    ref = oracle.oracle_decode(w)
+    g = run_gpu(w, mode=mode, calls=3, metadata_ready=True)
+    assert g["dev_error"] == 0
+    check_out(w, g["out"], ref["out"])
+    if g["plan"]["mode"] == "v2":
+        check_stats(w, g, ref)
+
+
 @pytest.mark.parametrize("mode", ["v1", "v2"])
 def test_cuda_graph_capture_replays_the_same_result(mode):
     """pa_decode allocates nothing and never synchronises, so a CUDA graph can
