@@ -164,6 +164,35 @@ def test_null_args(lib):
     assert lib.pa_decode(None, None) == _abi.PA_ERR_INVALID_ARG
 
 
+def test_binding_struct_layouts_match_the_header(tmp_path):
+    """The ctypes structs mirror include/pa_decode.h field by field: size and
+    every field offset, as a C compiler lays them out (no GPU)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = pathlib.Path(__file__).resolve().parents[1] / "include"
+    lines = ['#include <stdio.h>', '#include "pa_decode.h"', "int main(void) {"]
+    for cname, cls in (("pa_decode_args", _abi.PaDecodeArgs), ("pa_launch_plan", _abi.PaLaunchPlan)):
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", str(inc), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        name, field, val = line.split()
+        got[(name, field)] = int(val)
+    for cname, cls in (("pa_decode_args", _abi.PaDecodeArgs), ("pa_launch_plan", _abi.PaLaunchPlan)):
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(_abi.LibraryMissing):
         _abi.load(tmp_path / "missing.so")
