@@ -34,7 +34,8 @@ def _workload(name, layout):
 FULL = [("tiny", "split"), ("tiny", "nhd"), ("gqa4k", "split"), ("gqa4k", "nhd"),
         ("long100k", "split"), ("long100k", "nhd"), ("ragged", "split"), ("ragged", "nhd"),
         ("gqa4k_fp8", "split"), ("gqa4k_fp8", "nhd"), ("long100k_fp8", "split"),
-        ("long100k_fp8", "nhd"), ("spec4k", "split"), ("spec4k", "nhd")]
+        ("long100k_fp8", "nhd"), ("spec4k", "split"), ("spec4k", "nhd"), ("spec4k_fp8", "split"),
+        ("spec4k_fp8", "nhd")]
 
 
 @pytest.mark.parametrize("name,layout", FULL, ids=[f"{n}-{l}" for n, l in FULL])

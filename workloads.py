@@ -92,6 +92,9 @@ SPECS = {
     # several query tokens per sequence (speculative decoding: 4 drafted tokens
     # verified at once): 32 x 4096, 32/8 heads (group 4, 16 rows per tile)
     "spec4k": Spec("spec4k", 32, 32, 8, 128, "bf16", seq_len=4096, seed_index=7, q_len=4),
+    # the same with an fp8 e4m3 KV cache
+    "spec4k_fp8": Spec("spec4k_fp8", 32, 32, 8, 128, "bf16", seq_len=4096, seed_index=10, q_len=4,
+                       kv_dtype="e4m3", k_scale=2.0 ** -6, v_scale=2.0 ** -6),
     # fp32 query and cache: the 4K and 100K shapes (tf32 tensor-core path, 1e-5 tolerance)
     "gqa4k_f32": Spec("gqa4k_f32", 32, 28, 4, 128, "f32", seq_len=4096, seed_index=8),
     "long100k_f32": Spec("long100k_f32", 4, 28, 4, 128, "f32", seq_len=100000, seed_index=9),
@@ -106,6 +109,7 @@ DESCRIPTIONS = {
     "gqa4k_fp8": "GQA decode, fp8 e4m3 KV cache (scales 2^-6): 32 seqs x 4096, 28/4 heads, d=128, fp16 query",
     "long100k_fp8": "long context, fp8 e4m3 KV cache (scales 2^-6): 4 seqs x 100000, 28/4 heads, d=128, bf16 query",
     "spec4k": "speculative decode: 32 seqs x 4096 with 4 query tokens each (causal), 32/8 heads, d=128, bf16",
+    "spec4k_fp8": "speculative decode, fp8 e4m3 KV cache (scales 2^-6): 32 seqs x 4096 with 4 query tokens each, 32/8 heads, d=128, bf16 query",
     "gqa4k_f32": "GQA decode, fp32 query and KV: 32 seqs x 4096, 28/4 heads, d=128",
     "long100k_f32": "long context, fp32 query and KV: 4 seqs x 100000, 28/4 heads, d=128",
 }
