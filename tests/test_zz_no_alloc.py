@@ -96,7 +96,9 @@ def test_static_workspace_matches_pa_decode_on_two_calls(case):
         layout={"split": 0, "nhd": 1}[w.layout], mode=_abi.PA_MODE_AUTO, dev_error=err.data_ptr(),
         query_start=dev["query_start"].data_ptr() if multi else None,
         num_query_tokens=w.num_query_tokens if multi else 0,
-        max_query_len=w.max_query_len if multi else 0)
+        max_query_len=w.max_query_len if multi else 0,
+        # the multi-token case also reads its metadata before the grid wait
+        metadata_ready=1 if multi else 0)
     stream = torch.cuda.current_stream().cuda_stream
 
     # Leave NaN in every entry of the array the checked calls can touch: a call
